@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 mixed-granularity linear-layer hot path on GB300.
+
+One step = the forward and backward of the four Llama-3.1-8B layer linears at
+M = 8192 training tokens (QKV 4096→6144, O 4096→4096, gate/up 4096→28672,
+down 14336→4096) through the jetfp8 C ABI:
+  RMSNorm+1×128 quant (QKV and gate/up inputs) or 1×128 quant (O and down),
+  128×128 weight quant with the transposed payload, FProp, dual gradient
+  quant, DGrad, 1×128→128×1 requantise-transpose, WGrad.
+Inputs are seeded synthetic bf16 tensors with the distributions of the Jet-RL
+workloads; together they exceed the 129 MB L2 many times over, so no L2 flush
+is needed between steps.
+
+metric  FP8 block-scaled GEMM TFLOP/s: the step's GEMM FLOPs (3 × 2·M·N·K per
+        linear) divided by the whole step's time (quantisers included), summed
+        over ranks.
+Also reported: each kernel family's own TFLOP/s or GB/s from CUDA events around
+every launch, the roofline of the dominant kernel, the CPU oracle on a bounded
+sample, and the same metric end to end from pinned host memory.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) every rank runs the same single-GPU step on its own
+GPU (replicas: the path needs no collective); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 block-scaled GEMM TFLOP/s (% dense-FP8 peak); quant kernels GB/s (% HBM)"
+WORKLOAD = "llama3.1-8b-training-linears"
+REF_ROWS, REF_COLS = 128, 1024       # CPU sample: 128 tokens × 1024 output features per linear
+
+# algorithmic bytes per element of each quantiser (inputs read + outputs written)
+QUANT_BYTES = {
+    "quant_act": 2 + 1 + 4 / 128,
+    "rmsnorm_quant": 2 + 1 + 4 / 128,
+    "quant_weight": 2 + 1 + 1 + 4 / 16384,
+    "quant_grad_dual": 2 + 2 * (1 + 4 / 128),
+    "requant": 1 + 4 / 128 + 1 + 4 / 128,
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"],
+                "bf16_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        smax = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle sample (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------
+def oracle_sample_step(lins, seed=0):
+    """The whole path for a 128-token × 1024-output-feature slice of every
+    linear, on the CPU oracle.  Returns the GEMM FLOPs it performed."""
+    from fp8_mixed_granularity_gb300 import workloads as W
+    from oracle import jetfp8_oracle as O
+    flops = 0
+    for i, lin in enumerate(lins):
+        m, n, k = REF_ROWS, min(REF_COLS, lin.N), lin.K
+        x = W.bf16_values(W.activations(m, k, seed=seed, stream=10 + i))
+        w = W.bf16_values(W.weights(n, k, seed=seed, stream=20 + i))
+        dy = W.bf16_values(W.gradients(m, n, seed=seed, stream=30 + i))
+        xq, sx = O.quant_act_1x128(x)
+        wq, sw, wqT = O.quant_weight_128x128(w)
+        O.gemm_fprop(xq, sx, wq, sw)
+        dq, ds, dqT, dsT = O.quant_grad_dual(dy)
+        O.gemm_dgrad(dq, ds, wqT, sw)
+        xqT, sxT = O.requant_rowgrp_to_colgrp(xq, sx)
+        O.gemm_wgrad(dqT, dsT, xqT, sxT)
+        flops += 3 * 2 * m * n * k
+    return flops
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def time_oracle(lins, steps):
+    t0 = time.perf_counter()
+    flops = 0
+    for s in range(steps):
+        flops += oracle_sample_step(lins, seed=s)
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, flops
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle, timed as it stands
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from fp8_mixed_granularity_gb300 import workloads as W
+    lins = W.llama8b_training()
+    for s in range(args.warmup):
+        oracle_sample_step(lins, seed=1000 + s)
+    value, dt, flops = time_oracle(lins, args.steps)
+    sample = (f"per step: the full path (quantisers + FProp/DGrad/WGrad) for {REF_ROWS} tokens × "
+              f"{REF_COLS} output features of each of the 4 linears")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": 8192, "linears": [l.name for l in lins],
+                   "l2": "inputs larger than L2"},
+        "cpu_baseline": {"kind": "oracle", "value": value, "unit": "TFLOP/s", "cores": cpu_threads(),
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__ as g
+    if rank == 0:
+        g.build()
+    if world > 1:
+        torch.distributed.barrier()
+    g.build()
+    from fp8_mixed_granularity_gb300 import jetfp8 as J
+    from fp8_mixed_granularity_gb300 import workloads as W
+    from fp8_mixed_granularity_gb300.linear import LinearBuffers
+
+    lins = W.llama8b_training()
+    norm_fed = {"qkv", "gate_up"}
+    bufs, inputs = [], []
+    for i, lin in enumerate(lins):
+        b = LinearBuffers(lin, dev, rmsnorm=lin.name in norm_fed)
+        x = W.device_activations(lin.M, lin.K, dev, seed=100 + i + 10 * rank)
+        w = W.device_normal((lin.N, lin.K), 0.02, dev, seed=200 + i + 10 * rank)
+        dy = W.device_normal((lin.M, lin.N), 1e-3, dev, seed=300 + i + 10 * rank)
+        gamma = W.device_uniform((lin.K,), 0.5, 1.5, dev, seed=400 + i) if b.rmsnorm else None
+        bufs.append(b)
+        inputs.append((x, w, dy, gamma))
+    gemm_flops = sum(3 * l.gemm_flops for l in lins)
+
+    def step(events=None):
+        n = 0
+        for b, (x, w, dy, gamma) in zip(bufs, inputs):
+            n += b.forward(x, w, gamma, events=events)
+            n += b.backward(dy, events=events)
+        return n
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    J.jetfp8_get_last_device_error()
+
+    # --- timed region: whole steps, CUDA events on the launching stream ---
+    sampler = ClockSampler(local)
+    events = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    launches = 0
+    for _ in range(args.steps):
+        launches += step(events)
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    J.jetfp8_get_last_device_error()
+    ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # per-GEMM-kind times from the events inside the timed region
+    gemm_ms = {}
+    for name, s, e in events:
+        gemm_ms[name] = gemm_ms.get(name, 0.0) + s.elapsed_time(e)
+    gemm_total_ms = sum(gemm_ms.values()) / args.steps
+
+    # --- quantiser breakdown: one extra pass with events around each quantiser ---
+    quant = quant_breakdown(bufs, inputs, J, torch)
+
+    # --- end to end from pinned host memory ---
+    e2e = None if args.no_e2e else run_e2e(bufs, inputs, args, torch, gemm_flops, world)
+
+    peaks = measured_peaks()
+    fp8_peak_sustained = 2.0 * peaks["bf16_sustained"]   # dense fp8 = 2 × bf16 (nominal ratio)
+    gemm_tflops = gemm_flops / (gemm_total_ms * 1e-3) / 1e12
+    value = gemm_flops * world / (ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": 8192, "linears": {l.name: [l.K, l.N] for l in lins},
+                   "step": "fwd+bwd of the 4 linears incl. all quantisers", "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "roofline": {
+            "kernel": "k_gemm_e4m3_blockscaled", "bound": "tensor", "achieved": gemm_tflops,
+            "peak": fp8_peak_sustained, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_sustained,
+            "traffic": None,
+            "peak_note": f"2 x {peaks['source']} sustained bf16 cuBLAS ({peaks['bf16_sustained']} TFLOP/s)",
+        },
+        "breakdown": {
+            "gemm_tflops": {k: sum(l.gemm_flops for l in lins) / (v / args.steps * 1e-3) / 1e12
+                            for k, v in gemm_ms.items()},
+            "gemm_ms_per_step": gemm_total_ms,
+            "quant": quant,
+            "hbm_peak_gbs": peaks["hbm_gbs"],
+        },
+        "clocks": clocks,
+        "gpu_launches": launches,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cv, cdt, cfl = time_oracle(lins, 2)
+        line["cpu_baseline"] = {
+            "value": cv, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": (f"2 steps of the full path on {REF_ROWS} tokens × {REF_COLS} output features of "
+                       f"each of the 4 linears ({cfl / 1e9:.1f} GFLOP in {cdt:.1f} s)")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def quant_breakdown(bufs, inputs, J, torch):
+    """GB/s of each quantiser kind from CUDA events around its launches (one
+    pass over the 4 linears, after the timed steps)."""
+    from fp8_mixed_granularity_gb300.linear import _timed
+    ev = []
+    bytes_by = {}
+    for b, (x, w, dy, gamma) in zip(bufs, inputs):
+        t, lin = b.t, b.lin
+        M, K, N = lin.M, lin.K, lin.N
+        if b.rmsnorm:
+            _timed(ev, "rmsnorm_quant", lambda: J.jetfp8_rmsnorm_quant(x, gamma, 1e-6, t["xq"], t["sx"], t["rstd"]))
+            bytes_by.setdefault("rmsnorm_quant", 0.0)
+            bytes_by["rmsnorm_quant"] += M * K * QUANT_BYTES["rmsnorm_quant"] + 2 * K + 4 * M
+        else:
+            _timed(ev, "quant_act", lambda: J.jetfp8_quant_act_1x128(x, t["xq"], t["sx"]))
+            bytes_by["quant_act"] = bytes_by.get("quant_act", 0.0) + M * K * QUANT_BYTES["quant_act"]
+        _timed(ev, "quant_weight", lambda: J.jetfp8_quant_weight_128x128(w, t["wq"], t["sw"], t["wqT"]))
+        bytes_by["quant_weight"] = bytes_by.get("quant_weight", 0.0) + N * K * QUANT_BYTES["quant_weight"]
+        _timed(ev, "quant_grad_dual", lambda: J.jetfp8_quant_grad_dual(dy, t["dyq"], t["sdy"], t["dyqT"], t["sdyT"]))
+        bytes_by["quant_grad_dual"] = bytes_by.get("quant_grad_dual", 0.0) + M * N * QUANT_BYTES["quant_grad_dual"]
+        _timed(ev, "requant", lambda: J.jetfp8_requant_rowgrp_to_colgrp(t["xq"], t["sx"], t["xqT"], t["sxT"]))
+        bytes_by["requant"] = bytes_by.get("requant", 0.0) + M * K * QUANT_BYTES["requant"]
+    torch.cuda.synchronize()
+    ms_by = {}
+    for name, s, e in ev:
+        ms_by[name] = ms_by.get(name, 0.0) + s.elapsed_time(e)
+    return {k: {"gbs": bytes_by[k] / (ms_by[k] * 1e-3) / 1e9, "ms": ms_by[k]} for k in ms_by}
+
+
+def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
+    """Same metric through the public API with host buffers: every step copies
+    its bf16 inputs from pinned host memory to the device and reads Y, ∇X and
+    ∇W back, all inside the timed region."""
+    host_in = [tuple(None if t is None else t.cpu().pin_memory() for t in inp) for inp in inputs]
+    host_out = [tuple(torch.empty_like(b.t[k], device="cpu").pin_memory() for k in ("y", "dx", "dw"))
+                for b in bufs]
+    dev_in = inputs
+    h2d = sum(t.numel() * t.element_size() for inp in host_in for t in inp if t is not None)
+    d2h = sum(t.numel() * t.element_size() for outs in host_out for t in outs)
+
+    def step():
+        for b, hi, di, ho in zip(bufs, host_in, dev_in, host_out):
+            for hsrc, ddst in zip(hi, di):
+                if hsrc is not None:
+                    ddst.copy_(hsrc, non_blocking=True)
+            x, w, dy, gamma = di
+            b.forward(x, w, gamma)
+            b.backward(dy)
+            for k, hdst in zip(("y", "dx", "dw"), ho):
+                hdst.copy_(b.t[k], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    steps = max(2, args.steps // 2)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    if world > 1:
+        tt = torch.tensor([ms], device=bufs[0].device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    return {"value": gemm_flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,239 @@
+// C ABI of the jetfp8 library: argument validation, per-device set-up and the
+// dispatch of each entry point to its kernel.  Declarations and the contract
+// of every function are in include/jetfp8.h.
+#include <mutex>
+
+#include "jetfp8_common.cuh"
+#include "jetfp8_internal.h"
+
+namespace jetfp8 {
+
+// One error word per device, written by kernels whose bounded waits expire.
+__device__ unsigned g_device_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::once_flag once;
+  unsigned* err_word = nullptr;
+  int sms = 0;
+  bool sm103 = false;
+  bool ok = false;
+};
+DeviceInfo g_devices[kMaxDevices];
+
+DeviceInfo* current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo* d = &g_devices[dev];
+  std::call_once(d->once, [d, dev]() {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return;
+    d->sms = prop.multiProcessorCount;
+    d->sm103 = prop.major == 10 && prop.minor == 3;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return;
+    d->err_word = static_cast<unsigned*>(p);
+    d->ok = true;
+  });
+  return d->ok ? d : nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+jetfp8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? JETFP8_OK : JETFP8_ERR_CUDA; }
+
+// Validation helpers ---------------------------------------------------------
+struct Check {
+  jetfp8_status st = JETFP8_OK;
+  Check& ptr(const void* p, bool required = true) {
+    if (st != JETFP8_OK) return *this;
+    if (p == nullptr) {
+      if (required) st = JETFP8_ERR_INVALID_ARG;
+    } else if (!aligned16(p)) {
+      st = JETFP8_ERR_MISALIGNED;
+    }
+    return *this;
+  }
+  Check& positive(int64_t v) {
+    if (st == JETFP8_OK && v <= 0) st = JETFP8_ERR_INVALID_ARG;
+    return *this;
+  }
+  Check& mult128(int64_t v) {
+    if (st == JETFP8_OK && (v <= 0 || v % 128 != 0)) st = (v <= 0) ? JETFP8_ERR_INVALID_ARG : JETFP8_ERR_UNSUPPORTED_SHAPE;
+    return *this;
+  }
+  // keep 32-bit index arithmetic inside the kernels safe
+  Check& fits(int64_t a, int64_t b) {
+    if (st == JETFP8_OK && (a > (int64_t(1) << 31) / (b > 0 ? b : 1) || a * b >= (int64_t(1) << 40)))
+      st = JETFP8_ERR_UNSUPPORTED_SHAPE;
+    return *this;
+  }
+  Check& device() {
+    if (st != JETFP8_OK) return *this;
+    DeviceInfo* d = current_device();
+    if (d == nullptr) st = JETFP8_ERR_CUDA;
+    else if (!d->sm103) st = JETFP8_ERR_UNSUPPORTED;
+    return *this;
+  }
+};
+
+}  // namespace
+
+unsigned* device_error_word() {
+  DeviceInfo* d = current_device();
+  return d ? d->err_word : nullptr;
+}
+
+int num_sms() {
+  DeviceInfo* d = current_device();
+  return (d && d->sms > 0) ? d->sms : 1;
+}
+
+bool device_is_sm103() {
+  DeviceInfo* d = current_device();
+  return d && d->sm103;
+}
+
+}  // namespace jetfp8
+
+using namespace jetfp8;
+
+extern "C" {
+
+const char* jetfp8_status_string(jetfp8_status st) {
+  switch (st) {
+    case JETFP8_OK: return "JETFP8_OK";
+    case JETFP8_ERR_INVALID_ARG: return "JETFP8_ERR_INVALID_ARG";
+    case JETFP8_ERR_UNSUPPORTED_SHAPE: return "JETFP8_ERR_UNSUPPORTED_SHAPE";
+    case JETFP8_ERR_MISALIGNED: return "JETFP8_ERR_MISALIGNED";
+    case JETFP8_ERR_CUDA: return "JETFP8_ERR_CUDA";
+    case JETFP8_ERR_TIMEOUT: return "JETFP8_ERR_TIMEOUT";
+    case JETFP8_ERR_UNSUPPORTED: return "JETFP8_ERR_UNSUPPORTED";
+  }
+  return "JETFP8_ERR_UNKNOWN";
+}
+
+jetfp8_status jetfp8_get_last_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return JETFP8_ERR_CUDA;
+  if (current_device() == nullptr) return JETFP8_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_device_error_word, sizeof(word)) != cudaSuccess)
+    return JETFP8_ERR_CUDA;
+  if (word == 0) return JETFP8_OK;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero)) != cudaSuccess)
+    return JETFP8_ERR_CUDA;
+  return JETFP8_ERR_TIMEOUT;
+}
+
+jetfp8_status jetfp8_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, uint8_t* q,
+                                     float* s, cudaStream_t stream) {
+  Check c;
+  c.ptr(x_bf16).ptr(q).ptr(s).positive(M).mult128(K).fits(M, K).device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_quant_rowgroups(x_bf16, M, K, q, s, stream));
+}
+
+jetfp8_status jetfp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K, uint8_t* q,
+                                          float* s, uint8_t* qT, cudaStream_t stream) {
+  Check c;
+  c.ptr(w_bf16).ptr(q).ptr(s).ptr(qT, false).mult128(N).mult128(K).fits(N, K).device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_quant_weight(w_bf16, N, K, q, s, qT, stream));
+}
+
+jetfp8_status jetfp8_requant_rowgrp_to_colgrp(const uint8_t* q, const float* s, int64_t M,
+                                              int64_t K, uint8_t* qT, float* sT,
+                                              cudaStream_t stream) {
+  Check c;
+  c.ptr(q).ptr(s).ptr(qT).ptr(sT).mult128(M).mult128(K).fits(M, K).device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_requant_row2col(q, s, M, K, qT, sT, stream));
+}
+
+jetfp8_status jetfp8_quant_grad_dual(const void* dy_bf16, int64_t M, int64_t N, uint8_t* q_row,
+                                     float* s_row, uint8_t* qT_col, float* sT_col,
+                                     cudaStream_t stream) {
+  Check c;
+  c.ptr(dy_bf16).ptr(q_row).ptr(s_row).ptr(qT_col, false).ptr(sT_col, false).positive(M)
+      .mult128(N).fits(M, N).device();
+  if (c.st != JETFP8_OK) return c.st;
+  if ((qT_col == nullptr) != (sT_col == nullptr)) return JETFP8_ERR_INVALID_ARG;
+  if (qT_col != nullptr && M % 128 != 0) return JETFP8_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_quant_grad_dual(dy_bf16, M, N, q_row, s_row, qT_col, sT_col, stream));
+}
+
+jetfp8_status jetfp8_rmsnorm_quant(const void* x_bf16, const void* gamma_bf16, float eps,
+                                   int64_t M, int64_t H, uint8_t* q, float* s, float* rstd,
+                                   void* y_bf16, cudaStream_t stream) {
+  Check c;
+  c.ptr(x_bf16).ptr(gamma_bf16).ptr(q).ptr(s).ptr(rstd).ptr(y_bf16, false).positive(M)
+      .mult128(H).fits(M, H).device();
+  if (c.st != JETFP8_OK) return c.st;
+  if (!(eps >= 0.0f)) return JETFP8_ERR_INVALID_ARG;
+  return from_cuda(launch_rmsnorm_quant(x_bf16, gamma_bf16, eps, M, H, q, s, rstd, y_bf16, stream));
+}
+
+static jetfp8_status gemm_common(const GemmArgs& g, jetfp8_out_dtype dt, cudaStream_t stream) {
+  if (dt != JETFP8_OUT_BF16 && dt != JETFP8_OUT_FP32) return JETFP8_ERR_INVALID_ARG;
+  return from_cuda(launch_gemm(g, stream));
+}
+
+jetfp8_status jetfp8_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq,
+                                const float* sw, int64_t M, int64_t N, int64_t K, void* y,
+                                jetfp8_out_dtype out_dtype, cudaStream_t stream) {
+  Check c;
+  c.ptr(xq).ptr(sx).ptr(wq).ptr(sw).ptr(y).positive(M).mult128(N).mult128(K).fits(M, K)
+      .fits(N, K).fits(M, N).device();
+  if (c.st != JETFP8_OK) return c.st;
+  GemmArgs g{xq, wq, sx, round_up4(M), sw, K / 128, 1, BScale::kBlock,
+             y, out_dtype == JETFP8_OUT_FP32, M, N, K};
+  return gemm_common(g, out_dtype, stream);
+}
+
+jetfp8_status jetfp8_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT,
+                                const float* sw, int64_t M, int64_t N, int64_t K, void* dx,
+                                jetfp8_out_dtype out_dtype, cudaStream_t stream) {
+  Check c;
+  c.ptr(dyq).ptr(sdy).ptr(wqT).ptr(sw).ptr(dx).positive(M).mult128(N).mult128(K).fits(M, N)
+      .fits(N, K).fits(M, K).device();
+  if (c.st != JETFP8_OK) return c.st;
+  // contraction over N (block kb = n/128), output columns over K (block j/128)
+  GemmArgs g{dyq, wqT, sdy, round_up4(M), sw, 1, K / 128, BScale::kBlock,
+             dx, out_dtype == JETFP8_OUT_FP32, M, K, N};
+  return gemm_common(g, out_dtype, stream);
+}
+
+jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,
+                                const float* sxT, int64_t M, int64_t N, int64_t K, void* dw,
+                                jetfp8_out_dtype out_dtype, cudaStream_t stream) {
+  Check c;
+  c.ptr(dyqT).ptr(sdyT).ptr(xqT).ptr(sxT).ptr(dw).mult128(M).mult128(N).mult128(K).fits(M, N)
+      .fits(M, K).fits(N, K).device();
+  if (c.st != JETFP8_OK) return c.st;
+  // contraction over tokens (block kb = m/128); per-row scale sdyT[kb][n], per-column sxT[kb][k]
+  GemmArgs g{dyqT, xqT, sdyT, N, sxT, 0, K, BScale::kColumn,
+             dw, out_dtype == JETFP8_OUT_FP32, N, K, M};
+  return gemm_common(g, out_dtype, stream);
+}
+
+jetfp8_status jetfp8_swiglu_quant(const void* gu_bf16, int64_t M, int64_t I, uint8_t* q, float* s,
+                                  void* h_bf16, cudaStream_t stream) {
+  Check c;
+  c.ptr(gu_bf16).ptr(q).ptr(s).ptr(h_bf16, false).positive(M).mult128(I).fits(M, 2 * I).device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_swiglu_quant(gu_bf16, M, I, q, s, h_bf16, stream));
+}
+
+jetfp8_status jetfp8_swiglu_bwd(const void* gu_bf16, const void* dh_bf16, int64_t M, int64_t I,
+                                void* dgu_bf16, cudaStream_t stream) {
+  Check c;
+  c.ptr(gu_bf16).ptr(dh_bf16).ptr(dgu_bf16).positive(M).mult128(I).fits(M, 2 * I).device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_swiglu_bwd(gu_bf16, dh_bf16, M, I, dgu_bf16, stream));
+}
+
+}  // extern "C"

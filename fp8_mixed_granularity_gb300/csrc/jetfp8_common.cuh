@@ -1,0 +1,124 @@
+// Device helpers shared by the jetfp8 kernels (sm_103a).
+//
+// Quantisation rule (Jet-RL digest "Jet-RL：通过统一训练与推理精度流实现 On-Policy FP8
+// 强化学习", 前置知识 › FP8 量化 (E4M3 格式)): S = max|x|/448 and x̂ = E4M3(x/S).
+// Both quotients are correctly rounded FP32 divisions; the E4M3 cast rounds to
+// nearest even and saturates (cvt.rn.satfinite).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/jetfp8.h"
+
+namespace jetfp8 {
+
+constexpr float kE4M3Max = 448.0f;
+
+// Error bits recorded in the device error word.
+constexpr unsigned kErrTimeout = 1u;
+
+// Host side: device address of this device's error word (set-up once per device).
+unsigned* device_error_word();
+int num_sms();
+bool device_is_sm103();
+
+// -------------------------------------------------------------------------
+// E4M3 quantisation with an exact FP32 quotient
+// -------------------------------------------------------------------------
+struct GroupScale {
+  float s;      // S = fp32(amax/448), or 1 when amax == 0
+  float rs;     // fp32(1/S), for the fast quotient
+  bool exact;   // S is so small that 1/S may overflow: always divide
+};
+
+__device__ __forceinline__ GroupScale make_scale(float amax) {
+  GroupScale g;
+  g.s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, kE4M3Max);
+  g.rs = __frcp_rn(g.s);
+  g.exact = !(g.rs < 1.0e37f);
+  return g;
+}
+
+// fp32(x/S) exactly as a correctly rounded division would give it, as far as
+// the E4M3 code of the result is concerned.  q~ = x·RN(1/S) lies within two
+// FP32 ulps of x/S, so it can sit on the other side of an E4M3 rounding
+// boundary from RN(x/S) only if it is within a few ulps of that boundary.  In
+// the E4M3 normal range (|q| >= 2^-6) the boundaries are the midpoints between
+// neighbouring codes, whose FP32 encodings have the low 20 mantissa bits equal
+// to 0x80000.  Inputs within 4 ulps of such a midpoint, or below 2^-6 (where
+// the boundaries sit elsewhere), take the IEEE division instead.
+__device__ __forceinline__ float quotient(float x, const GroupScale& g) {
+  float q = __fmul_rn(x, g.rs);
+  uint32_t u = __float_as_uint(q);
+  bool near_tie = ((u & 0xFFFFFu) - (0x80000u - 4u)) <= 8u;
+  bool small = (u & 0x7FFFFFFFu) < 0x3C800000u;   // |q| < 2^-6
+  if (near_tie || small || g.exact) q = __fdiv_rn(x, g.s);
+  return q;
+}
+
+// Two FP32 values -> two E4M3 codes; v0 lands in the low byte (lower address).
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float v0, float v1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
+  return (uint32_t)r;
+}
+
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, const GroupScale& g) {
+  return cvt_e4m3x2(quotient(a, g), quotient(b, g)) |
+         (cvt_e4m3x2(quotient(c, g), quotient(d, g)) << 16);
+}
+
+// Two E4M3 codes (low byte first) -> two exact floats.
+__device__ __forceinline__ float2 dec_e4m3x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_codes));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+// bf16x2 word -> two floats (exact)
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);   // a -> low half
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float absmax4(float m, float a, float b, float c, float d) {
+  return fmaxf(fmaxf(fmaxf(m, fabsf(a)), fabsf(b)), fmaxf(fabsf(c), fabsf(d)));
+}
+
+// 4×4 byte transpose: rows a,b,c,d (byte i = column i) -> columns.
+__device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                             uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
+  uint32_t t0 = __byte_perm(a, b, 0x5140);   // a0 b0 a1 b1
+  uint32_t t1 = __byte_perm(a, b, 0x7362);   // a2 b2 a3 b3
+  uint32_t t2 = __byte_perm(c, d, 0x5140);   // c0 d0 c1 d1
+  uint32_t t3 = __byte_perm(c, d, 0x7362);   // c2 d2 c3 d3
+  o0 = __byte_perm(t0, t2, 0x5410);          // a0 b0 c0 d0
+  o1 = __byte_perm(t0, t2, 0x7632);          // a1 b1 c1 d1
+  o2 = __byte_perm(t1, t3, 0x5410);
+  o3 = __byte_perm(t1, t3, 0x7632);
+}
+
+// 8×8 byte transpose.  In: row r = (lo[r], hi[r]) (columns 0-3, 4-7).
+// Out: column c = (olo[c], ohi[c]) (rows 0-3, 4-7).
+__device__ __forceinline__ void transpose8x8(const uint32_t lo[8], const uint32_t hi[8],
+                                             uint32_t olo[8], uint32_t ohi[8]) {
+  transpose4x4(lo[0], lo[1], lo[2], lo[3], olo[0], olo[1], olo[2], olo[3]);
+  transpose4x4(lo[4], lo[5], lo[6], lo[7], ohi[0], ohi[1], ohi[2], ohi[3]);
+  transpose4x4(hi[0], hi[1], hi[2], hi[3], olo[4], olo[5], olo[6], olo[7]);
+  transpose4x4(hi[4], hi[5], hi[6], hi[7], ohi[4], ohi[5], ohi[6], ohi[7]);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+}  // namespace jetfp8

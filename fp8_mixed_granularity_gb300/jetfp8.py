@@ -1,0 +1,209 @@
+"""Thin Python binding of libjetfp8.so (the C ABI in include/jetfp8.h).
+
+Argument marshalling only: every function takes torch tensors that already
+live on the GPU, checks dtype/shape/contiguity, passes raw device pointers and
+the current CUDA stream to the C entry point of the same name, and raises
+JetFP8Error on a non-OK status.  No arithmetic of the method happens here and
+there is no fallback: if the library is missing, loading it raises.
+
+Scale tensors use the library's group-index-major layout: the scales of an
+[R, C] tensor quantised in 1×128 row groups are a float32 tensor
+[C/128, roundup(R, 4)]; `scale_shape()` gives that shape.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libjetfp8.so")
+
+JETFP8_OK = 0
+OUT_BF16 = 0
+OUT_FP32 = 1
+
+_STATUS = {0: "JETFP8_OK", 1: "JETFP8_ERR_INVALID_ARG", 2: "JETFP8_ERR_UNSUPPORTED_SHAPE",
+           3: "JETFP8_ERR_MISALIGNED", 4: "JETFP8_ERR_CUDA", 5: "JETFP8_ERR_TIMEOUT",
+           6: "JETFP8_ERR_UNSUPPORTED"}
+
+# name -> argument types (all entry points return jetfp8_status as int)
+_P, _I64, _F32, _INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+SIGNATURES = {
+    "jetfp8_quant_act_1x128": [_P, _I64, _I64, _P, _P, _P],
+    "jetfp8_quant_weight_128x128": [_P, _I64, _I64, _P, _P, _P, _P],
+    "jetfp8_requant_rowgrp_to_colgrp": [_P, _P, _I64, _I64, _P, _P, _P],
+    "jetfp8_quant_grad_dual": [_P, _I64, _I64, _P, _P, _P, _P, _P],
+    "jetfp8_rmsnorm_quant": [_P, _P, _F32, _I64, _I64, _P, _P, _P, _P, _P],
+    "jetfp8_gemm_fprop": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
+    "jetfp8_gemm_dgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
+    "jetfp8_gemm_wgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
+    "jetfp8_swiglu_quant": [_P, _I64, _I64, _P, _P, _P, _P],
+    "jetfp8_swiglu_bwd": [_P, _P, _I64, _I64, _P, _P],
+    "jetfp8_get_last_device_error": [_P],
+}
+
+
+class JetFP8Error(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libjetfp8.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise JetFP8Error(f"{path} not found: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+        lib = ctypes.CDLL(path)
+        for name, argtypes in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = argtypes
+            fn.restype = ctypes.c_int
+        lib.jetfp8_status_string.argtypes = [ctypes.c_int]
+        lib.jetfp8_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, name: str) -> None:
+    if status != JETFP8_OK:
+        raise JetFP8Error(f"{name} returned {_STATUS.get(status, status)}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None, dtype: torch.dtype | None = None, shape=None, name: str = "") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise JetFP8Error(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise JetFP8Error(f"{name}: expected a contiguous tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise JetFP8Error(f"{name}: expected {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise JetFP8Error(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def round_up4(n: int) -> int:
+    return (n + 3) // 4 * 4
+
+
+def scale_shape(rows: int, cols: int) -> tuple[int, int]:
+    """Scale tensor shape for an [rows, cols] tensor in 1×128 row groups."""
+    return (cols // 128, round_up4(rows))
+
+
+_U8, _F, _BF = torch.uint8, torch.float32, torch.bfloat16
+
+
+def jetfp8_quant_act_1x128(x, q, s, stream=None):
+    M, K = x.shape
+    _check(load_library().jetfp8_quant_act_1x128(
+        _ptr(x, _BF, None, "x"), M, K, _ptr(q, _U8, (M, K), "q"), _ptr(s, _F, scale_shape(M, K), "s"),
+        _stream(stream)), "jetfp8_quant_act_1x128")
+
+
+def jetfp8_quant_weight_128x128(w, q, s, qT=None, stream=None):
+    N, K = w.shape
+    _check(load_library().jetfp8_quant_weight_128x128(
+        _ptr(w, _BF, None, "w"), N, K, _ptr(q, _U8, (N, K), "q"), _ptr(s, _F, (N // 128, K // 128), "s"),
+        _ptr(qT, _U8, (K, N), "qT"), _stream(stream)), "jetfp8_quant_weight_128x128")
+
+
+def jetfp8_requant_rowgrp_to_colgrp(q, s, qT, sT, stream=None):
+    M, K = q.shape
+    _check(load_library().jetfp8_requant_rowgrp_to_colgrp(
+        _ptr(q, _U8, None, "q"), _ptr(s, _F, scale_shape(M, K), "s"), M, K,
+        _ptr(qT, _U8, (K, M), "qT"), _ptr(sT, _F, scale_shape(K, M), "sT"), _stream(stream)),
+        "jetfp8_requant_rowgrp_to_colgrp")
+
+
+def jetfp8_quant_grad_dual(dy, q_row, s_row, qT_col=None, sT_col=None, stream=None):
+    M, N = dy.shape
+    _check(load_library().jetfp8_quant_grad_dual(
+        _ptr(dy, _BF, None, "dy"), M, N, _ptr(q_row, _U8, (M, N), "q_row"),
+        _ptr(s_row, _F, scale_shape(M, N), "s_row"), _ptr(qT_col, _U8, (N, M), "qT_col"),
+        _ptr(sT_col, _F, None if sT_col is None else scale_shape(N, M), "sT_col"), _stream(stream)),
+        "jetfp8_quant_grad_dual")
+
+
+def jetfp8_rmsnorm_quant(x, gamma, eps, q, s, rstd, y=None, stream=None):
+    M, H = x.shape
+    _check(load_library().jetfp8_rmsnorm_quant(
+        _ptr(x, _BF, None, "x"), _ptr(gamma, _BF, (H,), "gamma"), float(eps), M, H,
+        _ptr(q, _U8, (M, H), "q"), _ptr(s, _F, scale_shape(M, H), "s"), _ptr(rstd, _F, (M,), "rstd"),
+        _ptr(y, _BF, (M, H), "y"), _stream(stream)), "jetfp8_rmsnorm_quant")
+
+
+def _out_dt(out: torch.Tensor) -> int:
+    if out.dtype == _BF:
+        return OUT_BF16
+    if out.dtype == _F:
+        return OUT_FP32
+    raise JetFP8Error("output must be bfloat16 or float32")
+
+
+def jetfp8_gemm_fprop(xq, sx, wq, sw, y, stream=None):
+    M, K = xq.shape
+    N = wq.shape[0]
+    _check(load_library().jetfp8_gemm_fprop(
+        _ptr(xq, _U8, None, "xq"), _ptr(sx, _F, scale_shape(M, K), "sx"), _ptr(wq, _U8, (N, K), "wq"),
+        _ptr(sw, _F, (N // 128, K // 128), "sw"), M, N, K, _ptr(y, None, (M, N), "y"), _out_dt(y),
+        _stream(stream)), "jetfp8_gemm_fprop")
+
+
+def jetfp8_gemm_dgrad(dyq, sdy, wqT, sw, dx, stream=None):
+    M, N = dyq.shape
+    K = wqT.shape[0]
+    _check(load_library().jetfp8_gemm_dgrad(
+        _ptr(dyq, _U8, None, "dyq"), _ptr(sdy, _F, scale_shape(M, N), "sdy"), _ptr(wqT, _U8, (K, N), "wqT"),
+        _ptr(sw, _F, (N // 128, K // 128), "sw"), M, N, K, _ptr(dx, None, (M, K), "dx"), _out_dt(dx),
+        _stream(stream)), "jetfp8_gemm_dgrad")
+
+
+def jetfp8_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw, stream=None):
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    _check(load_library().jetfp8_gemm_wgrad(
+        _ptr(dyqT, _U8, None, "dyqT"), _ptr(sdyT, _F, scale_shape(N, M), "sdyT"),
+        _ptr(xqT, _U8, (K, M), "xqT"), _ptr(sxT, _F, scale_shape(K, M), "sxT"), M, N, K,
+        _ptr(dw, None, (N, K), "dw"), _out_dt(dw), _stream(stream)), "jetfp8_gemm_wgrad")
+
+
+def jetfp8_swiglu_quant(gu, q, s, h=None, stream=None):
+    M, I2 = gu.shape
+    I = I2 // 2
+    _check(load_library().jetfp8_swiglu_quant(
+        _ptr(gu, _BF, None, "gu"), M, I, _ptr(q, _U8, (M, I), "q"), _ptr(s, _F, scale_shape(M, I), "s"),
+        _ptr(h, _BF, (M, I), "h"), _stream(stream)), "jetfp8_swiglu_quant")
+
+
+def jetfp8_swiglu_bwd(gu, dh, dgu, stream=None):
+    M, I2 = gu.shape
+    I = I2 // 2
+    _check(load_library().jetfp8_swiglu_bwd(
+        _ptr(gu, _BF, None, "gu"), _ptr(dh, _BF, (M, I), "dh"), M, I, _ptr(dgu, _BF, (M, I2), "dgu"),
+        _stream(stream)), "jetfp8_swiglu_bwd")
+
+
+def jetfp8_get_last_device_error(stream=None):
+    _check(load_library().jetfp8_get_last_device_error(_stream(stream)), "jetfp8_get_last_device_error")
+
+
+# ---------------------------------------------------------------------------
+# Allocation helpers (torch.empty on the device; no computation)
+# ---------------------------------------------------------------------------
+def empty_rowgroup_quant(rows: int, cols: int, device) -> tuple[torch.Tensor, torch.Tensor]:
+    """(q uint8 [rows, cols], S float32 [cols/128, roundup(rows,4)])"""
+    return (torch.empty(rows, cols, dtype=_U8, device=device),
+            torch.empty(*scale_shape(rows, cols), dtype=_F, device=device))

@@ -1,0 +1,85 @@
+"""One FP8 linear layer's forward and backward through the jetfp8 C ABI.
+
+The order of calls follows the Jet-RL method steps ("Jet-RL：通过统一训练与推理精度流实现
+On-Policy FP8 强化学习", 方法步骤详情):
+
+  forward   X --(RMSNorm+)1×128 quant--> X̂ (kept for backward, step 3)
+            W --128×128 quant--> Ŵ, Ŵᵀ (step 1; the transpose serves DGrad, step 4)
+            Y = X̂·Ŵᵀ (FProp, step 2)
+  backward  ∇Y (BF16) --dual quant--> 1×128 rows + 128×1 columns (step 4)
+            ∇X = ∇Ŷ·Ŵ (DGrad with Ŵᵀ)
+            X̂ --requantise 1×128→128×1, transpose--> X̂ᵀ
+            ∇W = ∇Ŷᵀ·X̂ (WGrad)
+
+All buffers are allocated once, on the device, by `LinearBuffers`; a step
+only launches kernels.  Every call goes to the CUDA library: there is no
+other code path.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+from . import jetfp8 as J
+from .workloads import Linear
+
+
+@dataclass
+class LinearBuffers:
+    lin: Linear
+    device: torch.device
+    rmsnorm: bool = False          # the layer input passes through RMSNorm first
+    wgrad_fp32: bool = False
+    t: dict = field(default_factory=dict)
+
+    def __post_init__(self):
+        M, K, N = self.lin.M, self.lin.K, self.lin.N
+        d, u8, f32, bf = self.device, torch.uint8, torch.float32, torch.bfloat16
+        e = lambda *s, dt: torch.empty(*s, dtype=dt, device=d)  # noqa: E731
+        self.t.update(
+            xq=e(M, K, dt=u8), sx=e(*J.scale_shape(M, K), dt=f32),
+            wq=e(N, K, dt=u8), sw=e(N // 128, K // 128, dt=f32), wqT=e(K, N, dt=u8),
+            y=e(M, N, dt=bf),
+            dyq=e(M, N, dt=u8), sdy=e(*J.scale_shape(M, N), dt=f32),
+            dyqT=e(N, M, dt=u8), sdyT=e(*J.scale_shape(N, M), dt=f32),
+            dx=e(M, K, dt=bf),
+            xqT=e(K, M, dt=u8), sxT=e(*J.scale_shape(K, M), dt=f32),
+            dw=e(N, K, dt=f32 if self.wgrad_fp32 else bf),
+        )
+        if self.rmsnorm:
+            self.t.update(rstd=e(M, dt=f32))
+
+    # Each method returns the number of kernels it launched.
+    def forward(self, x: torch.Tensor, w: torch.Tensor, gamma: torch.Tensor | None = None,
+                stream=None, events=None) -> int:
+        t = self.t
+        if self.rmsnorm:
+            J.jetfp8_rmsnorm_quant(x, gamma, 1e-6, t["xq"], t["sx"], t["rstd"], None, stream)
+        else:
+            J.jetfp8_quant_act_1x128(x, t["xq"], t["sx"], stream)
+        J.jetfp8_quant_weight_128x128(w, t["wq"], t["sw"], t["wqT"], stream)
+        _timed(events, "gemm_fprop", lambda: J.jetfp8_gemm_fprop(t["xq"], t["sx"], t["wq"], t["sw"], t["y"], stream))
+        return 3
+
+    def backward(self, dy: torch.Tensor, stream=None, events=None) -> int:
+        t = self.t
+        J.jetfp8_quant_grad_dual(dy, t["dyq"], t["sdy"], t["dyqT"], t["sdyT"], stream)
+        _timed(events, "gemm_dgrad", lambda: J.jetfp8_gemm_dgrad(t["dyq"], t["sdy"], t["wqT"], t["sw"], t["dx"], stream))
+        J.jetfp8_requant_rowgrp_to_colgrp(t["xq"], t["sx"], t["xqT"], t["sxT"], stream)
+        _timed(events, "gemm_wgrad", lambda: J.jetfp8_gemm_wgrad(t["dyqT"], t["sdyT"], t["xqT"], t["sxT"], t["dw"], stream))
+        return 4
+
+
+def _timed(events, name, fn):
+    """Run fn; if `events` (a list) is given, bracket it with CUDA events on the
+    current stream and append (name, start, end)."""
+    if events is None:
+        fn()
+        return
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    fn()
+    e.record()
+    events.append((name, s, e))

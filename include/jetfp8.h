@@ -1,0 +1,182 @@
+/*
+ * jetfp8.h — C ABI of the GB300 (sm_103a) mixed-granularity E4M3 linear layer.
+ *
+ * The operations follow the Jet-RL pages:
+ *   [digest]  "Jet-RL：通过统一训练与推理精度流实现 On-Policy FP8 强化学习"
+ *             (paper.rainbus.top), sections 前置知识 (FP8 量化 (E4M3 格式);
+ *             GEMM 量化布局; Per-group / Per-block 量化粒度), 核心方法 and
+ *             方法步骤详情 (steps 1-5).
+ *   [summary] "Jet-RL: Enabling On-Policy FP8 Reinforcement Learning with
+ *             Unified Training and Rollout Precision Flow" (sciencestack.ai),
+ *             Figure 5 (the inference graph is a subgraph of the training graph).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - E4M3 means the FN encoding (bias 7, no infinities, largest finite 448),
+ *    stored one code per uint8_t.  Quantisation of a group:
+ *        S = fp32(amax / 448)          (S = 1 when amax = 0)
+ *        q = sat_rne_e4m3(fp32(x / S)) (round to nearest even, saturate to ±448,
+ *                                       sign of zero kept)
+ *    where both quotients are correctly rounded FP32 divisions.
+ *  - All tensors are dense, row-major, unit inner stride.  bf16 data is passed
+ *    as `const void*` holding IEEE bfloat16.
+ *  - Scale arrays are FP32 and "group-index major": the scales of an [R, C]
+ *    tensor quantised in 1×128 row groups are stored as S[g][r] with row
+ *    stride ld = roundup(R, 4), i.e. an array of (C/128) × ld floats; padding
+ *    entries are never read and may be left unwritten.
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, 16-byte
+ *    aligned, and must stay valid until the work on `stream` completes.  The
+ *    library allocates no device memory and keeps no pointer after a call
+ *    returns.  A null `stream` is the legacy default stream.
+ *  - Shapes: every length named K, N, H or I must be a positive multiple of
+ *    128.  M (tokens) may be any positive value unless an entry point says
+ *    it must be a multiple of 128.
+ *  - Calls are asynchronous on `stream`.  The returned status covers argument
+ *    validation and the launch.  A kernel whose bounded wait expires records
+ *    an error word on the device instead of hanging; read it with
+ *    jetfp8_get_last_device_error() after synchronising.
+ *  - Outputs must not alias inputs.  No C++ exception crosses this boundary.
+ *    NaN or infinite inputs are outside the contract.
+ */
+#ifndef JETFP8_H_
+#define JETFP8_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef __CUDA_RUNTIME_H__
+typedef struct CUstream_st* cudaStream_t;  /* same type as the CUDA runtime's */
+#endif
+
+typedef enum {
+  JETFP8_OK = 0,
+  JETFP8_ERR_INVALID_ARG = 1,       /* null pointer, non-positive size, bad enum */
+  JETFP8_ERR_UNSUPPORTED_SHAPE = 2, /* a length violates the multiple-of-128 rules */
+  JETFP8_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
+  JETFP8_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed */
+  JETFP8_ERR_TIMEOUT = 5,           /* a device-side bounded wait expired */
+  JETFP8_ERR_UNSUPPORTED = 6        /* device is not sm_103, or feature not built */
+} jetfp8_status;
+
+typedef enum { JETFP8_OUT_BF16 = 0, JETFP8_OUT_FP32 = 1 } jetfp8_out_dtype;
+
+/* Human-readable name of a status code (static string, never null). */
+const char* jetfp8_status_string(jetfp8_status st);
+
+/* Synchronises `stream`, returns JETFP8_ERR_TIMEOUT if any kernel of this
+ * library on the current device recorded an expired bounded wait since the
+ * last call (and clears the record), else JETFP8_OK (or JETFP8_ERR_CUDA). */
+jetfp8_status jetfp8_get_last_device_error(cudaStream_t stream);
+
+/* Q1 — 1×128 per-group activation quantisation ([digest] 方法步骤详情, steps 1-2;
+ * 前置知识 › Per-group / Per-block 量化粒度).
+ *   x  bf16 [M, K]
+ *   q  E4M3 [M, K]           (row groups of 128 consecutive elements)
+ *   s  fp32 [K/128][roundup(M,4)]
+ * M arbitrary, K multiple of 128. */
+jetfp8_status jetfp8_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K,
+                                     uint8_t* q, float* s, cudaStream_t stream);
+
+/* Q2 — 128×128 per-block weight quantisation ([digest] 方法步骤详情, step 1), with
+ * the optional transposed payload that DGrad consumes (step 4: the weight's
+ * quantisation is reused between passes, only transposed).
+ *   w   bf16 [N, K]
+ *   q   E4M3 [N, K]
+ *   s   fp32 [N/128][K/128]   (one scale per block; serves q and qT)
+ *   qT  E4M3 [K, N] or NULL  (qT[k][n] == q[n][k])
+ * N and K multiples of 128. */
+jetfp8_status jetfp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K,
+                                          uint8_t* q, float* s, uint8_t* qT,
+                                          cudaStream_t stream);
+
+/* Q3 — requantise the FP8-saved activation from 1×128 row groups to 128×1
+ * column groups, written transposed, for WGrad ([digest] 方法步骤详情, step 4;
+ * 技术新颖性).  x̃ = fp32(dec(q)·S_row) (one FP32 multiply), then each column's
+ * 128-token group is quantised with its own scale.
+ *   q   E4M3 [M, K],  s  fp32 [K/128][M]          (output of Q1 or R1)
+ *   qT  E4M3 [K, M],  sT fp32 [M/128][K]
+ * M and K multiples of 128. */
+jetfp8_status jetfp8_requant_rowgrp_to_colgrp(const uint8_t* q, const float* s,
+                                              int64_t M, int64_t K, uint8_t* qT,
+                                              float* sT, cudaStream_t stream);
+
+/* Q4 — gradient quantisation from one read of the BF16 ∇Y ([digest]
+ * 方法步骤详情, step 4: ∇Y stays BF16; gradients use 1×128 groups):
+ *   dy      bf16 [M, N]
+ *   q_row   E4M3 [M, N],  s_row  fp32 [N/128][roundup(M,4)]  (groups along N, for DGrad)
+ *   qT_col  E4M3 [N, M],  sT_col fp32 [M/128][N]             (128-token groups, transposed,
+ *                                                            for WGrad) — both NULL or both set
+ * N multiple of 128; M multiple of 128 when qT_col is set, else arbitrary. */
+jetfp8_status jetfp8_quant_grad_dual(const void* dy_bf16, int64_t M, int64_t N,
+                                     uint8_t* q_row, float* s_row, uint8_t* qT_col,
+                                     float* sT_col, cudaStream_t stream);
+
+/* R1 — RMSNorm fused with the 1×128 quantiser ([digest] 方法步骤详情, step 5).
+ *   r = 1/sqrt(mean(x²) + eps),  y = bf16((x·r)·γ),  then Q1 on y.
+ *   x      bf16 [M, H],  gamma bf16 [H]
+ *   q      E4M3 [M, H],  s fp32 [H/128][roundup(M,4)]
+ *   rstd   fp32 [M]      (kept for the backward)
+ *   y_bf16 bf16 [M, H] or NULL (the normalised output, for checking)
+ * H multiple of 128, M arbitrary, eps >= 0. */
+jetfp8_status jetfp8_rmsnorm_quant(const void* x_bf16, const void* gamma_bf16, float eps,
+                                   int64_t M, int64_t H, uint8_t* q, float* s, float* rstd,
+                                   void* y_bf16, cudaStream_t stream);
+
+/* F1 — FProp Y = X̂·Ŵᵀ with (1×128)×(128×128) scales and FP32 accumulation
+ * ([digest] 核心方法; 方法步骤详情, step 2; 前置知识 › GEMM 量化布局):
+ *   Y[m,n] = Σ_kb sx[kb][m]·sw[n/128][kb]·Σ_{k in kb} dec(xq[m,k])·dec(wq[n,k])
+ *   xq E4M3 [M, K], sx fp32 [K/128][roundup(M,4)]
+ *   wq E4M3 [N, K], sw fp32 [N/128][K/128]
+ *   y  bf16 or fp32 [M, N] per `out_dtype`
+ * Used unchanged for rollout (decode-sized M) and training, so both see the
+ * same quantised graph ([summary] Figure 5).  M arbitrary. */
+jetfp8_status jetfp8_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq,
+                                const float* sw, int64_t M, int64_t N, int64_t K, void* y,
+                                jetfp8_out_dtype out_dtype, cudaStream_t stream);
+
+/* F2 — DGrad ∇X = ∇Ŷ·Ŵ, reusing FProp's configuration with the transposed
+ * weight payload ([digest] 核心方法; 方法步骤详情, step 4):
+ *   dX[m,k] = Σ_nb sdy[nb][m]·sw[nb][k/128]·Σ_{n in nb} dec(dyq[m,n])·dec(wqT[k,n])
+ *   dyq E4M3 [M, N], sdy fp32 [N/128][roundup(M,4)]   (Q4 row output)
+ *   wqT E4M3 [K, N], sw  fp32 [N/128][K/128]          (Q2 outputs)
+ *   dx  bf16 or fp32 [M, K].  M arbitrary. */
+jetfp8_status jetfp8_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT,
+                                const float* sw, int64_t M, int64_t N, int64_t K, void* dx,
+                                jetfp8_out_dtype out_dtype, cudaStream_t stream);
+
+/* F3 — WGrad ∇W = ∇Ŷᵀ·X̂ with (1×128)×(128×1) scales: the contraction runs
+ * over tokens and both operands carry one scale per 128 tokens ([digest]
+ * 核心方法; 方法步骤详情, step 4):
+ *   dW[n,k] = Σ_tb sdyT[tb][n]·sxT[tb][k]·Σ_{m in tb} dec(dyqT[n,m])·dec(xqT[k,m])
+ *   dyqT E4M3 [N, M], sdyT fp32 [M/128][N]   (Q4 column output)
+ *   xqT  E4M3 [K, M], sxT  fp32 [M/128][K]   (Q3 output)
+ *   dw   bf16 or fp32 [N, K].  M multiple of 128. */
+jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,
+                                const float* sxT, int64_t M, int64_t N, int64_t K, void* dw,
+                                jetfp8_out_dtype out_dtype, cudaStream_t stream);
+
+/* X1 — SwiGLU fused with the 1×128 quantiser, for the decoder MLP between the
+ * gate/up and down projections (not described by the pages):
+ *   h = bf16(silu(g)·u), silu(g) = g/(1+exp(-g)), in FP32; then Q1 on h.
+ *   gu     bf16 [M, 2I]  (gate in columns [0,I), up in [I,2I))
+ *   q      E4M3 [M, I],  s fp32 [I/128][roundup(M,4)]
+ *   h_bf16 bf16 [M, I] or NULL
+ * I multiple of 128, M arbitrary. */
+jetfp8_status jetfp8_swiglu_quant(const void* gu_bf16, int64_t M, int64_t I, uint8_t* q,
+                                  float* s, void* h_bf16, cudaStream_t stream);
+
+/* X2 — SwiGLU backward: with σ = 1/(1+exp(-g)),
+ *   ∇g = ∇h·u·σ·(1 + g·(1-σ)),  ∇u = ∇h·g·σ, in FP32, rounded once to bf16.
+ *   gu  bf16 [M, 2I],  dh bf16 [M, I]  ->  dgu bf16 [M, 2I] = [∇g | ∇u]
+ * I multiple of 128, M arbitrary. */
+jetfp8_status jetfp8_swiglu_bwd(const void* gu_bf16, const void* dh_bf16, int64_t M,
+                                int64_t I, void* dgu_bf16, cudaStream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* JETFP8_H_ */

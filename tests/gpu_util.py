@@ -1,0 +1,61 @@
+"""Helpers for the GPU parity tests: run each C-ABI entry point on seeded
+inputs and bring the results back as numpy arrays."""
+import numpy as np
+import torch
+
+from fp8_mixed_granularity_gb300 import jetfp8 as J
+
+
+def h(t):
+    return t.detach().cpu().numpy()
+
+
+def check_errors():
+    J.jetfp8_get_last_device_error()
+
+
+def q_act(x_bf16, dev):
+    M, K = x_bf16.shape
+    q, s = J.empty_rowgroup_quant(M, K, dev)
+    s.fill_(float("nan"))          # padding must never be read
+    J.jetfp8_quant_act_1x128(x_bf16.to(dev), q, s)
+    check_errors()
+    return q, s
+
+
+def q_weight(w_bf16, dev, with_t=True):
+    N, K = w_bf16.shape
+    q = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    s = torch.empty(N // 128, K // 128, dtype=torch.float32, device=dev)
+    qT = torch.empty(K, N, dtype=torch.uint8, device=dev) if with_t else None
+    J.jetfp8_quant_weight_128x128(w_bf16.to(dev), q, s, qT)
+    check_errors()
+    return q, s, qT
+
+
+def q_grad(dy_bf16, dev, with_col=True):
+    M, N = dy_bf16.shape
+    q, s = J.empty_rowgroup_quant(M, N, dev)
+    s.fill_(float("nan"))
+    qT, sT = J.empty_rowgroup_quant(N, M, dev) if with_col else (None, None)
+    J.jetfp8_quant_grad_dual(dy_bf16.to(dev), q, s, qT, sT)
+    check_errors()
+    return q, s, qT, sT
+
+
+def requant(q, s, dev):
+    M, K = q.shape
+    qT, sT = J.empty_rowgroup_quant(K, M, dev)
+    J.jetfp8_requant_rowgrp_to_colgrp(q, s, qT, sT)
+    check_errors()
+    return qT, sT
+
+
+def gemm_tol_ok(got, ref, rel=1e-2, rms_frac=1e-3):
+    """|Δ| <= rel·|ref| + rms_frac·rms(ref) elementwise; returns (ok, worst ratio)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    bound = rel * np.abs(ref) + rms_frac * rms
+    ratio = np.abs(got - ref) / np.maximum(bound, 1e-300)
+    return bool(np.all(ratio <= 1.0)), float(ratio.max()) if ratio.size else 0.0

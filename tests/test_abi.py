@@ -1,0 +1,70 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds/loads,
+exports every entry point include/jetfp8.h declares, and the binding knows
+each one's arity."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "jetfp8.h")
+
+
+def _declared():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(jetfp8_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from fp8_mixed_granularity_gb300 import jetfp8
+    return jetfp8.load_library()
+
+
+def test_header_declares_the_hot_path():
+    names = _declared()
+    for n in ["jetfp8_quant_act_1x128", "jetfp8_quant_weight_128x128",
+              "jetfp8_requant_rowgrp_to_colgrp", "jetfp8_quant_grad_dual",
+              "jetfp8_rmsnorm_quant", "jetfp8_gemm_fprop", "jetfp8_gemm_dgrad",
+              "jetfp8_gemm_wgrad"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_declared_symbol():
+    from fp8_mixed_granularity_gb300 import jetfp8
+    for name in _declared():
+        if name == "jetfp8_status_string":
+            continue
+        assert name in jetfp8.SIGNATURES, name
+        assert callable(getattr(jetfp8, name)), name
+
+
+def test_status_strings(lib):
+    for code, text in [(0, b"JETFP8_OK"), (2, b"JETFP8_ERR_UNSUPPORTED_SHAPE"), (5, b"JETFP8_ERR_TIMEOUT")]:
+        assert lib.jetfp8_status_string(code) == text
+
+
+def test_validation_rejects_before_touching_the_device(lib):
+    """Null pointers and bad shapes are refused synchronously, before any
+    CUDA call (so this runs on a machine without a GPU)."""
+    P = ctypes.c_void_p
+    # null input
+    assert lib.jetfp8_quant_act_1x128(None, 4, 128, P(16), P(16), None) == 1
+    # K not a multiple of 128
+    assert lib.jetfp8_quant_act_1x128(P(16), 4, 100, P(16), P(16), None) == 2
+    # misaligned pointer
+    assert lib.jetfp8_quant_act_1x128(P(18), 4, 128, P(16), P(16), None) == 3
+    # WGrad needs M multiple of 128
+    assert lib.jetfp8_gemm_wgrad(P(16), P(16), P(16), P(16), 100, 128, 128, P(16), 0, None) == 2
+    # bad output dtype is caught after shape checks, before the launch
+    assert lib.jetfp8_gemm_fprop(P(16), P(16), P(16), P(16), 0, 128, 128, P(16), 0, None) == 1

@@ -1,0 +1,185 @@
+"""GPU parity of the quantisers against the CPU oracle, through the C ABI.
+Codes and scales must be bit-identical."""
+import numpy as np
+import pytest
+import torch
+
+from fp8_mixed_granularity_gb300 import jetfp8 as J
+from fp8_mixed_granularity_gb300 import workloads as W
+from oracle import jetfp8_oracle as O
+from tests.gpu_util import check_errors, h, q_act, q_grad, q_weight, requant
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__ as g
+    g.build()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+def _assert_rowquant(q, s, xf):
+    oq, os_ = O.quant_rowgroups(xf)
+    M = xf.shape[0]
+    assert np.array_equal(h(s)[:, :M], os_), "scales differ"
+    gq = h(q)
+    if not np.array_equal(gq, oq):
+        bad = np.argwhere(gq != oq)
+        i, j = bad[0]
+        raise AssertionError(f"{len(bad)} codes differ; first at {(i, j)}: x={xf[i, j]!r} "
+                             f"gpu={gq[i, j]:#04x} oracle={oq[i, j]:#04x}")
+
+
+@pytest.mark.parametrize("M,K", [(256, 512), (1, 128), (3, 256), (130, 384), (257, 1024), (1000, 4096)])
+def test_quant_act_parity(dev, M, K):
+    x = W.activations(M, K, seed=0, stream=M)
+    q, s = q_act(x, dev)
+    _assert_rowquant(q, s, W.bf16_values(x))
+
+
+def test_quant_act_edge_values(dev):
+    """Zero groups, signed zeros, ties of the E4M3 grid, tiny (subnormal-scale)
+    groups, huge groups, and every positive code's midpoint under S = 1."""
+    K = 128
+    rows = []
+    r = np.zeros(K, np.float32); rows.append(r)                       # all zero -> S = 1
+    r = np.zeros(K, np.float32); r[::2] = -0.0; r[1] = 0.0; rows.append(r)
+    r = np.zeros(K, np.float32); r[0] = 448; r[1:19] = [17, 19, -17, -19, 0.0009765625, 1.5 * 2**-10,
+                                                         2**-12, -2**-12, 240, 3.1, 0.3, 2**-6, 7 * 2**-9,
+                                                         -448, 1, -1, 2, 0.5]; rows.append(r)
+    r = (np.arange(K, dtype=np.float32) - 64) * np.float32(1e-38); rows.append(r)   # subnormal S
+    r = (np.arange(K, dtype=np.float32) - 64) * np.float32(1e36); rows.append(r)
+    d = O.e4m3_decode(np.arange(0x7F))
+    mids = ((d[:-1] + d[1:]) / 2).astype(np.float32)
+    for c in range(0, len(mids), K - 1):
+        r = np.zeros(K, np.float32); r[0] = 448
+        chunk = mids[c:c + K - 1]; r[1:1 + len(chunk)] = chunk; rows.append(r)
+    x = W.to_bf16(np.stack(rows))
+    q, s = q_act(x, dev)
+    _assert_rowquant(q, s, W.bf16_values(x))
+
+
+@pytest.mark.parametrize("N,K", [(384, 512), (128, 128), (1024, 2048)])
+def test_quant_weight_parity(dev, N, K):
+    w = W.weights(N, K, seed=1)
+    q, s, qT = q_weight(w, dev)
+    oq, os_, oqT = O.quant_weight_128x128(W.bf16_values(w))
+    assert np.array_equal(h(s), os_)
+    assert np.array_equal(h(q), oq)
+    assert np.array_equal(h(qT), oqT)
+
+
+def test_quant_weight_without_transpose(dev):
+    w = W.weights(256, 384, seed=2)
+    q, s, _ = q_weight(w, dev, with_t=False)
+    oq, os_, _ = O.quant_weight_128x128(W.bf16_values(w))
+    assert np.array_equal(h(q), oq) and np.array_equal(h(s), os_)
+
+
+@pytest.mark.parametrize("M,K", [(256, 512), (128, 128), (1024, 1536)])
+def test_requant_parity(dev, M, K):
+    x = W.activations(M, K, seed=0, stream=7)
+    q, s = q_act(x, dev)
+    qT, sT = requant(q, s, dev)
+    oq, os_ = O.quant_act_1x128(W.bf16_values(x))
+    oqT, osT = O.requant_rowgrp_to_colgrp(oq, os_)
+    assert np.array_equal(h(sT), osT)
+    assert np.array_equal(h(qT), oqT)
+
+
+def test_requant_decodes_every_code(dev):
+    """All 254 finite codes through the GPU decode with power-of-two row
+    scales (exact dequantisation)."""
+    g = np.random.default_rng(0)
+    codes = np.tile(np.concatenate([np.arange(0x7F), np.arange(0x80, 0xFF)]).astype(np.uint8), 129)[:128 * 256]
+    codes = codes.reshape(128, 256)
+    g.shuffle(codes, axis=1)
+    s = np.ldexp(1.0, g.integers(-8, 8, size=(2, 128))).astype(np.float32)
+    q = torch.from_numpy(codes).to(dev)
+    st = torch.from_numpy(s).to(dev)
+    qT, sT = requant(q, st, dev)
+    oqT, osT = O.requant_rowgrp_to_colgrp(codes, s)
+    assert np.array_equal(h(sT), osT) and np.array_equal(h(qT), oqT)
+
+
+@pytest.mark.parametrize("M,N", [(256, 384), (128, 128), (512, 1024)])
+def test_quant_grad_dual_parity(dev, M, N):
+    dy = W.gradients(M, N, seed=3)
+    q, s, qT, sT = q_grad(dy, dev)
+    oq, os_, oqT, osT = O.quant_grad_dual(W.bf16_values(dy))
+    assert np.array_equal(h(s)[:, :M], os_) and np.array_equal(h(q), oq)
+    assert np.array_equal(h(sT), osT) and np.array_equal(h(qT), oqT)
+
+
+@pytest.mark.parametrize("M", [1, 200])
+def test_quant_grad_rows_only_ragged(dev, M):
+    dy = W.gradients(M, 384, seed=4)
+    q, s, _, _ = q_grad(dy, dev, with_col=False)
+    _assert_rowquant(q, s, W.bf16_values(dy))
+
+
+def test_quant_grad_dual_rejects_ragged_columns(dev):
+    dy = W.gradients(200, 128, seed=5).to(dev)
+    q, s = J.empty_rowgroup_quant(200, 128, dev)
+    qT = torch.empty(128, 200, dtype=torch.uint8, device=dev)
+    sT = torch.empty(2, 128, dtype=torch.float32, device=dev)
+    with pytest.raises(J.JetFP8Error, match="UNSUPPORTED_SHAPE"):
+        J.jetfp8_quant_grad_dual(dy, q, s, qT, sT)
+
+
+@pytest.mark.parametrize("M,H", [(64, 4096), (5, 384), (300, 1024)])
+def test_rmsnorm_quant_parity(dev, M, H):
+    x = W.activations(M, H, seed=6)
+    gamma = W.uniform((H,), 0.5, 1.5, seed=6, stream=9)
+    q, s = J.empty_rowgroup_quant(M, H, dev)
+    rstd = torch.empty(M, dtype=torch.float32, device=dev)
+    y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    J.jetfp8_rmsnorm_quant(x.to(dev), gamma.to(dev), 1e-6, q, s, rstd, y)
+    check_errors()
+    oy, orstd, oq, os_ = O.rmsnorm_quant(W.bf16_values(x), W.bf16_values(gamma), 1e-6)
+    gy = h(y.float()).astype(np.float64)
+    # y within one bf16 ulp of the FP64 result rounded to bf16
+    ulp = np.ldexp(1.0, np.frexp(np.abs(oy))[1] - 8)
+    assert np.all(np.abs(gy - oy) <= ulp)
+    # rstd: per lane, 8-square FP32 chunk sums (<= 7 roundings) added in FP32
+    # (<= H/256 - 1 more), lanes combined in FP64: relative error of Σx² below
+    # 22·2^-24 for H = 4096, halved by the square root, plus the final FP32
+    # rounding -> at most 12·2^-24; the test allows 16·2^-24.
+    assert np.allclose(h(rstd), orstd, rtol=16 * 2.0 ** -24, atol=0)
+    # the fused quantiser is bit-exact on the GPU's own y
+    gq, gs = O.quant_rowgroups(gy.astype(np.float32))
+    assert np.array_equal(h(s)[:, :M], gs) and np.array_equal(h(q), gq)
+    # and end to end the codes match the oracle's except at rare bf16 ties
+    mismatch = np.mean(h(q) != oq)
+    assert mismatch < 1e-3
+
+
+@pytest.mark.parametrize("M,I", [(64, 1024), (3, 128)])
+def test_swiglu_quant_parity(dev, M, I):
+    gu = W.normal((M, 2 * I), 2.0, seed=7)
+    q, s = J.empty_rowgroup_quant(M, I, dev)
+    hb = torch.empty(M, I, dtype=torch.bfloat16, device=dev)
+    J.jetfp8_swiglu_quant(gu.to(dev), q, s, hb)
+    check_errors()
+    oh, oq, os_ = O.swiglu_quant(W.bf16_values(gu))
+    gh = h(hb.float()).astype(np.float64)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(oh))[1] - 8)
+    assert np.all(np.abs(gh - oh) <= ulp + 1e-40)
+    gq, gs = O.quant_rowgroups(gh.astype(np.float32))
+    assert np.array_equal(h(s)[:, :M], gs) and np.array_equal(h(q), gq)
+
+
+def test_swiglu_bwd_parity(dev):
+    M, I = 64, 512
+    gu = W.normal((M, 2 * I), 2.0, seed=8)
+    dh = W.normal((M, I), 1e-3, seed=8, stream=3)
+    dgu = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dev)
+    J.jetfp8_swiglu_bwd(gu.to(dev), dh.to(dev), dgu)
+    check_errors()
+    od = O.swiglu_bwd(W.bf16_values(gu), W.bf16_values(dh))
+    gd = h(dgu.float()).astype(np.float64)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(od))[1] - 8)
+    assert np.all(np.abs(gd - od) <= ulp + 1e-40)
