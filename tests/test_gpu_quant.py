@@ -94,7 +94,7 @@ def test_requant_decodes_every_code(dev):
     """All 254 finite codes through the GPU decode with power-of-two row
     scales (exact dequantisation)."""
     g = np.random.default_rng(0)
-    codes = np.tile(np.concatenate([np.arange(0x7F), np.arange(0x80, 0xFF)]).astype(np.uint8), 129)[:128 * 256]
+    codes = np.tile(np.concatenate([np.arange(0x7F), np.arange(0x80, 0xFF)]).astype(np.uint8), 130)[:128 * 256]
     codes = codes.reshape(128, 256)
     g.shuffle(codes, axis=1)
     s = np.ldexp(1.0, g.integers(-8, 8, size=(2, 128))).astype(np.float32)
@@ -125,7 +125,7 @@ def test_quant_grad_dual_rejects_ragged_columns(dev):
     dy = W.gradients(200, 128, seed=5).to(dev)
     q, s = J.empty_rowgroup_quant(200, 128, dev)
     qT = torch.empty(128, 200, dtype=torch.uint8, device=dev)
-    sT = torch.empty(2, 128, dtype=torch.float32, device=dev)
+    sT = torch.empty(*J.scale_shape(128, 200), dtype=torch.float32, device=dev)
     with pytest.raises(J.JetFP8Error, match="UNSUPPORTED_SHAPE"):
         J.jetfp8_quant_grad_dual(dy, q, s, qT, sT)
 
