@@ -60,6 +60,9 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--case", choices=sorted(CASES), default=None,
+                   help="time one kernel alone (for profiling) instead of the layer step")
+    p.add_argument("--shape", default="8192,28672,4096", help="M,N,K for --case")
     return p.parse_args()
 
 
@@ -396,8 +399,69 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
+# ---------------------------------------------------------------------------
+# single-kernel cases (profiling aid): one kernel, one shape, W + K launches
+# ---------------------------------------------------------------------------
+CASES = {"fprop", "dgrad", "wgrad", "quant_act", "rmsnorm_quant", "quant_weight",
+         "quant_grad_dual", "requant"}
+
+
+def run_case(args):
+    import torch
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import __graft_entry__ as g
+    g.build()
+    from fp8_mixed_granularity_gb300 import jetfp8 as J
+    from fp8_mixed_granularity_gb300 import workloads as W
+    from fp8_mixed_granularity_gb300.linear import LinearBuffers
+    M, N, K = (int(v) for v in args.shape.split(","))
+    lin = W.Linear("case", M, K, N)
+    b = LinearBuffers(lin, dev, rmsnorm=args.case == "rmsnorm_quant")
+    x = W.device_activations(M, K, dev, seed=1)
+    w = W.device_normal((N, K), 0.02, dev, seed=2)
+    dy = W.device_normal((M, N), 1e-3, dev, seed=3)
+    gamma = W.device_uniform((K,), 0.5, 1.5, dev, seed=4)
+    b.forward(x, w, gamma)
+    b.backward(dy)
+    t = b.t
+    calls = {
+        "fprop": (lambda: J.jetfp8_gemm_fprop(t["xq"], t["sx"], t["wq"], t["sw"], t["y"]), 2 * M * N * K, "TFLOP/s"),
+        "dgrad": (lambda: J.jetfp8_gemm_dgrad(t["dyq"], t["sdy"], t["wqT"], t["sw"], t["dx"]), 2 * M * N * K, "TFLOP/s"),
+        "wgrad": (lambda: J.jetfp8_gemm_wgrad(t["dyqT"], t["sdyT"], t["xqT"], t["sxT"], t["dw"]), 2 * M * N * K, "TFLOP/s"),
+        "quant_act": (lambda: J.jetfp8_quant_act_1x128(x, t["xq"], t["sx"]), M * K * QUANT_BYTES["quant_act"], "GB/s"),
+        "rmsnorm_quant": (lambda: J.jetfp8_rmsnorm_quant(x, gamma, 1e-6, t["xq"], t["sx"], t["rstd"]),
+                          M * K * QUANT_BYTES["rmsnorm_quant"] + 2 * K + 4 * M, "GB/s"),
+        "quant_weight": (lambda: J.jetfp8_quant_weight_128x128(w, t["wq"], t["sw"], t["wqT"]),
+                         N * K * QUANT_BYTES["quant_weight"], "GB/s"),
+        "quant_grad_dual": (lambda: J.jetfp8_quant_grad_dual(dy, t["dyq"], t["sdy"], t["dyqT"], t["sdyT"]),
+                            M * N * QUANT_BYTES["quant_grad_dual"], "GB/s"),
+        "requant": (lambda: J.jetfp8_requant_rowgrp_to_colgrp(t["xq"], t["sx"], t["xqT"], t["sxT"]),
+                    M * K * QUANT_BYTES["requant"], "GB/s"),
+    }
+    fn, work, unit = calls[args.case]
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.steps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(); fn(); e.record()
+        evs.append((s, e))
+    torch.cuda.synchronize()
+    J.jetfp8_get_last_device_error()
+    ms = sorted(s.elapsed_time(e) for s, e in evs)
+    med = ms[len(ms) // 2]
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    print(json.dumps({"case": args.case, "shape": [M, N, K], "median_ms": med, "min_ms": ms[0],
+                      "value": work / (med * 1e-3) / scale, "unit": unit}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.case is not None:
+        run_case(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -10,19 +10,23 @@
 // 128-deep block is accumulated on its own in TMEM and promoted in registers,
 //   acc[i,j] += partial_kb[i,j] · sA[kb][i] · sB(kb,j).
 //
-// CTA organisation (persistent, one CTA per SM, 384 threads):
-//   warp 0      TMA producer: A tile 128×128 B and B tile 256×128 B per stage,
-//               128-byte swizzle, 4-stage shared-memory ring.
+// CTA organisation (persistent, one CTA per SM, 384 threads), for a tile of
+// 128 rows × BN columns (BN = 256 with two TMEM accumulators, or BN = 128 with
+// four, so the tensor core can run further ahead of the promotion):
+//   warp 0      TMA producer: A tile 128 rows × 128 bytes and B tile BN rows ×
+//               128 bytes per stage, 128-byte swizzle, multi-stage ring.
 //   warp 1      allocates 512 TMEM columns; one lane issues tcgen05.mma
-//               (M=128, N=256, K=32, E4M3×E4M3→FP32) four times per block into
-//               one of two 256-column TMEM accumulators, then commits.
-//   warps 2-3   idle (they complete the control warpgroup, which gives up
-//               registers with setmaxnreg.dec).
-//   warps 4-11  two warpgroups; warpgroup w owns output columns [128w, 128w+128)
-//               of the tile and each thread one row (its TMEM lane).  They
-//               tcgen05.ld the block partial, release the TMEM buffer, promote
-//               it into 128 FP32 registers, and after the last block write the
-//               row out as bf16 or fp32.
+//               (M=128, N=BN, K=32, E4M3×E4M3→FP32) four times per block into
+//               the next TMEM accumulator, then commits.
+//   warps 2-3   idle; with warps 0-1 they form the control warpgroup, which
+//               gives registers back (setmaxnreg.dec) to the promotion warps.
+//   warps 4-11  two warpgroups; warpgroup w owns output columns
+//               [w·BN/2, (w+1)·BN/2) of the tile and each thread one row (its
+//               TMEM lane).  Per block they load the partial 32 columns at a
+//               time (the next chunk's load overlapping the current chunk's
+//               FMAs), hand the accumulator back as soon as the last chunk is
+//               in registers, and promote with packed FP32 FMAs; after the
+//               last block the row is written out as bf16 or fp32.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records an
 // error word, lets copies and MMAs in flight land, frees TMEM and returns.
 #include <cuda.h>
@@ -34,42 +38,56 @@
 namespace jetfp8 {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int ACC_BUFS = 2;
-constexpr int TMEM_COLS = ACC_BUFS * BN;   // 512
+constexpr int BM = 128, BK = 128;
+constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
-constexpr int EPI_WARP0 = 4;                     // warps 0-3: control warpgroup
+constexpr int EPI_WARP0 = 4;                             // warps 0-3: control warpgroup
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 384
 // Register split.  The kernel is launched with LAUNCH_REGS per thread
 // (384 × 168 = 64512); the control warpgroup gives registers back and the two
 // promotion warpgroups take them: 128·CTRL_REGS + 256·EPI_REGS must not exceed
-// the launch total, or setmaxnreg.inc would wait forever.
+// the launch total, or setmaxnreg.inc would wait forever.  The host refuses to
+// launch unless the compiled kernel uses exactly LAUNCH_REGS.
 constexpr int LAUNCH_REGS = 168;
-constexpr int CTRL_REGS = 56;
-constexpr int EPI_REGS = 224;
+constexpr int CTRL_REGS = 40;
+constexpr int EPI_REGS = 232;
 static_assert(128 * CTRL_REGS + 256 * EPI_REGS <= THREADS * LAUNCH_REGS, "register split");
 constexpr uint64_t WAIT_NS = 2000000000ull;
+constexpr int MAX_STAGES = 8, MAX_BUFS = 4;
+// bf16 output leaves through shared memory in 32-row × 32-column chunks, one
+// 2 KB staging buffer per promotion warp, written to global memory by TMA.
+constexpr int OUT_CHUNK_BYTES = 32 * 32 * 2;
 
-// UMMA instruction descriptor: D = F32 (bits 4-5 = 1), A = B = E4M3 (format 0),
-// both K-major, N/8 at bits 17-22, M/16 at bits 24-28.
-constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+template <int BN_>
+struct Cfg {
+  static constexpr int BN = BN_;
+  static constexpr int STAGES = BN_ == 256 ? 4 : 6;
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int ACC_BUFS = TMEM_COLS / BN;
+  static constexpr int EPI_COLS = BN / 2;        // columns per promotion warp
+  static constexpr int CHUNKS = EPI_COLS / 32;   // 32-column TMEM loads per block
+  // UMMA instruction descriptor: D = F32 (bits 4-5 = 1), A = B = E4M3 (format 0),
+  // both K-major, N/8 at bits 17-22, M/16 at bits 24-28.
+  static constexpr uint32_t IDESC =
+      (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  static constexpr int COLBUF_BYTES = EPI_WARPS * 2 * EPI_COLS * 4;
+  static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES +
+                                    1024 /*barriers*/ + COLBUF_BYTES + EPI_WARPS * OUT_CHUNK_BYTES;
+  static_assert(STAGES <= MAX_STAGES && ACC_BUFS <= MAX_BUFS, "barrier arrays");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
 
 struct Barriers {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[ACC_BUFS];
-  uint64_t tempty[ACC_BUFS];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  uint64_t tfull[MAX_BUFS];
+  uint64_t tempty[MAX_BUFS];
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
 };
-
-constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + 1024 /*barriers*/ +
-                           EPI_WARPS * 2 * 128 * 4 /*column scales*/;
 
 struct DevArgs {
   const float* sA;
@@ -78,9 +96,24 @@ struct DevArgs {
   long long sb_j, sb_k;
   void* out;
   int R, C, nKB, tiles_m, tiles_n;
+  int m_fastest;   // tile order: 1 = consecutive tiles walk down M (share a B tile)
   int b_col_mode, out_fp32;
   unsigned* err;
 };
+
+// Tile index -> (m tile, n tile).  Consecutive tiles (which run at the same
+// time on neighbouring SMs) share one operand tile; the other operand is
+// streamed once per band, so the order keeps the re-streamed operand the
+// smaller of the two.
+__device__ __forceinline__ void tile_coords(const DevArgs& p, int tile, int& mt, int& nt) {
+  if (p.m_fastest) {
+    mt = tile % p.tiles_m;
+    nt = tile / p.tiles_m;
+  } else {
+    nt = tile % p.tiles_n;
+    mt = tile / p.tiles_n;
+  }
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -109,7 +142,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of parity `parity` to complete.  Gives up (false) after
 // WAIT_NS, or early when another role has already aborted and `honour_abort`.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                       bool honour_abort) {
+                                          bool honour_abort) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -136,6 +169,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Bulk tensor store of a shared-memory box to global memory (async proxy).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until the previous bulk stores of this thread have finished reading shared memory.
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major tile stored as 128-byte rows
 // with the 128-byte swizzle (8-row atoms of 1024 B): start address >> 4,
 // leading offset 16 B (unused for this layout), stride offset 1024 B, the
@@ -146,12 +200,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 }
 
 __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate));
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -168,29 +222,165 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul_pair(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
+// Starts loading 32 TMEM columns into r[0..31]; the values are valid only
+// after tmem_wait_ld(r).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Waits for this thread's TMEM loads.  The destination registers of the load
+// are tied to the wait so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// acc[j] += (p[2j], p[2j+1]) · s2 for 16 packed FP32 pairs (one scale pair).
+__device__ __forceinline__ void fma32_uniform(uint64_t (&acc)[16], const uint32_t (&p)[32], uint64_t s2) {
+  asm("{\n\t.reg .b64 q;\n\t"
+      "mov.b64 q, {%16, %17};\n\t"
+      "fma.rn.f32x2 %0, q, %48, %0;\n\t"
+      "mov.b64 q, {%18, %19};\n\t"
+      "fma.rn.f32x2 %1, q, %48, %1;\n\t"
+      "mov.b64 q, {%20, %21};\n\t"
+      "fma.rn.f32x2 %2, q, %48, %2;\n\t"
+      "mov.b64 q, {%22, %23};\n\t"
+      "fma.rn.f32x2 %3, q, %48, %3;\n\t"
+      "mov.b64 q, {%24, %25};\n\t"
+      "fma.rn.f32x2 %4, q, %48, %4;\n\t"
+      "mov.b64 q, {%26, %27};\n\t"
+      "fma.rn.f32x2 %5, q, %48, %5;\n\t"
+      "mov.b64 q, {%28, %29};\n\t"
+      "fma.rn.f32x2 %6, q, %48, %6;\n\t"
+      "mov.b64 q, {%30, %31};\n\t"
+      "fma.rn.f32x2 %7, q, %48, %7;\n\t"
+      "mov.b64 q, {%32, %33};\n\t"
+      "fma.rn.f32x2 %8, q, %48, %8;\n\t"
+      "mov.b64 q, {%34, %35};\n\t"
+      "fma.rn.f32x2 %9, q, %48, %9;\n\t"
+      "mov.b64 q, {%36, %37};\n\t"
+      "fma.rn.f32x2 %10, q, %48, %10;\n\t"
+      "mov.b64 q, {%38, %39};\n\t"
+      "fma.rn.f32x2 %11, q, %48, %11;\n\t"
+      "mov.b64 q, {%40, %41};\n\t"
+      "fma.rn.f32x2 %12, q, %48, %12;\n\t"
+      "mov.b64 q, {%42, %43};\n\t"
+      "fma.rn.f32x2 %13, q, %48, %13;\n\t"
+      "mov.b64 q, {%44, %45};\n\t"
+      "fma.rn.f32x2 %14, q, %48, %14;\n\t"
+      "mov.b64 q, {%46, %47};\n\t"
+      "fma.rn.f32x2 %15, q, %48, %15;\n\t"
+      "}"
+      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]),
+        "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
+      : "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]),
+        "r"(p[6]), "r"(p[7]), "r"(p[8]), "r"(p[9]), "r"(p[10]), "r"(p[11]),
+        "r"(p[12]), "r"(p[13]), "r"(p[14]), "r"(p[15]), "r"(p[16]), "r"(p[17]),
+        "r"(p[18]), "r"(p[19]), "r"(p[20]), "r"(p[21]), "r"(p[22]), "r"(p[23]),
+        "r"(p[24]), "r"(p[25]), "r"(p[26]), "r"(p[27]), "r"(p[28]), "r"(p[29]),
+        "r"(p[30]), "r"(p[31]), "l"(s2));
+}
+
+// acc[j] += (p[2j], p[2j+1]) · s2[j] for 16 packed FP32 pairs.
+__device__ __forceinline__ void fma32_pairs(uint64_t (&acc)[16], const uint32_t (&p)[32], const uint64_t (&s2)[16]) {
+  asm("{\n\t.reg .b64 q;\n\t"
+      "mov.b64 q, {%16, %17};\n\t"
+      "fma.rn.f32x2 %0, q, %48, %0;\n\t"
+      "mov.b64 q, {%18, %19};\n\t"
+      "fma.rn.f32x2 %1, q, %49, %1;\n\t"
+      "mov.b64 q, {%20, %21};\n\t"
+      "fma.rn.f32x2 %2, q, %50, %2;\n\t"
+      "mov.b64 q, {%22, %23};\n\t"
+      "fma.rn.f32x2 %3, q, %51, %3;\n\t"
+      "mov.b64 q, {%24, %25};\n\t"
+      "fma.rn.f32x2 %4, q, %52, %4;\n\t"
+      "mov.b64 q, {%26, %27};\n\t"
+      "fma.rn.f32x2 %5, q, %53, %5;\n\t"
+      "mov.b64 q, {%28, %29};\n\t"
+      "fma.rn.f32x2 %6, q, %54, %6;\n\t"
+      "mov.b64 q, {%30, %31};\n\t"
+      "fma.rn.f32x2 %7, q, %55, %7;\n\t"
+      "mov.b64 q, {%32, %33};\n\t"
+      "fma.rn.f32x2 %8, q, %56, %8;\n\t"
+      "mov.b64 q, {%34, %35};\n\t"
+      "fma.rn.f32x2 %9, q, %57, %9;\n\t"
+      "mov.b64 q, {%36, %37};\n\t"
+      "fma.rn.f32x2 %10, q, %58, %10;\n\t"
+      "mov.b64 q, {%38, %39};\n\t"
+      "fma.rn.f32x2 %11, q, %59, %11;\n\t"
+      "mov.b64 q, {%40, %41};\n\t"
+      "fma.rn.f32x2 %12, q, %60, %12;\n\t"
+      "mov.b64 q, {%42, %43};\n\t"
+      "fma.rn.f32x2 %13, q, %61, %13;\n\t"
+      "mov.b64 q, {%44, %45};\n\t"
+      "fma.rn.f32x2 %14, q, %62, %14;\n\t"
+      "mov.b64 q, {%46, %47};\n\t"
+      "fma.rn.f32x2 %15, q, %63, %15;\n\t"
+      "}"
+      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]),
+        "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
+      : "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]),
+        "r"(p[6]), "r"(p[7]), "r"(p[8]), "r"(p[9]), "r"(p[10]), "r"(p[11]),
+        "r"(p[12]), "r"(p[13]), "r"(p[14]), "r"(p[15]), "r"(p[16]), "r"(p[17]),
+        "r"(p[18]), "r"(p[19]), "r"(p[20]), "r"(p[21]), "r"(p[22]), "r"(p[23]),
+        "r"(p[24]), "r"(p[25]), "r"(p[26]), "r"(p[27]), "r"(p[28]), "r"(p[29]),
+        "r"(p[30]), "r"(p[31]), "l"(s2[0]), "l"(s2[1]), "l"(s2[2]), "l"(s2[3]),
+        "l"(s2[4]), "l"(s2[5]), "l"(s2[6]), "l"(s2[7]), "l"(s2[8]), "l"(s2[9]),
+        "l"(s2[10]), "l"(s2[11]), "l"(s2[12]), "l"(s2[13]), "l"(s2[14]), "l"(s2[15]));
+}
+
+
+template <int EPI_COLS>
+struct ColScaleVec;
+template <>
+struct ColScaleVec<64> {
+  using T = float2;
+};
+template <>
+struct ColScaleVec<128> {
+  using T = float4;
+};
+
+template <int BN_>
 __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const DevArgs p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmOut, const DevArgs p) {
+  using C = Cfg<BN_>;
+  constexpr int BN = C::BN, STAGES = C::STAGES, ACC_BUFS = C::ACC_BUFS;
+  constexpr int EPI_COLS = C::EPI_COLS, CHUNKS = C::CHUNKS;
+  using CsVec = typename ColScaleVec<EPI_COLS>::T;
+
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + STAGES * STAGE_BYTES);
-  float* colbuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 1024);  // [8 warps][2][128]
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + STAGES * C::STAGE_BYTES);
+  // [8 promotion warps][2][EPI_COLS] column scales (column mode)
+  float* colbuf = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES + 1024);
+  // [8 promotion warps][32 rows][32 bf16] output staging
+  uint8_t* outbuf = smem + STAGES * C::STAGE_BYTES + 1024 + C::COLBUF_BYTES;
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -231,7 +421,8 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-          const int mt = tile % p.tiles_m, nt = tile / p.tiles_m;
+          int mt, nt;
+          tile_coords(p, tile, mt, nt);
           for (int kb = 0; kb < p.nKB; ++kb, ++it) {
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort_flag, true)) {
@@ -239,10 +430,10 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
               ok = false;
               break;
             }
-            uint8_t* st = smem + s * STAGE_BYTES;
-            mbar_arrive_expect_tx(&bars->full[s], STAGE_BYTES);
+            uint8_t* st = smem + s * C::STAGE_BYTES;
+            mbar_arrive_expect_tx(&bars->full[s], C::STAGE_BYTES);
             tma_load_2d(smem_u32(st), &tmA, &bars->full[s], kb * BK, mt * BM);
-            tma_load_2d(smem_u32(st + A_BYTES), &tmB, &bars->full[s], kb * BK, nt * BN);
+            tma_load_2d(smem_u32(st + C::A_BYTES), &tmB, &bars->full[s], kb * BK, nt * BN);
           }
         }
         if (!ok) {
@@ -268,12 +459,12 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
-            const uint32_t b_addr = a_addr + A_BYTES;
-  #pragma unroll
+            const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
+            const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
             for (int k = 0; k < BK / 32; ++k)
               umma_e4m3(tmem + b * BN, sdesc_sw128(a_addr + 32 * k), sdesc_sw128(b_addr + 32 * k),
-                        k > 0 ? 1u : 0u);
+                        C::IDESC, k > 0 ? 1u : 0u);
             umma_commit(&bars->empty[s]);
             umma_commit(&bars->tfull[b]);
           }
@@ -290,35 +481,64 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
     const int wg = ew >> 2;                 // column half of the tile
     const int lq = warp & 3;                // TMEM lane quarter this warp may access
     const int row_in_tile = lq * 32 + lane;
-    const uint32_t taddr_row = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(wg * 128);
-    // per-warp double buffer of this half-tile's 128 column scales (column mode)
-    float* cbuf = colbuf + ew * 256;
+    const uint32_t taddr_row = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(wg * EPI_COLS);
+    float* cbuf = colbuf + ew * 2 * EPI_COLS;
     uint32_t acc_it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const int mt = tile % p.tiles_m, nt = tile / p.tiles_m;
+      int mt, nt;
+      tile_coords(p, tile, mt, nt);
       const int row = mt * BM + row_in_tile;
-      const int col0 = nt * BN + wg * 128;
-      const bool row_ok = row < p.R, cols_ok = col0 < p.C;
-      float acc[128];
+      const int col0 = nt * BN + wg * EPI_COLS;
+      const bool row_ok = row < p.R;
+      const int nkb = p.nKB;
+      // scale loads run two blocks ahead of their use
+      auto load_sa = [&](int kb) {
+        return (row_ok && kb < nkb) ? __ldg(p.sA + (long long)kb * p.ld_sA + row) : 0.0f;
+      };
+      auto load_sb = [&](int kb) {
+        return kb < nkb ? __ldg(p.sB + (long long)(col0 / 128) * p.sb_j + (long long)kb * p.sb_k)
+                        : 0.0f;
+      };
+      auto load_cs = [&](int kb) {
+        CsVec v;
+        if (kb < nkb) v = __ldg(reinterpret_cast<const CsVec*>(p.sB + (long long)kb * p.sb_k + col0) + lane);
+        else memset(&v, 0, sizeof(v));
+        return v;
+      };
+      float sa0 = load_sa(0), sa1 = load_sa(1);
+      float sb0 = 0.f, sb1 = 0.f;
+      CsVec cs0, cs1;
+      memset(&cs0, 0, sizeof(cs0));
+      memset(&cs1, 0, sizeof(cs1));
+      if (p.b_col_mode) {
+        cs0 = load_cs(0);
+        cs1 = load_cs(1);
+      } else {
+        sb0 = load_sb(0);
+        sb1 = load_sb(1);
+      }
+      uint64_t acc[CHUNKS][16];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-      float4 cs_next = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (p.b_col_mode && cols_ok) cs_next = __ldg(reinterpret_cast<const float4*>(p.sB + col0) + lane);
-      for (int kb = 0; kb < p.nKB; ++kb, ++acc_it) {
+      for (int c = 0; c < CHUNKS; ++c)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[c][j] = 0ull;
+      for (int kb = 0; kb < nkb; ++kb, ++acc_it) {
         const uint32_t b = acc_it % ACC_BUFS, bph = (acc_it / ACC_BUFS) & 1u;
-        const float sa = row_ok ? __ldg(p.sA + (long long)kb * p.ld_sA + row) : 0.0f;
-        float scale = sa;
+        const float sa = sa0;
+        sa0 = sa1;
+        sa1 = load_sa(kb + 2);
+        uint64_t s2u = 0;
         if (p.b_col_mode) {
-          reinterpret_cast<float4*>(cbuf + (kb & 1) * 128)[lane] = cs_next;
-          if (cols_ok && kb + 1 < p.nKB)
-            cs_next = __ldg(reinterpret_cast<const float4*>(p.sB + (long long)(kb + 1) * p.sb_k + col0) + lane);
+          reinterpret_cast<CsVec*>(cbuf + (kb & 1) * EPI_COLS)[lane] = cs0;
+          cs0 = cs1;
+          cs1 = load_cs(kb + 2);
           __syncwarp();
         } else {
-          const float sb = cols_ok ? __ldg(p.sB + (long long)(col0 / 128) * p.sb_j +
-                                           (long long)kb * p.sb_k)
-                                   : 0.0f;
-          scale = sa * sb;
+          const float sc = sa * sb0;
+          s2u = pack2(sc, sc);
+          sb0 = sb1;
+          sb1 = load_sb(kb + 2);
         }
         if (!mbar_wait(&bars->tfull[b], bph, abort_flag, true)) {
           record_abort(abort_flag, p.err);
@@ -326,43 +546,77 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
         }
         if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
         tc_fence_after();
-        const float* cb = cbuf + (kb & 1) * 128;
+        const uint32_t tbase = taddr_row + b * BN;
+        const uint64_t* cs = reinterpret_cast<const uint64_t*>(cbuf + (kb & 1) * EPI_COLS);
+        const uint64_t sa2 = pack2(sa, sa);
+        uint32_t ra[32], rb[32];
+        tmem_ld32_async(tbase, ra);
+        tmem_wait_ld(ra);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(taddr_row + b * BN + c * 32, r);
-          tmem_wait_ld();
-          if (p.b_col_mode) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), sa * cb[c * 32 + j], acc[c * 32 + j]);
+        for (int c = 0; c < CHUNKS; ++c) {
+          uint32_t (&cur)[32] = (c & 1) ? rb : ra;
+          uint32_t (&nxt)[32] = (c & 1) ? ra : rb;
+          if (c + 1 < CHUNKS) {
+            tmem_ld32_async(tbase + (c + 1) * 32, nxt);
           } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), scale, acc[c * 32 + j]);
+            // the last chunk is in registers: hand the TMEM accumulator back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[b]);
           }
+          if (p.b_col_mode) {
+            uint64_t s2[16];
+            const ulonglong2* cs2 = reinterpret_cast<const ulonglong2*>(cs + c * 16);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const ulonglong2 v = cs2[j];
+              s2[2 * j] = mul_pair(sa2, v.x);
+              s2[2 * j + 1] = mul_pair(sa2, v.y);
+            }
+            fma32_pairs(acc[c], cur, s2);
+          } else {
+            fma32_uniform(acc[c], cur, s2u);
+          }
+          if (c + 1 < CHUNKS) tmem_wait_ld(nxt);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->tempty[b]);
       }
       if (!ok) break;
-      if (row_ok && cols_ok) {
-        if (p.out_fp32) {
+      if (p.out_fp32) {
+        if (row_ok) {
           float* o = static_cast<float*>(p.out) + (size_t)row * p.C + col0;
 #pragma unroll
-          for (int j = 0; j < 128; j += 4)
-            *reinterpret_cast<float4*>(o + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-        } else {
-          uint16_t* o = static_cast<uint16_t*>(p.out) + (size_t)row * p.C + col0;
+          for (int c = 0; c < CHUNKS; ++c)
 #pragma unroll
-          for (int j = 0; j < 128; j += 8)
-            *reinterpret_cast<uint4*>(o + j) =
-                make_uint4(f2_to_bf2(acc[j], acc[j + 1]), f2_to_bf2(acc[j + 2], acc[j + 3]),
-                           f2_to_bf2(acc[j + 4], acc[j + 5]), f2_to_bf2(acc[j + 6], acc[j + 7]));
+            for (int j = 0; j < 16; j += 2) {
+              const float2 a = unpack2(acc[c][j]), bq = unpack2(acc[c][j + 1]);
+              *reinterpret_cast<float4*>(o + c * 32 + 2 * j) = make_float4(a.x, a.y, bq.x, bq.y);
+            }
+        }
+      } else {
+        // bf16: each 32-row × 32-column chunk goes row-major into this warp's
+        // staging buffer and leaves with one TMA store (rows >= R are clipped)
+        uint8_t* ob = outbuf + ew * OUT_CHUNK_BYTES;
+#pragma unroll
+        for (int c = 0; c < CHUNKS; ++c) {
+          if (lane == 0) tma_store_wait_read();   // the previous chunk has left the buffer
+          __syncwarp();
+          uint4* dst = reinterpret_cast<uint4*>(ob + lane * 64);
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) {
+            const float2 a0 = unpack2(acc[c][j]), a1 = unpack2(acc[c][j + 1]);
+            const float2 a2 = unpack2(acc[c][j + 2]), a3 = unpack2(acc[c][j + 3]);
+            dst[j / 4] = make_uint4(f2_to_bf2(a0.x, a0.y), f2_to_bf2(a1.x, a1.y),
+                                    f2_to_bf2(a2.x, a2.y), f2_to_bf2(a3.x, a3.y));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && mt * BM + lq * 32 < p.R)
+            tma_store_2d(&tmOut, smem_u32(ob), col0 + c * 32, mt * BM + lq * 32);
         }
       }
     }
+    // stores must be complete before the CTA (and its shared memory) goes away
+    if (lane == 0) tma_store_wait_all();
   }
 
   // ---------------- teardown ----------------
@@ -394,6 +648,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
+// 2-D bf16 output [rows, cols] stored in boxes of 32 rows × 32 columns.
+bool make_out_map(CUtensorMap* m, void* ptr, uint64_t cols, uint64_t rows) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D E4M3 tensor [outer, inner] (row-major, inner contiguous) loaded in
 // boxes of box_outer rows × 128 bytes with the 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
@@ -411,21 +679,37 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(k_gemm_e4m3_blockscaled, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
+namespace {
+
+template <int BN>
+cudaError_t launch_cfg(const GemmArgs& a, int dev, cudaStream_t st) {
+  using C = Cfg<BN>;
+  auto kern = k_gemm_e4m3_blockscaled<BN>;
+  static int ready[64] = {0};   // 0 = unchecked, 1 = ok, -1 = unusable
+  if (ready[dev] == 0) {
+    // The setmaxnreg split assumes the kernel launches with LAUNCH_REGS
+    // registers per thread; with fewer, the promotion warps could never get theirs.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (fa.numRegs != LAUNCH_REGS) {
+      ready[dev] = -1;
+    } else {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      ready[dev] = 1;
+    }
   }
-  CUtensorMap ta, tb;
+  if (ready[dev] != 1) return cudaErrorInvalidConfiguration;
+  CUtensorMap ta, tb, to;
   if (!make_map(&ta, a.A, (uint64_t)a.Kc, (uint64_t)a.R, BM) ||
       !make_map(&tb, a.B, (uint64_t)a.Kc, (uint64_t)a.C, BN))
     return cudaErrorInvalidValue;
+  if (a.out_fp32) {
+    to = ta;   // unused by the fp32 epilogue
+  } else if (!make_out_map(&to, a.out, (uint64_t)a.C, (uint64_t)a.R)) {
+    return cudaErrorInvalidValue;
+  }
   DevArgs d;
   d.sA = a.sA;
   d.ld_sA = a.ld_sA;
@@ -437,25 +721,28 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   d.C = (int)a.C;
   d.nKB = (int)(a.Kc / BK);
   d.tiles_m = (int)((a.R + BM - 1) / BM);
-  d.tiles_n = (int)((a.C + BN - 1) / BN);
+  d.tiles_n = (int)(a.C / BN);
+  d.m_fastest = a.R <= a.C ? 1 : 0;
   d.b_col_mode = a.b_mode == BScale::kColumn ? 1 : 0;
   d.out_fp32 = a.out_fp32 ? 1 : 0;
   d.err = device_error_word();
   if (d.err == nullptr) return cudaErrorInvalidValue;
-  // The setmaxnreg split assumes the kernel launches with LAUNCH_REGS registers
-  // per thread; with fewer, the promotion warpgroups could never get theirs.
-  static int regs_checked[64] = {0};
-  if (dev < 64 && regs_checked[dev] == 0) {
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, k_gemm_e4m3_blockscaled);
-    if (e != cudaSuccess) return e;
-    regs_checked[dev] = fa.numRegs == LAUNCH_REGS ? 1 : -1;
-  }
-  if (dev >= 64 || regs_checked[dev] != 1) return cudaErrorInvalidConfiguration;
   const int tiles = d.tiles_m * d.tiles_n;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  k_gemm_e4m3_blockscaled<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, d);
+  kern<<<grid, THREADS, C::SMEM_BYTES, st>>>(ta, tb, to, d);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  // 128×256 tiles where the output width allows, else 128×128
+  if (a.C % 256 == 0) return launch_cfg<256>(a, dev, st);
+  return launch_cfg<128>(a, dev, st);
 }
 
 }  // namespace jetfp8

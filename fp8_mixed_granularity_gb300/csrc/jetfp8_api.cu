@@ -41,18 +41,22 @@ DeviceInfo* current_device() {
   return d->ok ? d : nullptr;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 jetfp8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? JETFP8_OK : JETFP8_ERR_CUDA; }
 
 // Validation helpers ---------------------------------------------------------
 struct Check {
   jetfp8_status st = JETFP8_OK;
-  Check& ptr(const void* p, bool required = true) {
+  // E4M3 / FP32 arrays: 16-byte aligned
+  Check& ptr(const void* p, bool required = true) { return ptr_aligned(p, 16, required); }
+  // bf16 tensors: 32-byte aligned
+  Check& bf(const void* p, bool required = true) { return ptr_aligned(p, 32, required); }
+  Check& ptr_aligned(const void* p, uintptr_t a, bool required) {
     if (st != JETFP8_OK) return *this;
     if (p == nullptr) {
       if (required) st = JETFP8_ERR_INVALID_ARG;
-    } else if (!aligned16(p)) {
+    } else if (!aligned(p, a)) {
       st = JETFP8_ERR_MISALIGNED;
     }
     return *this;
@@ -132,7 +136,7 @@ jetfp8_status jetfp8_get_last_device_error(cudaStream_t stream) {
 jetfp8_status jetfp8_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, uint8_t* q,
                                      float* s, cudaStream_t stream) {
   Check c;
-  c.ptr(x_bf16).ptr(q).ptr(s).positive(M).mult128(K).fits(M, K).device();
+  c.bf(x_bf16).ptr(q).ptr(s).positive(M).mult128(K).fits(M, K).device();
   if (c.st != JETFP8_OK) return c.st;
   return from_cuda(launch_quant_rowgroups(x_bf16, M, K, q, s, stream));
 }
@@ -140,7 +144,7 @@ jetfp8_status jetfp8_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, u
 jetfp8_status jetfp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K, uint8_t* q,
                                           float* s, uint8_t* qT, cudaStream_t stream) {
   Check c;
-  c.ptr(w_bf16).ptr(q).ptr(s).ptr(qT, false).mult128(N).mult128(K).fits(N, K).device();
+  c.bf(w_bf16).ptr(q).ptr(s).ptr(qT, false).mult128(N).mult128(K).fits(N, K).device();
   if (c.st != JETFP8_OK) return c.st;
   return from_cuda(launch_quant_weight(w_bf16, N, K, q, s, qT, stream));
 }
@@ -158,7 +162,7 @@ jetfp8_status jetfp8_quant_grad_dual(const void* dy_bf16, int64_t M, int64_t N, 
                                      float* s_row, uint8_t* qT_col, float* sT_col,
                                      cudaStream_t stream) {
   Check c;
-  c.ptr(dy_bf16).ptr(q_row).ptr(s_row).ptr(qT_col, false).ptr(sT_col, false).positive(M)
+  c.bf(dy_bf16).ptr(q_row).ptr(s_row).ptr(qT_col, false).ptr(sT_col, false).positive(M)
       .mult128(N).fits(M, N).device();
   if (c.st != JETFP8_OK) return c.st;
   if ((qT_col == nullptr) != (sT_col == nullptr)) return JETFP8_ERR_INVALID_ARG;
@@ -170,7 +174,7 @@ jetfp8_status jetfp8_rmsnorm_quant(const void* x_bf16, const void* gamma_bf16, f
                                    int64_t M, int64_t H, uint8_t* q, float* s, float* rstd,
                                    void* y_bf16, cudaStream_t stream) {
   Check c;
-  c.ptr(x_bf16).ptr(gamma_bf16).ptr(q).ptr(s).ptr(rstd).ptr(y_bf16, false).positive(M)
+  c.bf(x_bf16).bf(gamma_bf16).ptr(q).ptr(s).ptr(rstd).bf(y_bf16, false).positive(M)
       .mult128(H).fits(M, H).device();
   if (c.st != JETFP8_OK) return c.st;
   if (!(eps >= 0.0f)) return JETFP8_ERR_INVALID_ARG;
@@ -186,7 +190,7 @@ jetfp8_status jetfp8_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_
                                 const float* sw, int64_t M, int64_t N, int64_t K, void* y,
                                 jetfp8_out_dtype out_dtype, cudaStream_t stream) {
   Check c;
-  c.ptr(xq).ptr(sx).ptr(wq).ptr(sw).ptr(y).positive(M).mult128(N).mult128(K).fits(M, K)
+  c.ptr(xq).ptr(sx).ptr(wq).ptr(sw).bf(y).positive(M).mult128(N).mult128(K).fits(M, K)
       .fits(N, K).fits(M, N).device();
   if (c.st != JETFP8_OK) return c.st;
   GemmArgs g{xq, wq, sx, round_up4(M), sw, K / 128, 1, BScale::kBlock,
@@ -198,7 +202,7 @@ jetfp8_status jetfp8_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint
                                 const float* sw, int64_t M, int64_t N, int64_t K, void* dx,
                                 jetfp8_out_dtype out_dtype, cudaStream_t stream) {
   Check c;
-  c.ptr(dyq).ptr(sdy).ptr(wqT).ptr(sw).ptr(dx).positive(M).mult128(N).mult128(K).fits(M, N)
+  c.ptr(dyq).ptr(sdy).ptr(wqT).ptr(sw).bf(dx).positive(M).mult128(N).mult128(K).fits(M, N)
       .fits(N, K).fits(M, K).device();
   if (c.st != JETFP8_OK) return c.st;
   // contraction over N (block kb = n/128), output columns over K (block j/128)
@@ -211,7 +215,7 @@ jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const ui
                                 const float* sxT, int64_t M, int64_t N, int64_t K, void* dw,
                                 jetfp8_out_dtype out_dtype, cudaStream_t stream) {
   Check c;
-  c.ptr(dyqT).ptr(sdyT).ptr(xqT).ptr(sxT).ptr(dw).mult128(M).mult128(N).mult128(K).fits(M, N)
+  c.ptr(dyqT).ptr(sdyT).ptr(xqT).ptr(sxT).bf(dw).mult128(M).mult128(N).mult128(K).fits(M, N)
       .fits(M, K).fits(N, K).device();
   if (c.st != JETFP8_OK) return c.st;
   // contraction over tokens (block kb = m/128); per-row scale sdyT[kb][n], per-column sxT[kb][k]
@@ -223,7 +227,7 @@ jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const ui
 jetfp8_status jetfp8_swiglu_quant(const void* gu_bf16, int64_t M, int64_t I, uint8_t* q, float* s,
                                   void* h_bf16, cudaStream_t stream) {
   Check c;
-  c.ptr(gu_bf16).ptr(q).ptr(s).ptr(h_bf16, false).positive(M).mult128(I).fits(M, 2 * I).device();
+  c.bf(gu_bf16).ptr(q).ptr(s).bf(h_bf16, false).positive(M).mult128(I).fits(M, 2 * I).device();
   if (c.st != JETFP8_OK) return c.st;
   return from_cuda(launch_swiglu_quant(gu_bf16, M, I, q, s, h_bf16, stream));
 }
@@ -231,7 +235,7 @@ jetfp8_status jetfp8_swiglu_quant(const void* gu_bf16, int64_t M, int64_t I, uin
 jetfp8_status jetfp8_swiglu_bwd(const void* gu_bf16, const void* dh_bf16, int64_t M, int64_t I,
                                 void* dgu_bf16, cudaStream_t stream) {
   Check c;
-  c.ptr(gu_bf16).ptr(dh_bf16).ptr(dgu_bf16).positive(M).mult128(I).fits(M, 2 * I).device();
+  c.bf(gu_bf16).bf(dh_bf16).bf(dgu_bf16).positive(M).mult128(I).fits(M, 2 * I).device();
   if (c.st != JETFP8_OK) return c.st;
   return from_cuda(launch_swiglu_bwd(gu_bf16, dh_bf16, M, I, dgu_bf16, stream));
 }

@@ -25,49 +25,75 @@ int num_sms();
 bool device_is_sm103();
 
 // -------------------------------------------------------------------------
-// E4M3 quantisation with an exact FP32 quotient
+// E4M3 quantisation of the correctly rounded FP32 quotient
 // -------------------------------------------------------------------------
+// Packed FP32 pair arithmetic (one instruction for two lanes of data).
+__device__ __forceinline__ uint64_t f2_bits(float2 v) {
+  return (uint64_t)__float_as_uint(v.x) | ((uint64_t)__float_as_uint(v.y) << 32);
+}
+__device__ __forceinline__ float2 bits_f2(uint64_t b) {
+  return make_float2(__uint_as_float((uint32_t)b), __uint_as_float((uint32_t)(b >> 32)));
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
+}
+
+// Bracketing factors 1 ± 2^-20 (exact in FP32).
+constexpr float kBracketUp = 1.0f + 0x1p-20f;
+constexpr float kBracketDn = 1.0f - 0x1p-20f;
+
 struct GroupScale {
   float s;      // S = fp32(amax/448), or 1 when amax == 0
-  float rs;     // fp32(1/S), for the fast quotient
-  bool exact;   // S is so small that 1/S may overflow: always divide
+  float ra;     // fp32(1/S)·(1 + 2^-20), rounded
+  float rb;     // fp32(1/S)·(1 - 2^-20), rounded
+  bool exact;   // 1/S is 1e37 or more (or not finite): always divide
 };
 
 __device__ __forceinline__ GroupScale make_scale(float amax) {
   GroupScale g;
   g.s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, kE4M3Max);
-  g.rs = __frcp_rn(g.s);
-  g.exact = !(g.rs < 1.0e37f);
+  const float rs = __frcp_rn(g.s);
+  g.exact = !(rs < 1.0e37f);
+  g.ra = __fmul_rn(rs, kBracketUp);
+  g.rb = __fmul_rn(rs, kBracketDn);
   return g;
 }
 
-// fp32(x/S) exactly as a correctly rounded division would give it, as far as
-// the E4M3 code of the result is concerned.  q~ = x·RN(1/S) lies within two
-// FP32 ulps of x/S, so it can sit on the other side of an E4M3 rounding
-// boundary from RN(x/S) only if it is within a few ulps of that boundary.  In
-// the E4M3 normal range (|q| >= 2^-6) the boundaries are the midpoints between
-// neighbouring codes, whose FP32 encodings have the low 20 mantissa bits equal
-// to 0x80000.  Inputs within 4 ulps of such a midpoint, or below 2^-6 (where
-// the boundaries sit elsewhere), take the IEEE division instead.
-__device__ __forceinline__ float quotient(float x, const GroupScale& g) {
-  float q = __fmul_rn(x, g.rs);
-  uint32_t u = __float_as_uint(q);
-  bool near_tie = ((u & 0xFFFFFu) - (0x80000u - 4u)) <= 8u;
-  bool small = (u & 0x7FFFFFFFu) < 0x3C800000u;   // |q| < 2^-6
-  if (near_tie || small || g.exact) q = __fdiv_rn(x, g.s);
-  return q;
-}
-
-// Two FP32 values -> two E4M3 codes; v0 lands in the low byte (lower address).
+// Two E4M3 codes (v0 in the low byte) from two FP32 values.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float v0, float v1) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
   return (uint32_t)r;
 }
 
+// E4M3(fp32(v/S)) for two values that share the scale S, without a division
+// in the common case.  With ra, rb = 1/S·(1 ± 2^-20) (each within 2^-23
+// relative of that), a = v·ra and b = v·rb bracket the correctly rounded
+// quotient RN(v/S) strictly: they sit at least 2^-20 - 4·2^-24 relative away
+// from v/S on either side, while RN(v/S) is within 2^-24.  E4M3 rounding
+// (nearest-even, saturating) is monotone, so if a and b round to the same code,
+// RN(v/S) rounds to it too.  Otherwise — a quotient within about 2^-20 of an
+// E4M3 rounding boundary, or a scale whose reciprocal overflows — the IEEE
+// division decides.  Zeros keep their sign on both paths.
+__device__ __forceinline__ uint32_t quant_pair(float2 v, const GroupScale& g) {
+  const float2 a = mul2(v, make_float2(g.ra, g.ra));
+  const float2 b = mul2(v, make_float2(g.rb, g.rb));
+  uint32_t ca = cvt_e4m3x2(a.x, a.y);
+  const uint32_t cb = cvt_e4m3x2(b.x, b.y);
+  if (ca != cb || g.exact) ca = cvt_e4m3x2(__fdiv_rn(v.x, g.s), __fdiv_rn(v.y, g.s));
+  return ca;
+}
+
+// Four values sharing one scale -> four codes, first value in the low byte.
 __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, const GroupScale& g) {
-  return cvt_e4m3x2(quotient(a, g), quotient(b, g)) |
-         (cvt_e4m3x2(quotient(c, g), quotient(d, g)) << 16);
+  return quant_pair(make_float2(a, b), g) | (quant_pair(make_float2(c, d), g) << 16);
 }
 
 // Two E4M3 codes (low byte first) -> two exact floats.

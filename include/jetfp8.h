@@ -24,8 +24,10 @@
  *    tensor quantised in 1×128 row groups are stored as S[g][r] with row
  *    stride ld = roundup(R, 4), i.e. an array of (C/128) × ld floats; padding
  *    entries are never read and may be left unwritten.
- *  - Every pointer argument is a DEVICE pointer owned by the caller, 16-byte
- *    aligned, and must stay valid until the work on `stream` completes.  The
+ *  - Every pointer argument is a DEVICE pointer owned by the caller and must
+ *    stay valid until the work on `stream` completes.  bf16 tensors must be
+ *    32-byte aligned (they move with 256-bit accesses); E4M3 and FP32 arrays
+ *    16-byte aligned (JETFP8_ERR_MISALIGNED otherwise).  The
  *    library allocates no device memory and keeps no pointer after a call
  *    returns.  A null `stream` is the legacy default stream.
  *  - Shapes: every length named K, N, H or I must be a positive multiple of
@@ -55,7 +57,7 @@ typedef enum {
   JETFP8_OK = 0,
   JETFP8_ERR_INVALID_ARG = 1,       /* null pointer, non-positive size, bad enum */
   JETFP8_ERR_UNSUPPORTED_SHAPE = 2, /* a length violates the multiple-of-128 rules */
-  JETFP8_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
+  JETFP8_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment rule above */
   JETFP8_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed */
   JETFP8_ERR_TIMEOUT = 5,           /* a device-side bounded wait expired */
   JETFP8_ERR_UNSUPPORTED = 6        /* device is not sm_103, or feature not built */

@@ -59,12 +59,13 @@ def test_validation_rejects_before_touching_the_device(lib):
     CUDA call (so this runs on a machine without a GPU)."""
     P = ctypes.c_void_p
     # null input
-    assert lib.jetfp8_quant_act_1x128(None, 4, 128, P(16), P(16), None) == 1
+    assert lib.jetfp8_quant_act_1x128(None, 4, 128, P(64), P(64), None) == 1
     # K not a multiple of 128
-    assert lib.jetfp8_quant_act_1x128(P(16), 4, 100, P(16), P(16), None) == 2
+    assert lib.jetfp8_quant_act_1x128(P(64), 4, 100, P(64), P(64), None) == 2
     # misaligned pointer
-    assert lib.jetfp8_quant_act_1x128(P(18), 4, 128, P(16), P(16), None) == 3
+    assert lib.jetfp8_quant_act_1x128(P(48), 4, 128, P(64), P(64), None) == 3   # bf16 needs 32 B
+    assert lib.jetfp8_quant_act_1x128(P(64), 4, 128, P(72), P(64), None) == 3   # E4M3 needs 16 B
     # WGrad needs M multiple of 128
-    assert lib.jetfp8_gemm_wgrad(P(16), P(16), P(16), P(16), 100, 128, 128, P(16), 0, None) == 2
-    # bad output dtype is caught after shape checks, before the launch
-    assert lib.jetfp8_gemm_fprop(P(16), P(16), P(16), P(16), 0, 128, 128, P(16), 0, None) == 1
+    assert lib.jetfp8_gemm_wgrad(P(64), P(64), P(64), P(64), 100, 128, 128, P(64), 0, None) == 2
+    # non-positive M
+    assert lib.jetfp8_gemm_fprop(P(64), P(64), P(64), P(64), 0, 128, 128, P(64), 0, None) == 1
