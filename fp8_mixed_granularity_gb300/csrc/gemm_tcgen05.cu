@@ -32,6 +32,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "jetfp8_common.cuh"
 #include "jetfp8_internal.h"
 
@@ -49,8 +51,8 @@ constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 384
 // the launch total, or setmaxnreg.inc would wait forever.  The host refuses to
 // launch unless the compiled kernel uses exactly LAUNCH_REGS.
 constexpr int LAUNCH_REGS = 168;
-constexpr int CTRL_REGS = 40;
-constexpr int EPI_REGS = 232;
+constexpr int CTRL_REGS = 24;
+constexpr int EPI_REGS = 240;
 static_assert(128 * CTRL_REGS + 256 * EPI_REGS <= THREADS * LAUNCH_REGS, "register split");
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int MAX_STAGES = 8, MAX_BUFS = 4;
@@ -97,7 +99,7 @@ struct DevArgs {
   void* out;
   int R, C, nKB, tiles_m, tiles_n;
   int m_fastest;   // tile order: 1 = consecutive tiles walk down M (share a B tile)
-  int b_col_mode, out_fp32;
+  int out_fp32;
   unsigned* err;
 };
 
@@ -352,6 +354,7 @@ __device__ __forceinline__ void fma32_pairs(uint64_t (&acc)[16], const uint32_t 
 }
 
 
+
 template <int EPI_COLS>
 struct ColScaleVec;
 template <>
@@ -363,7 +366,7 @@ struct ColScaleVec<128> {
   using T = float4;
 };
 
-template <int BN_>
+template <int BN_, bool COLS>
 __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -492,79 +495,78 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
       const int col0 = nt * BN + wg * EPI_COLS;
       const bool row_ok = row < p.R;
       const int nkb = p.nKB;
-      // scale loads run two blocks ahead of their use
+      // Scales are prefetched two blocks ahead into a two-slot register ring;
+      // the block loop is unrolled by two so every slot index is a
+      // compile-time constant and no register copy waits on a load in flight.
+      const float* sa_ptr = p.sA + row;
+      const float* sb_ptr = p.sB + (COLS ? (long long)col0 : (long long)(col0 / 128) * p.sb_j);
       auto load_sa = [&](int kb) {
-        return (row_ok && kb < nkb) ? __ldg(p.sA + (long long)kb * p.ld_sA + row) : 0.0f;
+        return (row_ok && kb < nkb) ? __ldg(sa_ptr + (long long)kb * p.ld_sA) : 0.0f;
       };
       auto load_sb = [&](int kb) {
-        return kb < nkb ? __ldg(p.sB + (long long)(col0 / 128) * p.sb_j + (long long)kb * p.sb_k)
-                        : 0.0f;
+        return kb < nkb ? __ldg(sb_ptr + (long long)kb * p.sb_k) : 0.0f;
       };
       auto load_cs = [&](int kb) {
         CsVec v;
-        if (kb < nkb) v = __ldg(reinterpret_cast<const CsVec*>(p.sB + (long long)kb * p.sb_k + col0) + lane);
+        if (kb < nkb) v = __ldg(reinterpret_cast<const CsVec*>(sb_ptr + (long long)kb * p.sb_k) + lane);
         else memset(&v, 0, sizeof(v));
         return v;
       };
-      float sa0 = load_sa(0), sa1 = load_sa(1);
-      float sb0 = 0.f, sb1 = 0.f;
-      CsVec cs0, cs1;
-      memset(&cs0, 0, sizeof(cs0));
-      memset(&cs1, 0, sizeof(cs1));
-      if (p.b_col_mode) {
-        cs0 = load_cs(0);
-        cs1 = load_cs(1);
+      float sa_r[2], sb_r[2];
+      CsVec cs_r[2];
+      sa_r[0] = load_sa(0);
+      sa_r[1] = load_sa(1);
+      if (COLS) {
+        cs_r[0] = load_cs(0);
+        cs_r[1] = load_cs(1);
       } else {
-        sb0 = load_sb(0);
-        sb1 = load_sb(1);
+        sb_r[0] = load_sb(0);
+        sb_r[1] = load_sb(1);
       }
       uint64_t acc[CHUNKS][16];
 #pragma unroll
       for (int c = 0; c < CHUNKS; ++c)
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[c][j] = 0ull;
-      for (int kb = 0; kb < nkb; ++kb, ++acc_it) {
+
+      // one 128-deep block; SL is the ring slot of this block's scales
+      auto block = [&](int kb, auto slot) -> bool {
+        constexpr int SL = decltype(slot)::value;
         const uint32_t b = acc_it % ACC_BUFS, bph = (acc_it / ACC_BUFS) & 1u;
-        const float sa = sa0;
-        sa0 = sa1;
-        sa1 = load_sa(kb + 2);
+        ++acc_it;
+        const float sa = sa_r[SL];
+        sa_r[SL] = load_sa(kb + 2);
         uint64_t s2u = 0;
-        if (p.b_col_mode) {
-          reinterpret_cast<CsVec*>(cbuf + (kb & 1) * EPI_COLS)[lane] = cs0;
-          cs0 = cs1;
-          cs1 = load_cs(kb + 2);
+        if (COLS) {
+          reinterpret_cast<CsVec*>(cbuf + SL * EPI_COLS)[lane] = cs_r[SL];
+          cs_r[SL] = load_cs(kb + 2);
           __syncwarp();
         } else {
-          const float sc = sa * sb0;
+          const float sc = sa * sb_r[SL];
           s2u = pack2(sc, sc);
-          sb0 = sb1;
-          sb1 = load_sb(kb + 2);
+          sb_r[SL] = load_sb(kb + 2);
         }
-        if (!mbar_wait(&bars->tfull[b], bph, abort_flag, true)) {
-          record_abort(abort_flag, p.err);
-          ok = false;
-        }
-        if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+        bool good = mbar_wait(&bars->tfull[b], bph, abort_flag, true);
+        if (!good) record_abort(abort_flag, p.err);
+        if (__any_sync(0xffffffffu, !good)) return false;
         tc_fence_after();
         const uint32_t tbase = taddr_row + b * BN;
-        const uint64_t* cs = reinterpret_cast<const uint64_t*>(cbuf + (kb & 1) * EPI_COLS);
+        const uint64_t* cs = reinterpret_cast<const uint64_t*>(cbuf + SL * EPI_COLS);
         const uint64_t sa2 = pack2(sa, sa);
-        uint32_t ra[32], rb[32];
-        tmem_ld32_async(tbase, ra);
-        tmem_wait_ld(ra);
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c) {
-          uint32_t (&cur)[32] = (c & 1) ? rb : ra;
-          uint32_t (&nxt)[32] = (c & 1) ? ra : rb;
-          if (c + 1 < CHUNKS) {
-            tmem_ld32_async(tbase + (c + 1) * 32, nxt);
-          } else {
+          // TMEM loads are short (tens of cycles); loading each chunk right
+          // before its FMAs keeps only 32 partial registers live
+          uint32_t cur[32];
+          tmem_ld32_async(tbase + c * 32, cur);
+          tmem_wait_ld(cur);
+          if (c + 1 == CHUNKS) {
             // the last chunk is in registers: hand the TMEM accumulator back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->tempty[b]);
           }
-          if (p.b_col_mode) {
+          if (COLS) {
             uint64_t s2[16];
             const ulonglong2* cs2 = reinterpret_cast<const ulonglong2*>(cs + c * 16);
 #pragma unroll
@@ -577,7 +579,14 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
           } else {
             fma32_uniform(acc[c], cur, s2u);
           }
-          if (c + 1 < CHUNKS) tmem_wait_ld(nxt);
+        }
+        return true;
+      };
+      for (int kb = 0; kb < nkb; kb += 2) {
+        if (!block(kb, std::integral_constant<int, 0>{}) ||
+            (kb + 1 < nkb && !block(kb + 1, std::integral_constant<int, 1>{}))) {
+          ok = false;
+          break;
         }
       }
       if (!ok) break;
@@ -630,6 +639,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -681,10 +691,10 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 
 namespace {
 
-template <int BN>
+template <int BN, bool COLS>
 cudaError_t launch_cfg(const GemmArgs& a, int dev, cudaStream_t st) {
   using C = Cfg<BN>;
-  auto kern = k_gemm_e4m3_blockscaled<BN>;
+  auto kern = k_gemm_e4m3_blockscaled<BN, COLS>;
   static int ready[64] = {0};   // 0 = unchecked, 1 = ok, -1 = unusable
   if (ready[dev] == 0) {
     // The setmaxnreg split assumes the kernel launches with LAUNCH_REGS
@@ -723,7 +733,6 @@ cudaError_t launch_cfg(const GemmArgs& a, int dev, cudaStream_t st) {
   d.tiles_m = (int)((a.R + BM - 1) / BM);
   d.tiles_n = (int)(a.C / BN);
   d.m_fastest = a.R <= a.C ? 1 : 0;
-  d.b_col_mode = a.b_mode == BScale::kColumn ? 1 : 0;
   d.out_fp32 = a.out_fp32 ? 1 : 0;
   d.err = device_error_word();
   if (d.err == nullptr) return cudaErrorInvalidValue;
@@ -733,6 +742,7 @@ cudaError_t launch_cfg(const GemmArgs& a, int dev, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
@@ -740,9 +750,10 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  // 128×256 tiles where the output width allows, else 128×128
-  if (a.C % 256 == 0) return launch_cfg<256>(a, dev, st);
-  return launch_cfg<128>(a, dev, st);
+  // 128×256 tiles (two TMEM accumulators) where the output width allows, else 128×128
+  const bool cols = a.b_mode == BScale::kColumn;
+  if (a.C % 256 == 0) return cols ? launch_cfg<256, true>(a, dev, st) : launch_cfg<256, false>(a, dev, st);
+  return cols ? launch_cfg<128, true>(a, dev, st) : launch_cfg<128, false>(a, dev, st);
 }
 
 }  // namespace jetfp8
