@@ -21,12 +21,22 @@
 //   warps 2-3   idle; with warps 0-1 they form the control warpgroup, which
 //               gives registers back (setmaxnreg.dec) to the promotion warps.
 //   warps 4-11  two warpgroups; warpgroup w owns output columns
-//               [w·BN/2, (w+1)·BN/2) of the tile and each thread one row (its
-//               TMEM lane).  Per block they load the partial 32 columns at a
-//               time (the next chunk's load overlapping the current chunk's
-//               FMAs), hand the accumulator back as soon as the last chunk is
-//               in registers, and promote with packed FP32 FMAs; after the
-//               last block the row is written out as bf16 or fp32.
+//               [w·BN/2, (w+1)·BN/2) of the tile, each warp the 32 TMEM lanes
+//               (tile rows) it may access.  Per block they load the partial
+//               from TMEM, hand the accumulator back as soon as the last piece
+//               is in registers, and promote with packed FP32 arithmetic;
+//               after the last block the tile is written out as bf16 or fp32.
+//               Scales are prefetched two blocks ahead into registers.
+//     uniform scales (FProp, DGrad: sB is one value per 128 output columns):
+//               each thread owns one row and 32-column chunks of it;
+//               promotion is one FMA per element with the product sA·sB.
+//     column scales (WGrad: sB is one value per output column): the partial
+//               is read as 16-lane × 256-bit fragments, so a thread holds 4
+//               rows × 2 adjacent columns of every 8 and needs only a quarter
+//               of the column scales; each block the warp stages its row and
+//               column scales once through shared memory in that order.
+//               Promotion is (partial·sB)·sA, a multiply and an FMA per
+//               element, with the next fragment's TMEM load in flight.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records an
 // error word, lets copies and MMAs in flight land, frees TMEM and returns.
 #include <cuda.h>
@@ -58,6 +68,9 @@ constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int MAX_STAGES = 8, MAX_BUFS = 4;
 // bf16 output leaves through shared memory in 32-row × 32-column chunks, one
 // 2 KB staging buffer per promotion warp, written to global memory by TMA.
+// The buffer uses the 64-byte swizzle: the 16-byte granule g of row r sits at
+// r·64 + 16·(g ^ ((r/2) mod 4)), so rows written by neighbouring lanes fall on
+// different banks.
 constexpr int OUT_CHUNK_BYTES = 32 * 32 * 2;
 
 template <int BN_>
@@ -74,11 +87,20 @@ struct Cfg {
   // both K-major, N/8 at bits 17-22, M/16 at bits 24-28.
   static constexpr uint32_t IDESC =
       (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-  static constexpr int COLBUF_BYTES = EPI_WARPS * 2 * EPI_COLS * 4;
+  // Column-mode scale staging, per promotion warp and ring slot: the warp's
+  // 32 row scales, then its column scales ordered [g][GS] where group
+  // g = (c mod 8)/2 holds the columns c = 8j + 2g + {0,1} at 2j + {0,1} (GS
+  // pads the groups onto different banks).
+  static constexpr int GS = EPI_COLS / 4 + 4;
+  static constexpr int CB_F = 32 + 4 * GS;
+  static constexpr int COLBUF_BYTES = EPI_WARPS * 2 * CB_F * 4;
   static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES +
                                     1024 /*barriers*/ + COLBUF_BYTES + EPI_WARPS * OUT_CHUNK_BYTES;
   static_assert(STAGES <= MAX_STAGES && ACC_BUFS <= MAX_BUFS, "barrier arrays");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(GS % 4 == 0 && CB_F % 4 == 0, "16-byte aligned staging fields");
+  static_assert(COLBUF_BYTES % 128 == 0 && OUT_CHUNK_BYTES % 128 == 0,
+                "output staging buffers (TMA store sources) 128-byte aligned");
 };
 
 struct Barriers {
@@ -234,11 +256,6 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
   return r;
 }
-__device__ __forceinline__ uint64_t mul_pair(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 
 // Starts loading 32 TMEM columns into r[0..31]; the values are valid only
 // after tmem_wait_ld(r).
@@ -305,55 +322,68 @@ __device__ __forceinline__ void fma32_uniform(uint64_t (&acc)[16], const uint32_
         "r"(p[30]), "r"(p[31]), "l"(s2));
 }
 
-// acc[j] += (p[2j], p[2j+1]) · s2[j] for 16 packed FP32 pairs.
-__device__ __forceinline__ void fma32_pairs(uint64_t (&acc)[16], const uint32_t (&p)[32], const uint64_t (&s2)[16]) {
-  asm("{\n\t.reg .b64 q;\n\t"
-      "mov.b64 q, {%16, %17};\n\t"
-      "fma.rn.f32x2 %0, q, %48, %0;\n\t"
-      "mov.b64 q, {%18, %19};\n\t"
-      "fma.rn.f32x2 %1, q, %49, %1;\n\t"
-      "mov.b64 q, {%20, %21};\n\t"
-      "fma.rn.f32x2 %2, q, %50, %2;\n\t"
-      "mov.b64 q, {%22, %23};\n\t"
-      "fma.rn.f32x2 %3, q, %51, %3;\n\t"
-      "mov.b64 q, {%24, %25};\n\t"
-      "fma.rn.f32x2 %4, q, %52, %4;\n\t"
-      "mov.b64 q, {%26, %27};\n\t"
-      "fma.rn.f32x2 %5, q, %53, %5;\n\t"
-      "mov.b64 q, {%28, %29};\n\t"
-      "fma.rn.f32x2 %6, q, %54, %6;\n\t"
-      "mov.b64 q, {%30, %31};\n\t"
-      "fma.rn.f32x2 %7, q, %55, %7;\n\t"
-      "mov.b64 q, {%32, %33};\n\t"
-      "fma.rn.f32x2 %8, q, %56, %8;\n\t"
-      "mov.b64 q, {%34, %35};\n\t"
-      "fma.rn.f32x2 %9, q, %57, %9;\n\t"
-      "mov.b64 q, {%36, %37};\n\t"
-      "fma.rn.f32x2 %10, q, %58, %10;\n\t"
-      "mov.b64 q, {%38, %39};\n\t"
-      "fma.rn.f32x2 %11, q, %59, %11;\n\t"
-      "mov.b64 q, {%40, %41};\n\t"
-      "fma.rn.f32x2 %12, q, %60, %12;\n\t"
-      "mov.b64 q, {%42, %43};\n\t"
-      "fma.rn.f32x2 %13, q, %61, %13;\n\t"
-      "mov.b64 q, {%44, %45};\n\t"
-      "fma.rn.f32x2 %14, q, %62, %14;\n\t"
-      "mov.b64 q, {%46, %47};\n\t"
-      "fma.rn.f32x2 %15, q, %63, %15;\n\t"
-      "}"
-      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]),
-        "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
-      : "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]),
-        "r"(p[6]), "r"(p[7]), "r"(p[8]), "r"(p[9]), "r"(p[10]), "r"(p[11]),
-        "r"(p[12]), "r"(p[13]), "r"(p[14]), "r"(p[15]), "r"(p[16]), "r"(p[17]),
-        "r"(p[18]), "r"(p[19]), "r"(p[20]), "r"(p[21]), "r"(p[22]), "r"(p[23]),
-        "r"(p[24]), "r"(p[25]), "r"(p[26]), "r"(p[27]), "r"(p[28]), "r"(p[29]),
-        "r"(p[30]), "r"(p[31]), "l"(s2[0]), "l"(s2[1]), "l"(s2[2]), "l"(s2[3]),
-        "l"(s2[4]), "l"(s2[5]), "l"(s2[6]), "l"(s2[7]), "l"(s2[8]), "l"(s2[9]),
-        "l"(s2[10]), "l"(s2[11]), "l"(s2[12]), "l"(s2[13]), "l"(s2[14]), "l"(s2[15]));
+// 16-lane × 256-bit TMEM fragments, four of them side by side (16 rows × 32
+// columns): for j < 4, r[4j], r[4j+1] are row lane/4 and r[4j+2], r[4j+3]
+// row lane/4 + 8 (of the 16 lanes addressed), both at columns
+// 8j + 2·(lane mod 4) + {0, 1}.  Valid after tmem_wait_ld16(r).
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
 }
 
-
+// Column-scale promotion of one fragment (layout of tmem_ld16x256_x4):
+//   acc[2j]   += ({p[4j],   p[4j+1]} · sb[j]) · sa_lo      (row lane/4)
+//   acc[2j+1] += ({p[4j+2], p[4j+3]} · sb[j]) · sa_hi      (row lane/4 + 8)
+// sb[j] holds the scales of the fragment's two columns, sa_lo / sa_hi the
+// row scale twice.  All eight products are formed before the eight FMAs, so
+// no FMA waits on the multiply just before it.  Volatile so that it stays
+// between the TMEM load of the next fragment and the wait for it.
+__device__ __forceinline__ void promote_cols_frag(uint64_t* acc, const uint32_t (&p)[16],
+                                                  const uint64_t (&sb)[4], uint64_t sa_lo, uint64_t sa_hi) {
+  asm volatile(
+      "{\n\t.reg .b64 q0, q1, q2, q3, q4, q5, q6, q7;\n\t"
+      "mov.b64 q0, {%8, %9};\n\t"
+      "mov.b64 q1, {%10, %11};\n\t"
+      "mov.b64 q2, {%12, %13};\n\t"
+      "mov.b64 q3, {%14, %15};\n\t"
+      "mov.b64 q4, {%16, %17};\n\t"
+      "mov.b64 q5, {%18, %19};\n\t"
+      "mov.b64 q6, {%20, %21};\n\t"
+      "mov.b64 q7, {%22, %23};\n\t"
+      "mul.rn.f32x2 q0, q0, %24;\n\t"
+      "mul.rn.f32x2 q1, q1, %24;\n\t"
+      "mul.rn.f32x2 q2, q2, %25;\n\t"
+      "mul.rn.f32x2 q3, q3, %25;\n\t"
+      "mul.rn.f32x2 q4, q4, %26;\n\t"
+      "mul.rn.f32x2 q5, q5, %26;\n\t"
+      "mul.rn.f32x2 q6, q6, %27;\n\t"
+      "mul.rn.f32x2 q7, q7, %27;\n\t"
+      "fma.rn.f32x2 %0, q0, %28, %0;\n\t"
+      "fma.rn.f32x2 %1, q1, %29, %1;\n\t"
+      "fma.rn.f32x2 %2, q2, %28, %2;\n\t"
+      "fma.rn.f32x2 %3, q3, %29, %3;\n\t"
+      "fma.rn.f32x2 %4, q4, %28, %4;\n\t"
+      "fma.rn.f32x2 %5, q5, %29, %5;\n\t"
+      "fma.rn.f32x2 %6, q6, %28, %6;\n\t"
+      "fma.rn.f32x2 %7, q7, %29, %7;\n\t"
+      "}"
+      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]),
+        "+l"(acc[7])
+      : "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7]), "r"(p[8]),
+        "r"(p[9]), "r"(p[10]), "r"(p[11]), "r"(p[12]), "r"(p[13]), "r"(p[14]), "r"(p[15]), "l"(sb[0]),
+        "l"(sb[1]), "l"(sb[2]), "l"(sb[3]), "l"(sa_lo), "l"(sa_hi));
+}
 
 template <int EPI_COLS>
 struct ColScaleVec;
@@ -380,7 +410,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   Barriers* bars = reinterpret_cast<Barriers*>(smem + STAGES * C::STAGE_BYTES);
-  // [8 promotion warps][2][EPI_COLS] column scales (column mode)
+  // [8 promotion warps][2 ring slots][CB_F] scale staging (column mode)
   float* colbuf = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES + 1024);
   // [8 promotion warps][32 rows][32 bf16] output staging
   uint8_t* outbuf = smem + STAGES * C::STAGE_BYTES + 1024 + C::COLBUF_BYTES;
@@ -483,15 +513,15 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
     const int ew = warp - EPI_WARP0;
     const int wg = ew >> 2;                 // column half of the tile
     const int lq = warp & 3;                // TMEM lane quarter this warp may access
-    const int row_in_tile = lq * 32 + lane;
-    const uint32_t taddr_row = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(wg * EPI_COLS);
-    float* cbuf = colbuf + ew * 2 * EPI_COLS;
+    const uint32_t taddr_w = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(wg * EPI_COLS);
+    float* cbuf = colbuf + ew * 2 * C::CB_F;
     uint32_t acc_it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       int mt, nt;
       tile_coords(p, tile, mt, nt);
-      const int row = mt * BM + row_in_tile;
+      const int wrow0 = mt * BM + lq * 32;   // first tile row of this warp
+      const int row = wrow0 + lane;          // the row whose sA this lane fetches
       const int col0 = nt * BN + wg * EPI_COLS;
       const bool row_ok = row < p.R;
       const int nkb = p.nKB;
@@ -523,6 +553,9 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
         sb_r[0] = load_sb(0);
         sb_r[1] = load_sb(1);
       }
+      // uniform mode: acc[c][j] holds row `row`, columns 32c + 2j + {0,1};
+      // column mode: acc[cq][8h + 2j + rs] holds row wrow0 + lane/4 + 8rs + 16h,
+      // columns 32cq + 8j + 2(lane mod 4) + {0,1}
       uint64_t acc[CHUNKS][16];
 #pragma unroll
       for (int c = 0; c < CHUNKS; ++c)
@@ -534,49 +567,94 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
         constexpr int SL = decltype(slot)::value;
         const uint32_t b = acc_it % ACC_BUFS, bph = (acc_it / ACC_BUFS) & 1u;
         ++acc_it;
-        const float sa = sa_r[SL];
-        sa_r[SL] = load_sa(kb + 2);
         uint64_t s2u = 0;
+        uint64_t sb[COLS ? CHUNKS : 1][4];
+        float sa_raw[4];
         if (COLS) {
-          reinterpret_cast<CsVec*>(cbuf + SL * EPI_COLS)[lane] = cs_r[SL];
+          // stage the block's scales in the warp's slot SL (row of lane l at l;
+          // column scales at their fragment-order places), then read back the
+          // ones this lane's fragments need: rows lane/4 + 8i, and the column
+          // pairs of group lane mod 4
+          float* cb = cbuf + SL * C::CB_F;
+          cb[lane] = sa_r[SL];
+          if constexpr (EPI_COLS == 128) {
+            // columns 4l..4l+3: groups 2(l mod 2) and 2(l mod 2) + 1 at 2j = l - (l mod 2)
+            float* d = cb + 32 + (lane & 1) * 2 * C::GS + (lane & ~1);
+            *reinterpret_cast<float2*>(d) = make_float2(cs_r[SL].x, cs_r[SL].y);
+            *reinterpret_cast<float2*>(d + C::GS) = make_float2(cs_r[SL].z, cs_r[SL].w);
+          } else {
+            // columns 2l, 2l+1: group l mod 4 at 2j = 2(l/4)
+            *reinterpret_cast<float2*>(cb + 32 + (lane & 3) * C::GS + 2 * (lane >> 2)) =
+                *reinterpret_cast<const float2*>(&cs_r[SL]);
+          }
+          sa_r[SL] = load_sa(kb + 2);
           cs_r[SL] = load_cs(kb + 2);
           __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sa_raw[i] = cb[(lane >> 2) + 8 * i];
+          const ulonglong2* cs = reinterpret_cast<const ulonglong2*>(cb + 32 + (lane & 3) * C::GS);
+#pragma unroll
+          for (int cq = 0; cq < (COLS ? CHUNKS : 1); ++cq) {
+            const ulonglong2 v0 = cs[2 * cq], v1 = cs[2 * cq + 1];
+            sb[cq][0] = v0.x;
+            sb[cq][1] = v0.y;
+            sb[cq][2] = v1.x;
+            sb[cq][3] = v1.y;
+          }
         } else {
-          const float sc = sa * sb_r[SL];
+          const float sc = sa_r[SL] * sb_r[SL];
           s2u = pack2(sc, sc);
+          sa_r[SL] = load_sa(kb + 2);
           sb_r[SL] = load_sb(kb + 2);
         }
         bool good = mbar_wait(&bars->tfull[b], bph, abort_flag, true);
         if (!good) record_abort(abort_flag, p.err);
         if (__any_sync(0xffffffffu, !good)) return false;
         tc_fence_after();
-        const uint32_t tbase = taddr_row + b * BN;
-        const uint64_t* cs = reinterpret_cast<const uint64_t*>(cbuf + SL * EPI_COLS);
-        const uint64_t sa2 = pack2(sa, sa);
+        const uint32_t tbase = taddr_w + b * BN;
+        if (COLS) {
+          // fragments i = 2·cq + h: columns 32cq.., lanes 16h..; the load of
+          // fragment i+1 is in flight while fragment i is promoted
+          constexpr int NF = 2 * CHUNKS;
+          uint32_t r[2][16];
+          tmem_ld16x256_x4(tbase, r[0]);
+          uint64_t sal[2], sah[2];
+          sal[0] = pack2(sa_raw[0], sa_raw[0]);
+          sah[0] = pack2(sa_raw[1], sa_raw[1]);
+          sal[1] = pack2(sa_raw[2], sa_raw[2]);
+          sah[1] = pack2(sa_raw[3], sa_raw[3]);
+          tmem_wait_ld16(r[0]);
 #pragma unroll
-        for (int c = 0; c < CHUNKS; ++c) {
-          // TMEM loads are short (tens of cycles); loading each chunk right
-          // before its FMAs keeps only 32 partial registers live
-          uint32_t cur[32];
-          tmem_ld32_async(tbase + c * 32, cur);
-          tmem_wait_ld(cur);
-          if (c + 1 == CHUNKS) {
-            // the last chunk is in registers: hand the TMEM accumulator back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->tempty[b]);
-          }
-          if (COLS) {
-            uint64_t s2[16];
-            const ulonglong2* cs2 = reinterpret_cast<const ulonglong2*>(cs + c * 16);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const ulonglong2 v = cs2[j];
-              s2[2 * j] = mul_pair(sa2, v.x);
-              s2[2 * j + 1] = mul_pair(sa2, v.y);
+          for (int i = 0; i < NF; ++i) {
+            const int cq = i >> 1, h = i & 1;
+            if (i + 1 < NF)
+              tmem_ld16x256_x4(tbase + ((uint32_t)(16 * ((i + 1) & 1)) << 16) + 32 * ((i + 1) >> 1),
+                               r[(i + 1) & 1]);
+            promote_cols_frag(&acc[cq][8 * h], r[i & 1], sb[cq], sal[h], sah[h]);
+            if (i + 1 < NF) {
+              tmem_wait_ld16(r[(i + 1) & 1]);
+              if (i + 2 == NF) {
+                // the last fragment is in registers: hand the TMEM accumulator back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->tempty[b]);
+              }
             }
-            fma32_pairs(acc[c], cur, s2);
-          } else {
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < CHUNKS; ++c) {
+            // TMEM loads are short (tens of cycles); loading each chunk right
+            // before its FMAs keeps only 32 partial registers live
+            uint32_t cur[32];
+            tmem_ld32_async(tbase + c * 32, cur);
+            tmem_wait_ld(cur);
+            if (c + 1 == CHUNKS) {
+              // the last chunk is in registers: hand the TMEM accumulator back
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->tempty[b]);
+            }
             fma32_uniform(acc[c], cur, s2u);
           }
         }
@@ -590,7 +668,47 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
         }
       }
       if (!ok) break;
-      if (p.out_fp32) {
+      if (COLS) {
+        const int g2 = 2 * (lane & 3);
+        if (p.out_fp32) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int rs = 0; rs < 2; ++rs) {
+              const int r = wrow0 + (lane >> 2) + 8 * rs + 16 * h;
+              if (r < p.R) {
+                float* o = static_cast<float*>(p.out) + (size_t)r * p.C + col0 + g2;
+#pragma unroll
+                for (int cq = 0; cq < CHUNKS; ++cq)
+#pragma unroll
+                  for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<float2*>(o + 32 * cq + 8 * j) = unpack2(acc[cq][8 * h + 2 * j + rs]);
+              }
+            }
+        } else {
+          uint8_t* ob = outbuf + ew * OUT_CHUNK_BYTES;
+#pragma unroll
+          for (int cq = 0; cq < CHUNKS; ++cq) {
+            if (lane == 0) tma_store_wait_read();   // the previous chunk has left the buffer
+            __syncwarp();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int rs = 0; rs < 2; ++rs)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  // row lane/4 + 8rs + 16h, granule j, bytes 4·(lane mod 4);
+                  // (row/2) mod 4 = (lane/8) mod 4
+                  const float2 v = unpack2(acc[cq][8 * h + 2 * j + rs]);
+                  *reinterpret_cast<uint32_t*>(ob + ((lane >> 2) + 8 * rs + 16 * h) * 64 +
+                                               16 * (j ^ ((lane >> 3) & 3)) + 2 * g2) = f2_to_bf2(v.x, v.y);
+                }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && wrow0 < p.R) tma_store_2d(&tmOut, smem_u32(ob), col0 + cq * 32, wrow0);
+          }
+        }
+      } else if (p.out_fp32) {
         if (row_ok) {
           float* o = static_cast<float*>(p.out) + (size_t)row * p.C + col0;
 #pragma unroll
@@ -602,8 +720,9 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
             }
         }
       } else {
-        // bf16: each 32-row × 32-column chunk goes row-major into this warp's
-        // staging buffer and leaves with one TMA store (rows >= R are clipped)
+        // bf16: each 32-row × 32-column chunk goes row-major (swizzled) into
+        // this warp's staging buffer and leaves with one TMA store (rows >= R
+        // are clipped)
         uint8_t* ob = outbuf + ew * OUT_CHUNK_BYTES;
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c) {
@@ -614,13 +733,12 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
           for (int j = 0; j < 16; j += 4) {
             const float2 a0 = unpack2(acc[c][j]), a1 = unpack2(acc[c][j + 1]);
             const float2 a2 = unpack2(acc[c][j + 2]), a3 = unpack2(acc[c][j + 3]);
-            dst[j / 4] = make_uint4(f2_to_bf2(a0.x, a0.y), f2_to_bf2(a1.x, a1.y),
-                                    f2_to_bf2(a2.x, a2.y), f2_to_bf2(a3.x, a3.y));
+            dst[(j / 4) ^ ((lane >> 1) & 3)] = make_uint4(f2_to_bf2(a0.x, a0.y), f2_to_bf2(a1.x, a1.y),
+                                                          f2_to_bf2(a2.x, a2.y), f2_to_bf2(a3.x, a3.y));
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && mt * BM + lq * 32 < p.R)
-            tma_store_2d(&tmOut, smem_u32(ob), col0 + c * 32, mt * BM + lq * 32);
+          if (lane == 0 && wrow0 < p.R) tma_store_2d(&tmOut, smem_u32(ob), col0 + c * 32, wrow0);
         }
       }
     }
@@ -658,7 +776,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 output [rows, cols] stored in boxes of 32 rows × 32 columns.
+// 2-D bf16 output [rows, cols] stored in boxes of 32 rows × 32 columns from a
+// shared-memory buffer in the 64-byte swizzle.
 bool make_out_map(CUtensorMap* m, void* ptr, uint64_t cols, uint64_t rows) {
   auto enc = get_encode_fn();
   if (!enc) return false;
@@ -667,7 +786,7 @@ bool make_out_map(CUtensorMap* m, void* ptr, uint64_t cols, uint64_t rows) {
   cuuint32_t box[2] = {32, 32};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
