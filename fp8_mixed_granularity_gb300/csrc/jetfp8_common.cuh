@@ -51,18 +51,49 @@ constexpr float kBracketDn = 1.0f - 0x1p-20f;
 
 struct GroupScale {
   float s;      // S = fp32(amax/448), or 1 when amax == 0
-  float ra;     // fp32(1/S)·(1 + 2^-20), rounded
-  float rb;     // fp32(1/S)·(1 - 2^-20), rounded
+  float ra;     // ≈ (1/S)·(1 + 2^-20), within 2^-21 relative
+  float rb;     // ≈ (1/S)·(1 - 2^-20), within 2^-21 relative
   bool exact;   // 1/S is 1e37 or more (or not finite): always divide
 };
 
-__device__ __forceinline__ GroupScale make_scale(float amax) {
-  GroupScale g;
-  g.s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, kE4M3Max);
-  const float rs = __frcp_rn(g.s);
+// Bracketing factors from S.  rcp.approx is within a few ulp of 1/S; the
+// bracket argument in quant_pair only needs ra, rb within 2^-21 relative of
+// (1/S)(1 ± 2^-20).  Reciprocals of 1e37 or more (S subnormal or zero) and
+// non-finite ones send every value of the group to the division.
+__device__ __forceinline__ void set_brackets(GroupScale& g) {
+  float rs;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(rs) : "f"(g.s));
   g.exact = !(rs < 1.0e37f);
   g.ra = __fmul_rn(rs, kBracketUp);
   g.rb = __fmul_rn(rs, kBracketDn);
+}
+
+// S = fp32(amax/448) by IEEE division (any finite amax).
+__device__ __forceinline__ GroupScale make_scale(float amax) {
+  GroupScale g;
+  g.s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, kE4M3Max);
+  set_brackets(g);
+  return g;
+}
+
+// S = fp32(amax/448) for an amax that is a bf16 value (the max of |x| over bf16
+// data): q0 = amax·c with c = fp32(1/448), the residual amax - 448·q0 (exact),
+// and one FMA correction give the correctly rounded quotient for every bf16
+// significand (checked exhaustively against exact rational arithmetic) while
+// the result is a normal number; tiny amax takes the division.
+__device__ __forceinline__ GroupScale make_scale_bf16(float amax) {
+  constexpr float kInv448 = 1.0f / 448.0f;   // fp32(1/448)
+  GroupScale g;
+  if (amax == 0.0f) {
+    g.s = 1.0f;
+  } else if (amax < 0x1p-100f) {
+    g.s = __fdiv_rn(amax, kE4M3Max);
+  } else {
+    const float q0 = __fmul_rn(amax, kInv448);
+    const float r = __fmaf_rn(-q0, kE4M3Max, amax);
+    g.s = __fmaf_rn(r, kInv448, q0);
+  }
+  set_brackets(g);
   return g;
 }
 
@@ -74,14 +105,15 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float v0, float v1) {
 }
 
 // E4M3(fp32(v/S)) for two values that share the scale S, without a division
-// in the common case.  With ra, rb = 1/S·(1 ± 2^-20) (each within 2^-23
-// relative of that), a = v·ra and b = v·rb bracket the correctly rounded
-// quotient RN(v/S) strictly: they sit at least 2^-20 - 4·2^-24 relative away
-// from v/S on either side, while RN(v/S) is within 2^-24.  E4M3 rounding
-// (nearest-even, saturating) is monotone, so if a and b round to the same code,
-// RN(v/S) rounds to it too.  Otherwise — a quotient within about 2^-20 of an
-// E4M3 rounding boundary, or a scale whose reciprocal overflows — the IEEE
-// division decides.  Zeros keep their sign on both paths.
+// in the common case.  With ra, rb within 2^-21 relative of 1/S·(1 ± 2^-20),
+// a = v·ra and b = v·rb (each rounded once more, 2^-24) sit at least
+// 2^-20 - 2^-21 - 2^-23 > 2^-24 relative away from v/S on either side, while
+// the correctly rounded quotient RN(v/S) is within 2^-24 of it: a and b
+// bracket RN(v/S) strictly.  E4M3 rounding (nearest-even, saturating) is
+// monotone, so if a and b round to the same code, RN(v/S) rounds to it too.
+// Otherwise — a quotient within about 2^-20 of an E4M3 rounding boundary, or a
+// scale whose reciprocal overflows — the IEEE division decides.  Zeros keep
+// their sign on both paths.
 __device__ __forceinline__ uint32_t quant_pair(float2 v, const GroupScale& g) {
   const float2 a = mul2(v, make_float2(g.ra, g.ra));
   const float2 b = mul2(v, make_float2(g.rb, g.rb));
@@ -89,6 +121,31 @@ __device__ __forceinline__ uint32_t quant_pair(float2 v, const GroupScale& g) {
   const uint32_t cb = cvt_e4m3x2(b.x, b.y);
   if (ca != cb || g.exact) ca = cvt_e4m3x2(__fdiv_rn(v.x, g.s), __fdiv_rn(v.y, g.s));
   return ca;
+}
+
+// N pairs sharing one scale -> 2N codes packed little-endian into N/2 words
+// (pair 2w in the low half of word w).  All brackets are formed first and one
+// branch takes the rare division path for the whole set.
+template <int N>
+__device__ __forceinline__ void quant_pairs(const float2 (&v)[N], const GroupScale& g, uint32_t (&out)[N / 2]) {
+  static_assert(N % 2 == 0, "pairs come in twos");
+  uint32_t cb[N / 2];
+  bool diff = g.exact;
+#pragma unroll
+  for (int w = 0; w < N / 2; ++w) {
+    const float2 a0 = mul2(v[2 * w], make_float2(g.ra, g.ra));
+    const float2 a1 = mul2(v[2 * w + 1], make_float2(g.ra, g.ra));
+    const float2 b0 = mul2(v[2 * w], make_float2(g.rb, g.rb));
+    const float2 b1 = mul2(v[2 * w + 1], make_float2(g.rb, g.rb));
+    out[w] = cvt_e4m3x2(a0.x, a0.y) | (cvt_e4m3x2(a1.x, a1.y) << 16);
+    cb[w] = cvt_e4m3x2(b0.x, b0.y) | (cvt_e4m3x2(b1.x, b1.y) << 16);
+    diff |= out[w] != cb[w];
+  }
+  if (diff) {
+#pragma unroll
+    for (int w = 0; w < N / 2; ++w)
+      out[w] = quant_pair(v[2 * w], g) | (quant_pair(v[2 * w + 1], g) << 16);
+  }
 }
 
 // Four values sharing one scale -> four codes, first value in the low byte.

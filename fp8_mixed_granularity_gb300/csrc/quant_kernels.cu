@@ -64,20 +64,20 @@ __device__ __forceinline__ float group16_max(float v) {
   return group8_max(v);
 }
 
-// One lane's 16 values (8 packed pairs) of a 1×128 group held by 8 lanes:
-// group amax, scale, and the 16 codes (4 words, first value in the low byte).
+// One lane's 16 values (8 packed pairs) of a 1×128 group held by 8 lanes,
+// all bf16 values: group amax, scale, and the 16 codes (4 words, first value
+// in the low byte).
 __device__ __forceinline__ uint4 quant16(const float2 (&f)[8], bool valid, float& S) {
   float amax = 0.0f;
   if (valid) {
 #pragma unroll
     for (int w = 0; w < 8; ++w) amax = fmaxf(amax, fmaxf(fabsf(f[w].x), fabsf(f[w].y)));
   }
-  const GroupScale g = make_scale(group8_max(amax));
+  const GroupScale g = make_scale_bf16(group8_max(amax));
   S = g.s;
-  uint32_t c[8];
-#pragma unroll
-  for (int w = 0; w < 8; ++w) c[w] = quant_pair(f[w], g);
-  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
+  uint32_t c[4];
+  quant_pairs<8>(f, g, c);
+  return make_uint4(c[0], c[1], c[2], c[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -153,13 +153,15 @@ __device__ __forceinline__ void ttile_store(const uint8_t* T, uint8_t* __restric
 // Column scales of a 128×128 tile: each thread passes its 8 columns' maxima
 // over its 8 rows; 128 threads reduce a column each, build its GroupScale and
 // store S to sT_out[0..127]; afterwards every thread can read the scale of any
-// column from shared memory.
+// column from shared memory.  BF16_AMAX: the maxima are of bf16 values, so the
+// scale takes the division-free exact path.
 struct ColScales {
   float red[16][128];
   float s[128], ra[128], rb[128];
   int exact[128];
 };
 
+template <bool BF16_AMAX>
 __device__ __forceinline__ void col_scales(const float (&cm)[8], ColScales& cs, float* sT_out) {
   const uint32_t rowgrp = threadIdx.x >> 4, c0 = 8u * (threadIdx.x & 15u);
 #pragma unroll
@@ -169,7 +171,7 @@ __device__ __forceinline__ void col_scales(const float (&cm)[8], ColScales& cs, 
     float m = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) m = fmaxf(m, cs.red[i][threadIdx.x]);
-    const GroupScale g = make_scale(m);
+    const GroupScale g = BF16_AMAX ? make_scale_bf16(m) : make_scale(m);
     cs.s[threadIdx.x] = g.s;
     cs.ra[threadIdx.x] = g.ra;
     cs.rb[threadIdx.x] = g.rb;
@@ -237,7 +239,7 @@ k_quant_weight(const uint16_t* __restrict__ w, uint32_t N, uint32_t K, uint8_t* 
     amax = sm.wmax[0];
 #pragma unroll
     for (int i = 1; i < kThreads / 32; ++i) amax = fmaxf(amax, sm.wmax[i]);
-    const GroupScale g = make_scale(amax);
+    const GroupScale g = make_scale_bf16(amax);
     if (threadIdx.x == 0) s[(size_t)nb * kblocks + kb] = g.s;
     uint32_t lo[8], hi[8];
 #pragma unroll
@@ -292,7 +294,7 @@ k_requant_row2col(const uint8_t* __restrict__ q, const float* __restrict__ s, ui
         cm[j + 1] = fmaxf(cm[j + 1], fabsf(v[i][j + 1]));
       }
     }
-    col_scales(cm, sm.cs, sT + (size_t)mb * K + (size_t)kb * 128);
+    col_scales<false>(cm, sm.cs, sT + (size_t)mb * K + (size_t)kb * 128);
     auto get = [&](int i, int j) { return v[i][j]; };
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -340,11 +342,11 @@ k_quant_grad_dual(const uint16_t* __restrict__ dy, uint32_t M, uint32_t N, uint3
         cm[2 * p + 1] = fmaxf(cm[2 * p + 1], fabsf(f[p].y));
         amax = fmaxf(amax, fmaxf(fabsf(f[p].x), fabsf(f[p].y)));
       }
-      const GroupScale g = make_scale(group16_max(amax));
+      const GroupScale g = make_scale_bf16(group16_max(amax));
       srow[i] = g.s;
-      const uint2 codes = make_uint2(quant_pair(f[0], g) | (quant_pair(f[1], g) << 16),
-                                     quant_pair(f[2], g) | (quant_pair(f[3], g) << 16));
-      *reinterpret_cast<uint2*>(q_row + (row0 + i) * N + col0) = codes;
+      uint32_t codes[2];
+      quant_pairs<4>(f, g, codes);
+      *reinterpret_cast<uint2*>(q_row + (row0 + i) * N + col0) = make_uint2(codes[0], codes[1]);
     }
     if (c0 == 0) {
       *reinterpret_cast<float4*>(s_row + (size_t)nb * ld_srow + row0) =
@@ -352,7 +354,7 @@ k_quant_grad_dual(const uint16_t* __restrict__ dy, uint32_t M, uint32_t N, uint3
       *reinterpret_cast<float4*>(s_row + (size_t)nb * ld_srow + row0 + 4) =
           make_float4(srow[4], srow[5], srow[6], srow[7]);
     }
-    col_scales(cm, sm.cs, sT_col + (size_t)mb * N + (size_t)nb * 128);
+    col_scales<true>(cm, sm.cs, sT_col + (size_t)mb * N + (size_t)nb * 128);
     auto get = [&](int i, int j) {
       const uint32_t wv = raw[i][j >> 1];
       return __uint_as_float((j & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
