@@ -44,6 +44,13 @@ __device__ __forceinline__ void st32(void* p, const uint32_t (&r)[8]) {
                "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
 }
+// 16-byte read that stays in L1 for a second pass over the same tile.
+__device__ __forceinline__ uint4 ldg_cached16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ uint4 ldg_stream16(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -263,7 +270,7 @@ k_quant_weight(const uint16_t* __restrict__ w, uint32_t N, uint32_t K, uint8_t* 
 // ---------------------------------------------------------------------------
 // Q3: dequantise 1×128 row groups, requantise 128×1 column groups, transpose.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 k_requant_row2col(const uint8_t* __restrict__ q, const float* __restrict__ s, uint32_t M,
                   uint32_t K, uint8_t* __restrict__ qT, float* __restrict__ sT) {
   __shared__ __align__(16) TileSmem sm;
@@ -310,8 +317,11 @@ k_requant_row2col(const uint8_t* __restrict__ q, const float* __restrict__ s, ui
 // ---------------------------------------------------------------------------
 // Q4: one read of the bf16 gradient: 1×128 row groups along N (stored as is)
 // and 128×1 column groups along M (stored transposed).  M multiple of 128.
+// The first pass reads the tile through L1 and the column pass reads the
+// thread's 8×8 sub-block again (an L1 hit) instead of holding it in registers
+// across the column-scale barriers, which leaves room for three CTAs per SM.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 k_quant_grad_dual(const uint16_t* __restrict__ dy, uint32_t M, uint32_t N, uint32_t ld_srow,
                   uint8_t* __restrict__ q_row, float* __restrict__ s_row,
                   uint8_t* __restrict__ qT_col, float* __restrict__ sT_col) {
@@ -324,7 +334,7 @@ k_quant_grad_dual(const uint16_t* __restrict__ dy, uint32_t M, uint32_t N, uint3
     uint32_t raw[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint4 t = ldg_stream16(dy + (row0 + i) * N + col0);
+      const uint4 t = ldg_cached16(dy + (row0 + i) * N + col0);
       raw[i][0] = t.x; raw[i][1] = t.y; raw[i][2] = t.z; raw[i][3] = t.w;
     }
     float cm[8];
@@ -355,6 +365,11 @@ k_quant_grad_dual(const uint16_t* __restrict__ dy, uint32_t M, uint32_t N, uint3
           make_float4(srow[4], srow[5], srow[6], srow[7]);
     }
     col_scales<true>(cm, sm.cs, sT_col + (size_t)mb * N + (size_t)nb * 128);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 t = ldg_cached16(dy + (row0 + i) * N + col0);
+      raw[i][0] = t.x; raw[i][1] = t.y; raw[i][2] = t.z; raw[i][3] = t.w;
+    }
     auto get = [&](int i, int j) {
       const uint32_t wv = raw[i][j >> 1];
       return __uint_as_float((j & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
@@ -551,7 +566,7 @@ cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, uint8_t* q,
 cudaError_t launch_requant_row2col(const uint8_t* q, const float* s, int64_t M, int64_t K,
                                    uint8_t* qT, float* sT, cudaStream_t st) {
   const size_t blocks = (size_t)(M / 128) * (K / 128);
-  const unsigned grid = grid_for(blocks, 1, 4);
+  const unsigned grid = grid_for(blocks, 1, 6);
   k_requant_row2col<<<grid, kThreads, 0, st>>>(q, s, (uint32_t)M, (uint32_t)K, qT, sT);
   return cudaGetLastError();
 }
@@ -560,7 +575,7 @@ cudaError_t launch_quant_grad_dual(const void* dy, int64_t M, int64_t N, uint8_t
                                    float* s_row, uint8_t* qT_col, float* sT_col, cudaStream_t st) {
   if (qT_col == nullptr) return launch_quant_rowgroups(dy, M, N, q_row, s_row, st);
   const size_t blocks = (size_t)(M / 128) * (N / 128);
-  const unsigned grid = grid_for(blocks, 1, 4);
+  const unsigned grid = grid_for(blocks, 1, 6);
   k_quant_grad_dual<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(dy), (uint32_t)M,
                                                (uint32_t)N, (uint32_t)round_up4(M), q_row, s_row,
                                                qT_col, sT_col);
