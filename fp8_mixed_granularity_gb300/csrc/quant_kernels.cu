@@ -217,7 +217,7 @@ struct TileSmem {
 // ---------------------------------------------------------------------------
 // Q2: 128×128 weight blocks, optional transposed payload (same codes).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 k_quant_weight(const uint16_t* __restrict__ w, uint32_t N, uint32_t K, uint8_t* __restrict__ q,
                float* __restrict__ s, uint8_t* __restrict__ qT) {
   __shared__ __align__(16) TileSmem sm;
@@ -226,9 +226,11 @@ k_quant_weight(const uint16_t* __restrict__ w, uint32_t N, uint32_t K, uint8_t* 
   for (uint32_t blk = blockIdx.x; blk < kblocks * nblocks; blk += gridDim.x) {
     const uint32_t nb = blk / kblocks, kb = blk % kblocks;
     const size_t row0 = (size_t)nb * 128 + r0, col0 = (size_t)kb * 128 + c0;
+    // read through L1; the codes pass reads the sub-block again (an L1 hit)
+    // rather than holding it across the block-amax barrier
     uint4 raw[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) raw[i] = ldg_stream16(w + (row0 + i) * K + col0);
+    for (int i = 0; i < 8; ++i) raw[i] = ldg_cached16(w + (row0 + i) * K + col0);
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -248,6 +250,8 @@ k_quant_weight(const uint16_t* __restrict__ w, uint32_t N, uint32_t K, uint8_t* 
     for (int i = 1; i < kThreads / 32; ++i) amax = fmaxf(amax, sm.wmax[i]);
     const GroupScale g = make_scale_bf16(amax);
     if (threadIdx.x == 0) s[(size_t)nb * kblocks + kb] = g.s;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) raw[i] = ldg_cached16(w + (row0 + i) * K + col0);
     uint32_t lo[8], hi[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -285,7 +289,14 @@ k_requant_row2col(const uint8_t* __restrict__ q, const float* __restrict__ s, ui
     const float4 s_lo = *reinterpret_cast<const float4*>(s + (size_t)kb * M + row0);
     const float4 s_hi = *reinterpret_cast<const float4*>(s + (size_t)kb * M + row0 + 4);
     const float srow[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
-    float v[8][8];
+    // x̃ = fp32(dec(q)·S) for a column pair (j, j+1) of the 8 rows; computed
+    // once for the column maxima and again for the codes, so that only the
+    // 64 code bytes stay in registers across the column-scale barriers
+    auto dequant = [&](int i, int j) {
+      const uint32_t word = (j < 4 ? c[i].x : c[i].y) >> (8 * (j & 3));
+      const float2 d = dec_e4m3x2(word & 0xFFFFu);
+      return make_float2(__fmul_rn(d.x, srow[i]), __fmul_rn(d.y, srow[i]));
+    };
     float cm[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) cm[j] = 0.0f;
@@ -293,20 +304,26 @@ k_requant_row2col(const uint8_t* __restrict__ q, const float* __restrict__ s, ui
     for (int i = 0; i < 8; ++i) {
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
-        const uint32_t word = (j < 4 ? c[i].x : c[i].y) >> (8 * (j & 3));
-        const float2 d = dec_e4m3x2(word & 0xFFFFu);
-        v[i][j] = __fmul_rn(d.x, srow[i]);
-        v[i][j + 1] = __fmul_rn(d.y, srow[i]);
-        cm[j] = fmaxf(cm[j], fabsf(v[i][j]));
-        cm[j + 1] = fmaxf(cm[j + 1], fabsf(v[i][j + 1]));
+        const float2 v = dequant(i, j);
+        cm[j] = fmaxf(cm[j], fabsf(v.x));
+        cm[j + 1] = fmaxf(cm[j + 1], fabsf(v.y));
       }
     }
     col_scales<false>(cm, sm.cs, sT + (size_t)mb * K + (size_t)kb * 128);
-    auto get = [&](int i, int j) { return v[i][j]; };
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint2 codes = quant_col8(get, j, load_col_scale(sm.cs, c0 + j));
-      ttile_put8(sm.T, c0 + j, r0 >> 3, codes.x, codes.y);
+    for (int j = 0; j < 8; j += 2) {
+      float v0[8], v1[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 v = dequant(i, j);
+        v0[i] = v.x;
+        v1[i] = v.y;
+      }
+      const uint2 codes0 = quant_col8([&](int i, int) { return v0[i]; }, j, load_col_scale(sm.cs, c0 + j));
+      ttile_put8(sm.T, c0 + j, r0 >> 3, codes0.x, codes0.y);
+      const uint2 codes1 =
+          quant_col8([&](int i, int) { return v1[i]; }, j + 1, load_col_scale(sm.cs, c0 + j + 1));
+      ttile_put8(sm.T, c0 + j + 1, r0 >> 3, codes1.x, codes1.y);
     }
     __syncthreads();
     ttile_store(sm.T, qT, M, (size_t)kb * 128, (size_t)mb * 128);
@@ -319,9 +336,9 @@ k_requant_row2col(const uint8_t* __restrict__ q, const float* __restrict__ s, ui
 // and 128×1 column groups along M (stored transposed).  M multiple of 128.
 // The first pass reads the tile through L1 and the column pass reads the
 // thread's 8×8 sub-block again (an L1 hit) instead of holding it in registers
-// across the column-scale barriers, which leaves room for three CTAs per SM.
+// across the column-scale barriers, which leaves room for four CTAs per SM.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
 k_quant_grad_dual(const uint16_t* __restrict__ dy, uint32_t M, uint32_t N, uint32_t ld_srow,
                   uint8_t* __restrict__ q_row, float* __restrict__ s_row,
                   uint8_t* __restrict__ qT_col, float* __restrict__ sT_col) {
@@ -557,7 +574,7 @@ cudaError_t launch_quant_rowgroups(const void* x, int64_t M, int64_t K, uint8_t*
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,
                                 uint8_t* qT, cudaStream_t st) {
   const size_t blocks = (size_t)(N / 128) * (K / 128);
-  const unsigned grid = grid_for(blocks, 1, 4);
+  const unsigned grid = grid_for(blocks, 1, 8);
   k_quant_weight<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(w), (uint32_t)N,
                                             (uint32_t)K, q, s, qT);
   return cudaGetLastError();
@@ -575,7 +592,7 @@ cudaError_t launch_quant_grad_dual(const void* dy, int64_t M, int64_t N, uint8_t
                                    float* s_row, uint8_t* qT_col, float* sT_col, cudaStream_t st) {
   if (qT_col == nullptr) return launch_quant_rowgroups(dy, M, N, q_row, s_row, st);
   const size_t blocks = (size_t)(M / 128) * (N / 128);
-  const unsigned grid = grid_for(blocks, 1, 6);
+  const unsigned grid = grid_for(blocks, 1, 8);
   k_quant_grad_dual<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(dy), (uint32_t)M,
                                                (uint32_t)N, (uint32_t)round_up4(M), q_row, s_row,
                                                qT_col, sT_col);
