@@ -29,7 +29,8 @@
 //               Scales are prefetched two blocks ahead into registers.
 //     uniform scales (FProp, DGrad: sB is one value per 128 output columns):
 //               each thread owns one row and 32-column chunks of it;
-//               promotion is one FMA per element with the product sA·sB.
+//               promotion is one FMA per element with the product sA·sB,
+//               with the next chunk's TMEM load in flight.
 //     column scales (WGrad: sB is one value per output column): the partial
 //               is read as 16-lane × 256-bit fragments, so a thread holds 4
 //               rows × 2 adjacent columns of every 8 and needs only a quarter
@@ -277,8 +278,10 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
 }
 
 // acc[j] += (p[2j], p[2j+1]) · s2 for 16 packed FP32 pairs (one scale pair).
+// Volatile so that it stays between the TMEM load of the next chunk and the
+// wait for it.
 __device__ __forceinline__ void fma32_uniform(uint64_t (&acc)[16], const uint32_t (&p)[32], uint64_t s2) {
-  asm("{\n\t.reg .b64 q;\n\t"
+  asm volatile("{\n\t.reg .b64 q;\n\t"
       "mov.b64 q, {%16, %17};\n\t"
       "fma.rn.f32x2 %0, q, %48, %0;\n\t"
       "mov.b64 q, {%18, %19};\n\t"
@@ -642,20 +645,25 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
             }
           }
         } else {
+          // 32-column chunks; the load of chunk c+1 is in flight while chunk c
+          // is promoted (TMEM loads take well over a hundred cycles while the
+          // tensor core and TMA keep the SM busy)
+          uint32_t cur[2][32];
+          tmem_ld32_async(tbase, cur[0]);
+          tmem_wait_ld(cur[0]);
 #pragma unroll
           for (int c = 0; c < CHUNKS; ++c) {
-            // TMEM loads are short (tens of cycles); loading each chunk right
-            // before its FMAs keeps only 32 partial registers live
-            uint32_t cur[32];
-            tmem_ld32_async(tbase + c * 32, cur);
-            tmem_wait_ld(cur);
-            if (c + 1 == CHUNKS) {
-              // the last chunk is in registers: hand the TMEM accumulator back
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars->tempty[b]);
+            if (c + 1 < CHUNKS) tmem_ld32_async(tbase + (c + 1) * 32, cur[(c + 1) & 1]);
+            fma32_uniform(acc[c], cur[c & 1], s2u);
+            if (c + 1 < CHUNKS) {
+              tmem_wait_ld(cur[(c + 1) & 1]);
+              if (c + 2 == CHUNKS) {
+                // the last chunk is in registers: hand the TMEM accumulator back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->tempty[b]);
+              }
             }
-            fma32_uniform(acc[c], cur, s2u);
           }
         }
         return true;
