@@ -44,7 +44,7 @@ REF_ROWS, REF_COLS = 128, 1024       # CPU sample: 128 tokens × 1024 output fea
 # DRAM bytes (read + write) of one gate/up FProp launch (8192 x 28672 x 4096), from the
 # ncu capture in profiles/gemm_e4m3_blockscaled_fprop_8192x28672x4096_dram.md; must be
 # re-measured (or set to None) whenever the GEMM kernel changes.
-GATEUP_FPROP_DRAM_BYTES = 617486336
+GATEUP_FPROP_DRAM_BYTES = 608445952
 
 # algorithmic bytes per element of each quantiser (inputs read + outputs written)
 QUANT_BYTES = {
@@ -53,6 +53,10 @@ QUANT_BYTES = {
     "quant_weight": 2 + 1 + 1 + 4 / 16384,
     "quant_grad_dual": 2 + 2 * (1 + 4 / 128),
     "requant": 1 + 4 / 128 + 1 + 4 / 128,
+    # per element of h [M, I]: gate and up read (2 + 2 B), codes and scales written
+    "swiglu_quant": 2 + 2 + 1 + 4 / 128,
+    # per element of ∇h [M, I]: gate, up and ∇h read, ∇gate and ∇up written
+    "swiglu_bwd": 5 * 2,
 }
 
 
@@ -445,7 +449,7 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
 # single-kernel cases (profiling aid): one kernel, one shape, W + K launches
 # ---------------------------------------------------------------------------
 CASES = {"fprop", "dgrad", "wgrad", "quant_act", "rmsnorm_quant", "quant_weight",
-         "quant_grad_dual", "requant"}
+         "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd"}
 
 
 def run_case(args):
@@ -458,6 +462,19 @@ def run_case(args):
     from fp8_mixed_granularity_gb300 import workloads as W
     from fp8_mixed_granularity_gb300.linear import LinearBuffers
     M, N, K = (int(v) for v in args.shape.split(","))
+    if args.case in ("swiglu_quant", "swiglu_bwd"):
+        # SwiGLU of an [M, 2I] gate/up output, I = N / 2 (N = the gate/up width)
+        I = N // 2
+        gu = W.device_normal((M, 2 * I), 1.0, dev, seed=5)
+        dh = W.device_normal((M, I), 1e-3, dev, seed=6)
+        hq, hs = J.empty_rowgroup_quant(M, I, dev)
+        dgu = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dev)
+        if args.case == "swiglu_quant":
+            fn = lambda: J.jetfp8_swiglu_quant(gu, hq, hs)
+        else:
+            fn = lambda: J.jetfp8_swiglu_bwd(gu, dh, dgu)
+        _time_case(args, fn, M * I * QUANT_BYTES[args.case], "GB/s", [M, N, K])
+        return
     lin = W.Linear("case", M, K, N)
     b = LinearBuffers(lin, dev, rmsnorm=args.case == "rmsnorm_quant")
     x = W.device_activations(M, K, dev, seed=1)
@@ -465,7 +482,8 @@ def run_case(args):
     dy = W.device_normal((M, N), 1e-3, dev, seed=3)
     gamma = W.device_uniform((K,), 0.5, 1.5, dev, seed=4)
     b.forward(x, w, gamma)
-    b.backward(dy)
+    if args.case not in ("fprop", "quant_act", "rmsnorm_quant", "quant_weight") or M % 128 == 0:
+        b.backward(dy)   # the backward quantisers need M to be a multiple of 128
     t = b.t
     calls = {
         "fprop": (lambda: J.jetfp8_gemm_fprop(t["xq"], t["sx"], t["wq"], t["sw"], t["y"]), 2 * M * N * K, "TFLOP/s"),
@@ -482,6 +500,12 @@ def run_case(args):
                     M * K * QUANT_BYTES["requant"], "GB/s"),
     }
     fn, work, unit = calls[args.case]
+    _time_case(args, fn, work, unit, [M, N, K])
+
+
+def _time_case(args, fn, work, unit, shape):
+    import torch
+    from fp8_mixed_granularity_gb300 import jetfp8 as J
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
@@ -495,7 +519,7 @@ def run_case(args):
     ms = sorted(s.elapsed_time(e) for s, e in evs)
     med = ms[len(ms) // 2]
     scale = 1e12 if unit == "TFLOP/s" else 1e9
-    print(json.dumps({"case": args.case, "shape": [M, N, K], "median_ms": med, "min_ms": ms[0],
+    print(json.dumps({"case": args.case, "shape": shape, "median_ms": med, "min_ms": ms[0],
                       "value": work / (med * 1e-3) / scale, "unit": unit}), flush=True)
 
 
