@@ -71,6 +71,9 @@ def parse_args():
     p.add_argument("--case", choices=sorted(CASES), default=None,
                    help="time one kernel alone (for profiling) instead of the layer step")
     p.add_argument("--shape", default="8192,28672,4096", help="M,N,K for --case")
+    p.add_argument("--graph", action="store_true",
+                   help="with --case: capture the timed launches in a CUDA graph and time its replay "
+                        "(kernel time without the per-call host work, as a serving loop runs decode)")
     return p.parse_args()
 
 
@@ -509,18 +512,41 @@ def _time_case(args, fn, work, unit, shape):
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
-    evs = []
-    for _ in range(args.steps):
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(); fn(); e.record()
-        evs.append((s, e))
-    torch.cuda.synchronize()
-    J.jetfp8_get_last_device_error()
-    ms = sorted(s.elapsed_time(e) for s, e in evs)
-    med = ms[len(ms) // 2]
+    if args.graph:
+        # one graph of `steps` launches, replayed `steps` times; per-launch time
+        stream = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()   # warm the capture stream
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(args.steps):
+                    fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(5):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(); graph.replay(); e.record()
+            torch.cuda.synchronize()
+            ms.append(s.elapsed_time(e) / args.steps)
+        J.jetfp8_get_last_device_error()
+        ms.sort()
+        med = ms[len(ms) // 2]
+    else:
+        evs = []
+        for _ in range(args.steps):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(); fn(); e.record()
+            evs.append((s, e))
+        torch.cuda.synchronize()
+        J.jetfp8_get_last_device_error()
+        ms = sorted(s.elapsed_time(e) for s, e in evs)
+        med = ms[len(ms) // 2]
     scale = 1e12 if unit == "TFLOP/s" else 1e9
     print(json.dumps({"case": args.case, "shape": shape, "median_ms": med, "min_ms": ms[0],
-                      "value": work / (med * 1e-3) / scale, "unit": unit}), flush=True)
+                      "value": work / (med * 1e-3) / scale, "unit": unit, "graph": bool(args.graph)}),
+          flush=True)
 
 
 def main():

@@ -77,11 +77,13 @@ constexpr int OUT_CHUNK_BYTES = 32 * 32 * 2;
 template <int BN_>
 struct Cfg {
   static constexpr int BN = BN_;
-  static constexpr int STAGES = BN_ == 256 ? 4 : 6;
+  // deeper rings for narrower tiles (same shared-memory budget)
+  static constexpr int STAGES = BN_ == 256 ? 4 : (BN_ == 128 ? 6 : 8);
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int ACC_BUFS = TMEM_COLS / BN;
+  static constexpr int ACC_BUFS = TMEM_COLS / BN < MAX_BUFS ? TMEM_COLS / BN : MAX_BUFS;
+  static constexpr int TMEM_ALLOC = ACC_BUFS * BN;   // a power of two >= 32
   static constexpr int EPI_COLS = BN / 2;        // columns per promotion warp
   static constexpr int CHUNKS = EPI_COLS / 32;   // 32-column TMEM loads per block
   // UMMA instruction descriptor: D = F32 (bits 4-5 = 1), A = B = E4M3 (format 0),
@@ -391,6 +393,10 @@ __device__ __forceinline__ void promote_cols_frag(uint64_t* acc, const uint32_t 
 template <int EPI_COLS>
 struct ColScaleVec;
 template <>
+struct ColScaleVec<32> {
+  using T = float;   // not used: column mode runs with 128- or 256-wide tiles
+};
+template <>
 struct ColScaleVec<64> {
   using T = float2;
 };
@@ -408,6 +414,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
   constexpr int BN = C::BN, STAGES = C::STAGES, ACC_BUFS = C::ACC_BUFS;
   constexpr int EPI_COLS = C::EPI_COLS, CHUNKS = C::CHUNKS;
   using CsVec = typename ColScaleVec<EPI_COLS>::T;
+  static_assert(!COLS || BN >= 128, "column-scale promotion needs 128- or 256-wide tiles");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -439,7 +446,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&bars->tmem_base)),
-                 "r"(TMEM_COLS));
+                 "r"(C::TMEM_ALLOC));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -651,6 +658,12 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
           uint32_t cur[2][32];
           tmem_ld32_async(tbase, cur[0]);
           tmem_wait_ld(cur[0]);
+          if (CHUNKS == 1) {
+            // the only chunk is in registers: hand the TMEM accumulator back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[b]);
+          }
 #pragma unroll
           for (int c = 0; c < CHUNKS; ++c) {
             if (c + 1 < CHUNKS) tmem_ld32_async(tbase + (c + 1) * 32, cur[(c + 1) & 1]);
@@ -761,7 +774,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
     __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(TMEM_COLS));
+                 "r"(C::TMEM_ALLOC));
   }
 }
 
@@ -877,10 +890,17 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  // 128×256 tiles (two TMEM accumulators) where the output width allows, else 128×128
+  // 128×256 tiles (two TMEM accumulators) where the output width allows, else
+  // 128×128.  Uniform-scale GEMMs with fewer 128×256 tiles than SMs (decode-sized
+  // M) take the widest of 128 or 64 columns that gives every SM a tile, so more
+  // SMs stream the weights; the arithmetic of every output element (its MMA
+  // blocks and promotion order) does not depend on the tile width.
   const bool cols = a.b_mode == BScale::kColumn;
-  if (a.C % 256 == 0) return cols ? launch_cfg<256, true>(a, dev, st) : launch_cfg<256, false>(a, dev, st);
-  return cols ? launch_cfg<128, true>(a, dev, st) : launch_cfg<128, false>(a, dev, st);
+  if (cols) return a.C % 256 == 0 ? launch_cfg<256, true>(a, dev, st) : launch_cfg<128, true>(a, dev, st);
+  const int64_t tiles_m = (a.R + BM - 1) / BM, sms = num_sms();
+  if (a.C % 256 == 0 && tiles_m * (a.C / 256) >= sms) return launch_cfg<256, false>(a, dev, st);
+  if (a.C % 256 != 0 || tiles_m * (a.C / 128) >= sms) return launch_cfg<128, false>(a, dev, st);
+  return launch_cfg<64, false>(a, dev, st);
 }
 
 }  // namespace jetfp8

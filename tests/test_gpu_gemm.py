@@ -67,6 +67,30 @@ def test_fprop_decode_rows_bit_identical_to_training_batch(dev):
         assert torch.equal(y_s, y_all[lo:hi])
 
 
+def test_fprop_decode_tiles_bit_identical_to_training_tiles(dev):
+    """Decode-sized batches run on narrower output tiles (more SMs streaming the
+    weights) than a training batch; every output element must still be the same
+    bits, so a token's result does not depend on the batch it was computed in."""
+    M, N, K = 8192, 1024, 2048          # 64 × 4 tiles of 128 × 256: the wide tiles
+    x = W.normal((M, K), 1.0, seed=2, stream=21)
+    w = W.weights(N, K, seed=2, stream=22)
+    wq, sw, _ = q_weight(w, dev, with_t=False)
+    xq, sx = q_act(x, dev)
+    y_all = _fprop(dev, xq, sx, wq, sw)
+    # 1, 64, 128 and 192 rows run on 64-wide tiles, 2560 rows (20 × 8 tiles) on 128-wide
+    for lo, hi in [(0, 64), (4096, 4224), (8000, 8192), (17, 18), (2048, 4608)]:
+        xq_s, sx_s = q_act(x[lo:hi], dev)
+        y_s = _fprop(dev, xq_s, sx_s, wq, sw)
+        assert torch.equal(y_s, y_all[lo:hi]), (lo, hi)
+    # decode-shaped parity against the oracle on the narrow tiles (N = 4096 -> 64-wide)
+    x = W.activations(64, 512, seed=3, stream=23)
+    w = W.weights(4096, 512, seed=3, stream=24)
+    xq, sx = q_act(x, dev)
+    wq, sw, _ = q_weight(w, dev, with_t=False)
+    y = _fprop(dev, xq, sx, wq, sw, torch.float32)
+    _assert_close(h(y), O.gemm_fprop(h(xq), h(sx)[:, :64], h(wq), h(sw)), "decode fprop")
+
+
 @pytest.mark.parametrize("M,N,K", [(256, 384, 512), (1, 256, 128), (200, 384, 640), (1024, 2048, 1024)])
 def test_dgrad_parity(dev, M, N, K):
     dy = W.gradients(M, N, seed=2)
