@@ -62,6 +62,47 @@ def test_quant_act_edge_values(dev):
     _assert_rowquant(q, s, W.bf16_values(x))
 
 
+def _near_tie_groups(n_groups, rel, seed):
+    """Groups of bf16 values whose quotient v/S lies within `rel` (relative) of an
+    E4M3 rounding midpoint, S = fp32(amax/448) of the group's own maximum.  For
+    each candidate maximum (a bf16 value) every smaller positive bf16 value is
+    tried; the near ones go into that maximum's group with random signs."""
+    rng = np.random.default_rng(seed)
+    allv = (np.arange(0x3000, 0x4800, dtype=np.uint32) << 16).view(np.float32)   # ≈ [4.7e-10, 131072)
+    d = O.e4m3_decode(np.arange(0x7F)).astype(np.float64)
+    mids = (d[:-1] + d[1:]) / 2
+    groups = []
+    for amax in rng.permutation(allv[(allv > 1e-3) & (allv < 1e3)]):
+        S = np.float32(np.float32(amax) / np.float32(448.0))
+        cand = allv[allv < amax]
+        qv = cand.astype(np.float64) / np.float64(S)
+        k = np.clip(np.searchsorted(mids, qv), 1, len(mids) - 1)
+        dist = np.minimum(np.abs(qv - mids[k - 1]), np.abs(qv - mids[k])) / qv
+        near = cand[dist < rel]
+        if len(near) == 0:
+            continue
+        row = np.zeros(128, np.float32)
+        row[0] = amax
+        pick = near[:127] * rng.choice(np.float32([-1.0, 1.0]), size=min(len(near), 127))
+        row[1:1 + len(pick)] = pick
+        groups.append(row)
+        if len(groups) == n_groups:
+            break
+    return np.stack(groups)
+
+
+def test_quant_act_near_rounding_boundaries(dev):
+    """Quotients v/S within 2^-19 of an E4M3 rounding boundary, over many
+    different scales: the bracketing products (from an approximate reciprocal
+    of S) must give exactly the codes of RN(v/S) or defer to the division."""
+    rows = _near_tie_groups(96, 2.0 ** -19, seed=7)
+    assert len(rows) >= 64
+    x = W.to_bf16(rows)
+    assert np.array_equal(W.bf16_values(x), rows)     # the values are bf16 already
+    q, s = q_act(x, dev)
+    _assert_rowquant(q, s, rows)
+
+
 @pytest.mark.parametrize("N,K", [(384, 512), (128, 128), (1024, 2048)])
 def test_quant_weight_parity(dev, N, K):
     w = W.weights(N, K, seed=1)
