@@ -84,6 +84,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank contributes its own time and all
+    receive the maximum (a no-op for one rank).  `device` is where the
+    collective runs (the rank's GPU under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: float, world: int, ms: float, scale: float = 1e12) -> float:
+    """Whole-job throughput: the units all replicas processed in the slowest
+    rank's time (weak scaling: every rank runs the same workload)."""
+    return units_per_rank * world / (ms * 1e-3) / scale
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -305,11 +323,7 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     J.jetfp8_get_last_device_error()
-    ms = t0.elapsed_time(t1) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
 
     # per-GEMM-kind times from the events inside the timed region
     gemm_ms = {}
@@ -334,7 +348,7 @@ def run_ours(args):
     peaks = measured_peaks()
     fp8_peak_sustained = 2.0 * peaks["bf16_sustained"]   # dense fp8 = 2 × bf16 (nominal ratio)
     gemm_tflops = gemm_flops / (gemm_total_ms * 1e-3) / 1e12
-    value = gemm_flops * world / (ms * 1e-3) / 1e12
+    value = job_value(gemm_flops, world, ms)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -469,12 +483,8 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
         cur.wait_stream(s_)
     t1.record(cur)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
-    if world > 1:
-        tt = torch.tensor([ms], device=bufs[0].device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-    return {"value": gemm_flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    ms = max_over_ranks(t0.elapsed_time(t1) / steps, world, bufs[0].device)
+    return {"value": job_value(gemm_flops, world, ms), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
             "overlap": "copies in, compute and copies out on three streams, pipelined per linear"}
 
