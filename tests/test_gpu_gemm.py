@@ -127,15 +127,20 @@ def test_gemm_rejects_bad_shapes(dev):
 
 
 # --------------------------------------------------------------------------
-# Full-size, sampled: the Llama-3.1-8B training shapes at M = 8192
+# Full-size, sampled: the Llama-3.1-8B training shapes at M = 8192 and two
+# 32B-class shapes at M = 16384
 # --------------------------------------------------------------------------
 def _stripes(n, rng, k=2, width=128):
     starts = rng.choice(n // width, size=k, replace=False) * width
     return np.concatenate([np.arange(s, s + width) for s in starts])
 
 
-@pytest.mark.parametrize("lin", [l for l in W.llama8b_training() if l.name in ("gate_up", "down")],
-                         ids=lambda l: l.name)
+@pytest.mark.parametrize(
+    "lin",
+    [l for l in W.llama8b_training() if l.name in ("gate_up", "down")]
+    # 32B-class layer at M = 16384: QKV (N = 7168) and down (K = 25600, 200 blocks per output)
+    + [l for l in W.dense32b_training() if l.name in ("qkv", "down")],
+    ids=lambda l: f"{l.name}_{l.M}x{l.N}x{l.K}")
 def test_full_size_linear_sampled(dev, lin):
     M, K, N = lin.M, lin.K, lin.N
     rng = np.random.default_rng(5)
