@@ -493,7 +493,7 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
 # single-kernel cases (profiling aid): one kernel, one shape, W + K launches
 # ---------------------------------------------------------------------------
 CASES = {"fprop", "dgrad", "wgrad", "quant_act", "rmsnorm_quant", "quant_weight",
-         "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd"}
+         "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd", "fprop_quant", "fprop_then_quant"}
 
 
 def run_case(args):
@@ -526,11 +526,23 @@ def run_case(args):
     dy = W.device_normal((M, N), 1e-3, dev, seed=3)
     gamma = W.device_uniform((K,), 0.5, 1.5, dev, seed=4)
     b.forward(x, w, gamma)
-    if args.case not in ("fprop", "quant_act", "rmsnorm_quant", "quant_weight") or M % 128 == 0:
+    if args.case not in ("fprop", "fprop_quant", "fprop_then_quant", "quant_act", "rmsnorm_quant",
+                         "quant_weight") or M % 128 == 0:
         b.backward(dy)   # the backward quantisers need M to be a multiple of 128
     t = b.t
+    yq, ys = J.empty_rowgroup_quant(M, N, dev)
+
+    def fprop_then_quant():
+        J.jetfp8_gemm_fprop(t["xq"], t["sx"], t["wq"], t["sw"], t["y"])
+        J.jetfp8_quant_act_1x128(t["y"], yq, ys)
+
     calls = {
         "fprop": (lambda: J.jetfp8_gemm_fprop(t["xq"], t["sx"], t["wq"], t["sw"], t["y"]), 2 * M * N * K, "TFLOP/s"),
+        # FProp whose epilogue also emits the 1×128-quantised output, against
+        # FProp followed by the separate quantiser on its bf16 output
+        "fprop_quant": (lambda: J.jetfp8_gemm_fprop_quant(t["xq"], t["sx"], t["wq"], t["sw"], yq, ys, t["y"]),
+                        2 * M * N * K, "TFLOP/s"),
+        "fprop_then_quant": (fprop_then_quant, 2 * M * N * K, "TFLOP/s"),
         "dgrad": (lambda: J.jetfp8_gemm_dgrad(t["dyq"], t["sdy"], t["wqT"], t["sw"], t["dx"]), 2 * M * N * K, "TFLOP/s"),
         "wgrad": (lambda: J.jetfp8_gemm_wgrad(t["dyqT"], t["sdyT"], t["xqT"], t["sxT"], t["dw"]), 2 * M * N * K, "TFLOP/s"),
         "quant_act": (lambda: J.jetfp8_quant_act_1x128(x, t["xq"], t["sx"]), M * K * QUANT_BYTES["quant_act"], "GB/s"),

@@ -102,6 +102,8 @@ struct Cfg {
   static_assert(STAGES <= MAX_STAGES && ACC_BUFS <= MAX_BUFS, "barrier arrays");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(GS % 4 == 0 && CB_F % 4 == 0, "16-byte aligned staging fields");
+  // the fused output quantiser stages 1 KB of codes per promotion warp there
+  static_assert(BN_ != 256 || COLBUF_BYTES >= EPI_WARPS * 1024, "code staging");
   static_assert(COLBUF_BYTES % 128 == 0 && OUT_CHUNK_BYTES % 128 == 0,
                 "output staging buffers (TMA store sources) 128-byte aligned");
 };
@@ -121,10 +123,15 @@ struct DevArgs {
   long long ld_sA;
   const float* sB;
   long long sb_j, sb_k;
-  void* out;
+  void* out;       // may be null when out_q is set
   int R, C, nKB, tiles_m, tiles_n;
   int m_fastest;   // tile order: 1 = consecutive tiles walk down M (share a B tile)
   int out_fp32;
+  // fused 1×128 quantisation of the bf16 output (uniform mode, 256-wide tiles):
+  // codes [R, C] (stored through tmQ), scales [C/128][ld_out_s]
+  uint8_t* out_q;
+  float* out_s;
+  long long ld_out_s;
   unsigned* err;
 };
 
@@ -409,7 +416,8 @@ template <int BN_, bool COLS>
 __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmOut, const DevArgs p) {
+                        const __grid_constant__ CUtensorMap tmOut,
+                        const __grid_constant__ CUtensorMap tmQ, const DevArgs p) {
   using C = Cfg<BN_>;
   constexpr int BN = C::BN, STAGES = C::STAGES, ACC_BUFS = C::ACC_BUFS;
   constexpr int EPI_COLS = C::EPI_COLS, CHUNKS = C::CHUNKS;
@@ -743,23 +751,59 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
       } else {
         // bf16: each 32-row × 32-column chunk goes row-major (swizzled) into
         // this warp's staging buffer and leaves with one TMA store (rows >= R
-        // are clipped)
+        // are clipped).  With the fused quantiser (256-wide tiles: the thread's
+        // 128 columns are exactly one 1×128 group of its row) the group's
+        // scale comes from the bf16-rounded values and each chunk's 32 codes
+        // per row leave through a 1 KB staging buffer in the (here unused)
+        // column-scale staging area, so the codes are those of the 1×128
+        // quantiser applied to the bf16 output.
         uint8_t* ob = outbuf + ew * OUT_CHUNK_BYTES;
+        uint8_t* qb = reinterpret_cast<uint8_t*>(colbuf) + ew * 1024;
+        const bool fuse_q = EPI_COLS == 128 && p.out_q != nullptr;
+        GroupScale gq{};
+        if (fuse_q) {
+          float amax = 0.0f;
+#pragma unroll
+          for (int c = 0; c < CHUNKS; ++c)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 v = unpack2(acc[c][j]);
+              const float2 f = bf2_to_f2(f2_to_bf2(v.x, v.y));
+              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+          gq = make_scale_bf16(amax);
+          if (row_ok) p.out_s[(long long)(col0 / 128) * p.ld_out_s + row] = gq.s;
+        }
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c) {
-          if (lane == 0) tma_store_wait_read();   // the previous chunk has left the buffer
+          if (lane == 0) tma_store_wait_read();   // the previous chunk's stores have left the buffers
           __syncwarp();
           uint4* dst = reinterpret_cast<uint4*>(ob + lane * 64);
+          uint32_t yb[16];
 #pragma unroll
-          for (int j = 0; j < 16; j += 4) {
-            const float2 a0 = unpack2(acc[c][j]), a1 = unpack2(acc[c][j + 1]);
-            const float2 a2 = unpack2(acc[c][j + 2]), a3 = unpack2(acc[c][j + 3]);
-            dst[(j / 4) ^ ((lane >> 1) & 3)] = make_uint4(f2_to_bf2(a0.x, a0.y), f2_to_bf2(a1.x, a1.y),
-                                                          f2_to_bf2(a2.x, a2.y), f2_to_bf2(a3.x, a3.y));
+          for (int j = 0; j < 16; ++j) {
+            const float2 v = unpack2(acc[c][j]);
+            yb[j] = f2_to_bf2(v.x, v.y);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            dst[(j / 4) ^ ((lane >> 1) & 3)] = make_uint4(yb[j], yb[j + 1], yb[j + 2], yb[j + 3]);
+          if (fuse_q) {
+            float2 f[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f[j] = bf2_to_f2(yb[j]);
+            uint32_t codes[8];
+            quant_pairs<16>(f, gq, codes);
+            uint4* qd = reinterpret_cast<uint4*>(qb + lane * 32);
+            qd[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            qd[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && wrow0 < p.R) tma_store_2d(&tmOut, smem_u32(ob), col0 + c * 32, wrow0);
+          if (lane == 0 && wrow0 < p.R) {
+            if (p.out != nullptr) tma_store_2d(&tmOut, smem_u32(ob), col0 + c * 32, wrow0);
+            if (fuse_q) tma_store_2d(&tmQ, smem_u32(qb), col0 + c * 32, wrow0);
+          }
         }
       }
     }
@@ -812,6 +856,20 @@ bool make_out_map(CUtensorMap* m, void* ptr, uint64_t cols, uint64_t rows) {
   return r == CUDA_SUCCESS;
 }
 
+// 2-D E4M3 codes [rows, cols] stored in boxes of 32 rows × 32 bytes, no swizzle.
+bool encode_codes_map(CUtensorMap* m, void* ptr, uint64_t cols, uint64_t rows) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D E4M3 tensor [outer, inner] (row-major, inner contiguous) loaded in
 // boxes of box_outer rows × 128 bytes with the 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
@@ -851,13 +909,18 @@ cudaError_t launch_cfg(const GemmArgs& a, int dev, cudaStream_t st) {
     }
   }
   if (ready[dev] != 1) return cudaErrorInvalidConfiguration;
-  CUtensorMap ta, tb, to;
+  CUtensorMap ta, tb, to, tq;
   if (!make_map(&ta, a.A, (uint64_t)a.Kc, (uint64_t)a.R, BM) ||
       !make_map(&tb, a.B, (uint64_t)a.Kc, (uint64_t)a.C, BN))
     return cudaErrorInvalidValue;
-  if (a.out_fp32) {
-    to = ta;   // unused by the fp32 epilogue
+  if (a.out_fp32 || a.out == nullptr) {
+    to = ta;   // unused: fp32 epilogue, or no bf16 output
   } else if (!make_out_map(&to, a.out, (uint64_t)a.C, (uint64_t)a.R)) {
+    return cudaErrorInvalidValue;
+  }
+  if (a.out_q == nullptr) {
+    tq = ta;   // unused
+  } else if (!encode_codes_map(&tq, a.out_q, (uint64_t)a.C, (uint64_t)a.R)) {
     return cudaErrorInvalidValue;
   }
   DevArgs d;
@@ -874,11 +937,14 @@ cudaError_t launch_cfg(const GemmArgs& a, int dev, cudaStream_t st) {
   d.tiles_n = (int)(a.C / BN);
   d.m_fastest = a.R <= a.C ? 1 : 0;
   d.out_fp32 = a.out_fp32 ? 1 : 0;
+  d.out_q = a.out_q;
+  d.out_s = a.out_s;
+  d.ld_out_s = a.ld_out_s;
   d.err = device_error_word();
   if (d.err == nullptr) return cudaErrorInvalidValue;
   const int tiles = d.tiles_m * d.tiles_n;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, THREADS, C::SMEM_BYTES, st>>>(ta, tb, to, d);
+  kern<<<grid, THREADS, C::SMEM_BYTES, st>>>(ta, tb, to, tq, d);
   return cudaGetLastError();
 }
 
@@ -897,6 +963,9 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   // blocks and promotion order) does not depend on the tile width.
   const bool cols = a.b_mode == BScale::kColumn;
   if (cols) return a.C % 256 == 0 ? launch_cfg<256, true>(a, dev, st) : launch_cfg<128, true>(a, dev, st);
+  // the fused quantiser needs a thread's 128 columns to be a whole 1×128 group
+  if (a.out_q != nullptr)
+    return a.C % 256 == 0 ? launch_cfg<256, false>(a, dev, st) : cudaErrorInvalidValue;
   const int64_t tiles_m = (a.R + BM - 1) / BM, sms = num_sms();
   if (a.C % 256 == 0 && tiles_m * (a.C / 256) >= sms) return launch_cfg<256, false>(a, dev, st);
   if (a.C % 256 != 0 || tiles_m * (a.C / 128) >= sms) return launch_cfg<128, false>(a, dev, st);

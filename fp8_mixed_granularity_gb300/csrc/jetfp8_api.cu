@@ -224,6 +224,40 @@ jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const ui
   return gemm_common(g, out_dtype, stream);
 }
 
+jetfp8_status jetfp8_gemm_fprop_quant(const uint8_t* xq, const float* sx, const uint8_t* wq,
+                                      const float* sw, int64_t M, int64_t N, int64_t K,
+                                      void* y_bf16, uint8_t* yq, float* ys, cudaStream_t stream) {
+  Check c;
+  c.ptr(xq).ptr(sx).ptr(wq).ptr(sw).bf(y_bf16, false).ptr(yq).ptr(ys).positive(M).mult128(N)
+      .mult128(K).fits(M, K).fits(N, K).fits(M, N);
+  // the fused quantiser needs whole 1×128 groups per 256-wide output tile
+  if (c.st == JETFP8_OK && N % 256 != 0) c.st = JETFP8_ERR_UNSUPPORTED_SHAPE;
+  c.device();
+  if (c.st != JETFP8_OK) return c.st;
+  GemmArgs g{xq, wq, sx, round_up4(M), sw, K / 128, 1, BScale::kBlock, y_bf16, false, M, N, K};
+  g.out_q = yq;
+  g.out_s = ys;
+  g.ld_out_s = round_up4(M);
+  return from_cuda(launch_gemm(g, stream));
+}
+
+jetfp8_status jetfp8_gemm_dgrad_quant(const uint8_t* dyq, const float* sdy, const uint8_t* wqT,
+                                      const float* sw, int64_t M, int64_t N, int64_t K,
+                                      void* dx_bf16, uint8_t* dxq, float* dxs, cudaStream_t stream) {
+  Check c;
+  c.ptr(dyq).ptr(sdy).ptr(wqT).ptr(sw).bf(dx_bf16, false).ptr(dxq).ptr(dxs).positive(M).mult128(N)
+      .mult128(K).fits(M, N).fits(N, K).fits(M, K);
+  // the fused quantiser needs whole 1×128 groups per 256-wide output tile
+  if (c.st == JETFP8_OK && K % 256 != 0) c.st = JETFP8_ERR_UNSUPPORTED_SHAPE;
+  c.device();
+  if (c.st != JETFP8_OK) return c.st;
+  GemmArgs g{dyq, wqT, sdy, round_up4(M), sw, 1, K / 128, BScale::kBlock, dx_bf16, false, M, K, N};
+  g.out_q = dxq;
+  g.out_s = dxs;
+  g.ld_out_s = round_up4(M);
+  return from_cuda(launch_gemm(g, stream));
+}
+
 jetfp8_status jetfp8_swiglu_quant(const void* gu_bf16, int64_t M, int64_t I, uint8_t* q, float* s,
                                   void* h_bf16, cudaStream_t stream) {
   Check c;

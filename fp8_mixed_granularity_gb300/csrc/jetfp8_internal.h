@@ -43,6 +43,11 @@ struct GemmArgs {
   void* out;
   bool out_fp32;
   int64_t R, C, Kc;  // rows of A / out, rows of B = columns of out, contraction length
+  // optional: 1×128 quantisation of the bf16 output fused into the epilogue
+  // (uniform scales only, C a multiple of 256); codes [R, C], scales [C/128][ld_out_s]
+  uint8_t* out_q = nullptr;
+  float* out_s = nullptr;
+  int64_t ld_out_s = 0;
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);

@@ -39,6 +39,8 @@ SIGNATURES = {
     "jetfp8_gemm_fprop": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_dgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_wgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
+    "jetfp8_gemm_fprop_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
+    "jetfp8_gemm_dgrad_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_swiglu_quant": [_P, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_swiglu_bwd": [_P, _P, _I64, _I64, _P, _P],
     "jetfp8_get_last_device_error": [_P],
@@ -178,6 +180,28 @@ def jetfp8_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw, stream=None):
         _ptr(dyqT, _U8, None, "dyqT"), _ptr(sdyT, _F, scale_shape(N, M), "sdyT"),
         _ptr(xqT, _U8, (K, M), "xqT"), _ptr(sxT, _F, scale_shape(K, M), "sxT"), M, N, K,
         _ptr(dw, None, (N, K), "dw"), _out_dt(dw), _stream(stream)), "jetfp8_gemm_wgrad")
+
+
+def jetfp8_gemm_fprop_quant(xq, sx, wq, sw, yq, ys, y=None, stream=None):
+    """FProp with the 1×128 quantiser of its bf16 output fused in (y optional)."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _check(load_library().jetfp8_gemm_fprop_quant(
+        _ptr(xq, _U8, None, "xq"), _ptr(sx, _F, scale_shape(M, K), "sx"), _ptr(wq, _U8, (N, K), "wq"),
+        _ptr(sw, _F, (N // 128, K // 128), "sw"), M, N, K, _ptr(y, _BF, (M, N), "y"),
+        _ptr(yq, _U8, (M, N), "yq"), _ptr(ys, _F, scale_shape(M, N), "ys"), _stream(stream)),
+        "jetfp8_gemm_fprop_quant")
+
+
+def jetfp8_gemm_dgrad_quant(dyq, sdy, wqT, sw, dxq, dxs, dx=None, stream=None):
+    """DGrad with the 1×128 quantiser of its bf16 output fused in (dx optional)."""
+    M, N = dyq.shape
+    K = wqT.shape[0]
+    _check(load_library().jetfp8_gemm_dgrad_quant(
+        _ptr(dyq, _U8, None, "dyq"), _ptr(sdy, _F, scale_shape(M, N), "sdy"), _ptr(wqT, _U8, (K, N), "wqT"),
+        _ptr(sw, _F, (N // 128, K // 128), "sw"), M, N, K, _ptr(dx, _BF, (M, K), "dx"),
+        _ptr(dxq, _U8, (M, K), "dxq"), _ptr(dxs, _F, scale_shape(M, K), "dxs"), _stream(stream)),
+        "jetfp8_gemm_dgrad_quant")
 
 
 def jetfp8_swiglu_quant(gu, q, s, h=None, stream=None):

@@ -160,6 +160,24 @@ jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const ui
                                 const float* sxT, int64_t M, int64_t N, int64_t K, void* dw,
                                 jetfp8_out_dtype out_dtype, cudaStream_t stream);
 
+/* F1 and F2 with the 1×128 quantiser fused into the epilogue ([digest] 方法步骤详情,
+ * step 5: the quantisation is fused into the neighbouring kernels to cut its
+ * overhead).  The output tile is rounded to bf16 as by jetfp8_gemm_fprop /
+ * jetfp8_gemm_dgrad and quantised in 1×128 groups along its columns exactly as
+ * by jetfp8_quant_act_1x128 applied to that bf16 output (the same codes and
+ * scales, bit for bit), so the next linear's input comes straight from the GEMM:
+ *   y_bf16 bf16 [M, N] or NULL (codes only)
+ *   yq     E4M3 [M, N],  ys fp32 [N/128][roundup(M,4)]
+ * Arguments otherwise as jetfp8_gemm_fprop (F1) and jetfp8_gemm_dgrad (F2,
+ * output [M, K]).  The output width (N for F1, K for F2) must be a multiple of
+ * 256: JETFP8_ERR_UNSUPPORTED_SHAPE otherwise.  M arbitrary. */
+jetfp8_status jetfp8_gemm_fprop_quant(const uint8_t* xq, const float* sx, const uint8_t* wq,
+                                      const float* sw, int64_t M, int64_t N, int64_t K,
+                                      void* y_bf16, uint8_t* yq, float* ys, cudaStream_t stream);
+jetfp8_status jetfp8_gemm_dgrad_quant(const uint8_t* dyq, const float* sdy, const uint8_t* wqT,
+                                      const float* sw, int64_t M, int64_t N, int64_t K,
+                                      void* dx_bf16, uint8_t* dxq, float* dxs, cudaStream_t stream);
+
 /* X1 — SwiGLU fused with the 1×128 quantiser, for the decoder MLP between the
  * gate/up and down projections (not described by the pages):
  *   h = bf16(silu(g)·u), silu(g) = g/(1+exp(-g)), in FP32; then Q1 on h.

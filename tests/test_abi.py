@@ -65,6 +65,9 @@ def test_validation_rejects_before_touching_the_device(lib):
     # misaligned pointer
     assert lib.jetfp8_quant_act_1x128(P(48), 4, 128, P(64), P(64), None) == 3   # bf16 needs 32 B
     assert lib.jetfp8_quant_act_1x128(P(64), 4, 128, P(72), P(64), None) == 3   # E4M3 needs 16 B
+    # fused output quantiser: the output width must be a multiple of 256
+    assert lib.jetfp8_gemm_fprop_quant(P(64), P(64), P(64), P(64), 4, 384, 128, None, P(64), P(64), None) == 2
+    assert lib.jetfp8_gemm_dgrad_quant(P(64), P(64), P(64), P(64), 4, 256, 384, None, P(64), P(64), None) == 2
     # WGrad needs M multiple of 128
     assert lib.jetfp8_gemm_wgrad(P(64), P(64), P(64), P(64), 100, 128, 128, P(64), 0, None) == 2
     # non-positive M

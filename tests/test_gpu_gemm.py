@@ -91,6 +91,50 @@ def test_fprop_decode_tiles_bit_identical_to_training_tiles(dev):
     _assert_close(h(y), O.gemm_fprop(h(xq), h(sx)[:, :64], h(wq), h(sw)), "decode fprop")
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 512, 384), (200, 768, 256), (1, 256, 128), (1024, 2048, 1024)])
+def test_fprop_quant_fused_equals_separate(dev, M, N, K):
+    """The epilogue-fused 1×128 quantiser gives the bf16 output of the plain
+    FProp and, bit for bit, the codes and scales of the 1×128 quantiser applied
+    to that output (on the GPU and in the oracle)."""
+    x = W.activations(M, K, seed=0, stream=41)
+    w = W.weights(N, K, seed=0, stream=42)
+    xq, sx = q_act(x, dev)
+    wq, sw, _ = q_weight(w, dev, with_t=False)
+    y = _fprop(dev, xq, sx, wq, sw)
+    yq, ys = J.empty_rowgroup_quant(M, N, dev)
+    ys.fill_(float("nan"))
+    y2 = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    J.jetfp8_gemm_fprop_quant(xq, sx, wq, sw, yq, ys, y2)
+    check_errors()
+    assert torch.equal(y2, y)
+    rq, rs = q_act(y, dev)
+    assert torch.equal(yq, rq) and torch.equal(ys[:, :M], rs[:, :M])
+    oq, os_ = O.quant_rowgroups(h(y.float()).astype(np.float32))
+    assert np.array_equal(h(yq), oq) and np.array_equal(h(ys)[:, :M], os_)
+    # codes only
+    yq3, ys3 = J.empty_rowgroup_quant(M, N, dev)
+    J.jetfp8_gemm_fprop_quant(xq, sx, wq, sw, yq3, ys3)
+    check_errors()
+    assert torch.equal(yq3, yq) and torch.equal(ys3[:, :M], ys[:, :M])
+
+
+def test_dgrad_quant_fused_equals_separate(dev):
+    M, N, K = 200, 384, 512
+    dy = W.gradients(M, N, seed=0, stream=43)
+    w = W.weights(N, K, seed=0, stream=44)
+    dyq, sdy, _, _ = q_grad(dy, dev, with_col=False)
+    _, sw, wqT = q_weight(w, dev)
+    dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    J.jetfp8_gemm_dgrad(dyq, sdy, wqT, sw, dx)
+    dxq, dxs = J.empty_rowgroup_quant(M, K, dev)
+    dx2 = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    J.jetfp8_gemm_dgrad_quant(dyq, sdy, wqT, sw, dxq, dxs, dx2)
+    check_errors()
+    assert torch.equal(dx2, dx)
+    rq, rs = q_act(dx, dev)
+    assert torch.equal(dxq, rq) and torch.equal(dxs[:, :M], rs[:, :M])
+
+
 @pytest.mark.parametrize("M,N,K", [(256, 384, 512), (1, 256, 128), (200, 384, 640), (1024, 2048, 1024)])
 def test_dgrad_parity(dev, M, N, K):
     dy = W.gradients(M, N, seed=2)
