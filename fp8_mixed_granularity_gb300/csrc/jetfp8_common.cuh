@@ -39,11 +39,6 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
   return bits_f2(d);
 }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
-  return bits_f2(d);
-}
 
 // Bracketing factors 1 ± 2^-20 (exact in FP32).
 constexpr float kBracketUp = 1.0f + 0x1p-20f;
@@ -148,11 +143,6 @@ __device__ __forceinline__ void quant_pairs(const float2 (&v)[N], const GroupSca
   }
 }
 
-// Four values sharing one scale -> four codes, first value in the low byte.
-__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, const GroupScale& g) {
-  return quant_pair(make_float2(a, b), g) | (quant_pair(make_float2(c, d), g) << 16);
-}
-
 // Two E4M3 codes (low byte first) -> two exact floats.
 __device__ __forceinline__ float2 dec_e4m3x2(uint32_t two_codes) {
   uint32_t h2;
@@ -169,10 +159,6 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
 __device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);   // a -> low half
   return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ float absmax4(float m, float a, float b, float c, float d) {
-  return fmaxf(fmaxf(fmaxf(m, fabsf(a)), fabsf(b)), fmaxf(fabsf(c), fabsf(d)));
 }
 
 // 4×4 byte transpose: rows a,b,c,d (byte i = column i) -> columns.

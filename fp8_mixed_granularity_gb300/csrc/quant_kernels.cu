@@ -51,12 +51,6 @@ __device__ __forceinline__ uint4 ldg_cached16(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
-__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
 
 // Max over the 8 lanes that share a group (lanes 8j .. 8j+7).
 __device__ __forceinline__ float group8_max(float v) {
