@@ -30,14 +30,14 @@
 //     uniform scales (FProp, DGrad: sB is one value per 128 output columns):
 //               each thread owns one row and 32-column chunks of it;
 //               promotion is one FMA per element with the product sA·sB,
-//               with the next chunk's TMEM load in flight.
+//               with the TMEM loads of the next two chunks in flight.
 //     column scales (WGrad: sB is one value per output column): the partial
 //               is read as 16-lane × 256-bit fragments, so a thread holds 4
 //               rows × 2 adjacent columns of every 8 and needs only a quarter
 //               of the column scales; each block the warp stages its row and
 //               column scales once through shared memory in that order.
 //               Promotion is (partial·sB)·sA, a multiply and an FMA per
-//               element, with the next fragment's TMEM load in flight.
+//               element, with the TMEM loads of the next two fragments in flight.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records an
 // error word, lets copies and MMAs in flight land, frees TMEM and returns.
 #include <cuda.h>
@@ -286,6 +286,15 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                : "memory");
 }
 
+// Orders later uses of r after the tcgen05.wait::ld just issued (which waits
+// for all of this thread's TMEM loads): ties further destination registers.
+__device__ __forceinline__ void tmem_tie32(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 // acc[j] += (p[2j], p[2j+1]) · s2 for 16 packed FP32 pairs (one scale pair).
 // Volatile so that it stays between the TMEM load of the next chunk and the
 // wait for it.
@@ -348,6 +357,13 @@ __device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[1
 }
 __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_tie16(uint32_t (&r)[16]) {
+  asm volatile(""
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
                  "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                :
@@ -630,60 +646,60 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
         if (__any_sync(0xffffffffu, !good)) return false;
         tc_fence_after();
         const uint32_t tbase = taddr_w + b * BN;
+        // TMEM loads take well over a hundred cycles while the tensor core and
+        // TMA keep the SM busy, and tcgen05.wait::ld waits for all of a
+        // thread's loads: pieces go through a three-buffer ring, loaded two
+        // ahead of their promotion, with a wait after every second piece; the
+        // accumulator is handed back right after the wait that covers the
+        // last piece.
+        auto release = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->tempty[b]);
+        };
         if (COLS) {
-          // fragments i = 2·cq + h: columns 32cq.., lanes 16h..; the load of
-          // fragment i+1 is in flight while fragment i is promoted
+          // fragments i = 2·cq + h: columns 32cq.., lanes 16h..
           constexpr int NF = 2 * CHUNKS;
-          uint32_t r[2][16];
-          tmem_ld16x256_x4(tbase, r[0]);
+          uint32_t r[3][16];
+          auto load = [&](int i) {
+            tmem_ld16x256_x4(tbase + ((uint32_t)(16 * (i & 1)) << 16) + 32 * (i >> 1), r[i % 3]);
+          };
+          load(0);
+          load(1);
           uint64_t sal[2], sah[2];
           sal[0] = pack2(sa_raw[0], sa_raw[0]);
           sah[0] = pack2(sa_raw[1], sa_raw[1]);
           sal[1] = pack2(sa_raw[2], sa_raw[2]);
           sah[1] = pack2(sa_raw[3], sa_raw[3]);
           tmem_wait_ld16(r[0]);
+          tmem_tie16(r[1]);
+          if (NF <= 2) release();
 #pragma unroll
           for (int i = 0; i < NF; ++i) {
-            const int cq = i >> 1, h = i & 1;
-            if (i + 1 < NF)
-              tmem_ld16x256_x4(tbase + ((uint32_t)(16 * ((i + 1) & 1)) << 16) + 32 * ((i + 1) >> 1),
-                               r[(i + 1) & 1]);
-            promote_cols_frag(&acc[cq][8 * h], r[i & 1], sb[cq], sal[h], sah[h]);
-            if (i + 1 < NF) {
-              tmem_wait_ld16(r[(i + 1) & 1]);
-              if (i + 2 == NF) {
-                // the last fragment is in registers: hand the TMEM accumulator back
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->tempty[b]);
-              }
+            if (i + 2 < NF) load(i + 2);
+            promote_cols_frag(&acc[i >> 1][8 * (i & 1)], r[i % 3], sb[i >> 1], sal[i & 1], sah[i & 1]);
+            if ((i & 1) && i + 1 < NF) {
+              tmem_wait_ld16(r[(i + 1) % 3]);
+              if (i + 2 < NF) tmem_tie16(r[(i + 2) % 3]);
+              if (i + 2 >= NF - 1) release();
             }
           }
         } else {
-          // 32-column chunks; the load of chunk c+1 is in flight while chunk c
-          // is promoted (TMEM loads take well over a hundred cycles while the
-          // tensor core and TMA keep the SM busy)
-          uint32_t cur[2][32];
+          // 32-column chunks
+          uint32_t cur[3][32];
           tmem_ld32_async(tbase, cur[0]);
+          if (CHUNKS > 1) tmem_ld32_async(tbase + 32, cur[1]);
           tmem_wait_ld(cur[0]);
-          if (CHUNKS == 1) {
-            // the only chunk is in registers: hand the TMEM accumulator back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->tempty[b]);
-          }
+          if (CHUNKS > 1) tmem_tie32(cur[1]);
+          if (CHUNKS <= 2) release();
 #pragma unroll
           for (int c = 0; c < CHUNKS; ++c) {
-            if (c + 1 < CHUNKS) tmem_ld32_async(tbase + (c + 1) * 32, cur[(c + 1) & 1]);
-            fma32_uniform(acc[c], cur[c & 1], s2u);
-            if (c + 1 < CHUNKS) {
-              tmem_wait_ld(cur[(c + 1) & 1]);
-              if (c + 2 == CHUNKS) {
-                // the last chunk is in registers: hand the TMEM accumulator back
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->tempty[b]);
-              }
+            if (c + 2 < CHUNKS) tmem_ld32_async(tbase + (c + 2) * 32, cur[(c + 2) % 3]);
+            fma32_uniform(acc[c], cur[c % 3], s2u);
+            if ((c & 1) && c + 1 < CHUNKS) {
+              tmem_wait_ld(cur[(c + 1) % 3]);
+              if (c + 2 < CHUNKS) tmem_tie32(cur[(c + 2) % 3]);
+              if (c + 2 >= CHUNKS - 1) release();
             }
           }
         }
