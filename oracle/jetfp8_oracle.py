@@ -40,6 +40,10 @@ What the pages fix, and the readings taken where they are silent:
 * SwiGLU (decoder MLP support): h = bf16_rne(silu(g)·u), silu(g) = g/(1+e^-g),
   computed in FP64; its backward in FP64, rounded once to bf16.  The pages do
   not describe it; it exists because the fused MLP chain needs it.
+* RMSNorm backward (decoder-layer support; the pages fuse the forward only):
+  the exact derivative of y = (x·r)·γ, r = (mean(x²)+eps)^-1/2, evaluated in
+  FP64 with the r the forward saved (FP32), ∇x rounded once to bf16; ∇γ is the
+  FP64 sum over rows.
 
 Layouts here are logical: a group-scale array for an [R, C] tensor quantised in
 1×128 row groups is float32 [C/128, R] (group index major).  Padding of the
@@ -57,7 +61,7 @@ __all__ = [
     "quant_rowgroups", "quant_act_1x128", "quant_weight_128x128",
     "requant_rowgrp_to_colgrp", "quant_grad_dual", "block_scaled_gemm",
     "gemm_fprop", "gemm_dgrad", "gemm_wgrad", "rmsnorm_quant",
-    "swiglu_quant", "swiglu_bwd",
+    "swiglu_quant", "swiglu_bwd", "rmsnorm_bwd",
 ]
 
 
@@ -313,3 +317,26 @@ def swiglu_bwd(gu, dh):
     dg = dh * u * sig * (1.0 + g * (1.0 - sig))
     du = dh * g * sig
     return bf16_rne(np.concatenate([dg, du], axis=1))
+
+
+# ---------------------------------------------------------------------------
+# Step 8: RMSNorm backward (decoder-layer support, not on the pages)
+# ---------------------------------------------------------------------------
+def rmsnorm_bwd(x, gamma, rstd, dy):
+    """Backward of y = (x·r)·γ with r = 1/sqrt(Σx²/H + eps) per row, given the
+    forward's saved r:
+        ∂L/∂x_i = r·γ_i·dy_i − x_i·r³·(Σ_j γ_j·dy_j·x_j)/H
+        ∂L/∂γ_j = Σ_rows dy_j·x_j·r
+    (r depends on x through Σx²: ∂r/∂x_i = −x_i·r³/H).  FP64; ∇x is rounded
+    once to bf16, ∇γ is returned in FP64.
+    Returns (dx float64 of bf16 values [M, H], dgamma float64 [H])."""
+    x = np.asarray(x, dtype=np.float64)
+    g = np.asarray(gamma, dtype=np.float64)
+    r = np.asarray(rstd, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    H = x.shape[1]
+    gd = dy * g[None, :]
+    dot = (gd * x).sum(axis=1)
+    dx = r[:, None] * gd - x * (r ** 3 * dot / H)[:, None]
+    dgamma = (dy * x * r[:, None]).sum(axis=0)
+    return bf16_rne(dx), dgamma

@@ -55,3 +55,63 @@ def test_swiglu_matches_torch_float64():
     out.backward(torch.from_numpy(dh).double())
     refd = tg.grad.numpy()
     assert np.all(np.abs(d - refd) <= np.abs(refd) * 2.0 ** -8 + 1e-300)
+
+
+def _rmsnorm_forward_f64(x, gamma, eps):
+    r = 1.0 / np.sqrt((x * x).sum(axis=1) / x.shape[1] + eps)
+    return (x * r[:, None]) * gamma[None, :], r
+
+
+def test_rmsnorm_bwd_matches_central_differences():
+    """The oracle's backward (without its final bf16 rounding) against central
+    differences of the FP64 forward, L = Σ y·dy, on a tiny problem."""
+    rng = np.random.default_rng(3)
+    M, H, eps = 3, 8, 1e-6
+    x = rng.standard_normal((M, H))
+    gamma = rng.uniform(0.5, 1.5, H)
+    dy = rng.standard_normal((M, H))
+    _, r = _rmsnorm_forward_f64(x, gamma, eps)
+    loss = lambda xx, gg: float((_rmsnorm_forward_f64(xx, gg, eps)[0] * dy).sum())  # noqa: E731
+    h = 1e-6
+    dx_fd = np.zeros_like(x)
+    for i in range(M):
+        for j in range(H):
+            xp, xm = x.copy(), x.copy()
+            xp[i, j] += h
+            xm[i, j] -= h
+            dx_fd[i, j] = (loss(xp, gamma) - loss(xm, gamma)) / (2 * h)
+    dg_fd = np.zeros(H)
+    for j in range(H):
+        gp, gm = gamma.copy(), gamma.copy()
+        gp[j] += h
+        gm[j] -= h
+        dg_fd[j] = (loss(x, gp) - loss(x, gm)) / (2 * h)
+    # the formula itself, before the bf16 rounding of dx
+    gd = dy * gamma[None, :]
+    dot = (gd * x).sum(axis=1)
+    dx = r[:, None] * gd - x * (r ** 3 * dot / H)[:, None]
+    assert np.allclose(dx, dx_fd, rtol=1e-6, atol=1e-8)
+    _, dg = O.rmsnorm_bwd(x, gamma, r, dy)
+    assert np.allclose(dg, dg_fd, rtol=1e-6, atol=1e-8)
+    dxo, _ = O.rmsnorm_bwd(x, gamma, r, dy)
+    assert np.array_equal(dxo, O.bf16_rne(dx))
+
+
+def test_rmsnorm_bwd_matches_torch_autograd_float64():
+    """Against torch autograd in FP64 on the CPU (an independent derivative)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(4)
+    M, H, eps = 5, 256, 1e-6
+    x = rng.standard_normal((M, H))
+    gamma = rng.uniform(0.5, 1.5, H)
+    dy = rng.standard_normal((M, H)) * 1e-3
+    xt = torch.tensor(x, requires_grad=True)
+    gt = torch.tensor(gamma, requires_grad=True)
+    r = torch.rsqrt((xt * xt).mean(dim=1, keepdim=True) + eps)
+    y = (xt * r) * gt
+    (y * torch.tensor(dy)).sum().backward()
+    dxo, dgo = O.rmsnorm_bwd(x, gamma, r.detach().numpy()[:, 0], dy)
+    ref = xt.grad.numpy()
+    # dxo is the FP64 formula rounded once to bf16: within one bf16 ulp of autograd
+    assert np.all(np.abs(dxo - ref) <= np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 8))
+    assert np.allclose(dgo, gt.grad.numpy(), rtol=1e-12, atol=1e-15)
