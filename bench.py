@@ -57,6 +57,8 @@ QUANT_BYTES = {
     "swiglu_quant": 2 + 2 + 1 + 4 / 128,
     # per element of ∇h [M, I]: gate, up and ∇h read, ∇gate and ∇up written
     "swiglu_bwd": 5 * 2,
+    # per element: x and ∇y read, ∇x written (γ, r and ∇γ are per row or column)
+    "rmsnorm_bwd": 3 * 2,
 }
 
 
@@ -493,7 +495,8 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
 # single-kernel cases (profiling aid): one kernel, one shape, W + K launches
 # ---------------------------------------------------------------------------
 CASES = {"fprop", "dgrad", "wgrad", "quant_act", "rmsnorm_quant", "quant_weight",
-         "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd", "fprop_quant", "fprop_then_quant"}
+         "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd", "fprop_quant", "fprop_then_quant",
+         "rmsnorm_bwd"}
 
 
 def run_case(args):
@@ -506,6 +509,20 @@ def run_case(args):
     from fp8_mixed_granularity_gb300 import workloads as W
     from fp8_mixed_granularity_gb300.linear import LinearBuffers
     M, N, K = (int(v) for v in args.shape.split(","))
+    if args.case == "rmsnorm_bwd":
+        # RMSNorm backward on an [M, H] = [M, K] activation with its forward's r
+        x = W.device_activations(M, K, dev, seed=1)
+        gamma = W.device_uniform((K,), 0.5, 1.5, dev, seed=4)
+        dy = W.device_normal((M, K), 1e-3, dev, seed=3)
+        xq, sx = J.empty_rowgroup_quant(M, K, dev)
+        rstd = torch.empty(M, dtype=torch.float32, device=dev)
+        J.jetfp8_rmsnorm_quant(x, gamma, 1e-6, xq, sx, rstd)
+        dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        dg = torch.empty(K, dtype=torch.float32, device=dev)
+        ws = torch.empty(J.jetfp8_rmsnorm_bwd_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+        fn = lambda: J.jetfp8_rmsnorm_bwd(x, gamma, rstd, dy, dx, dg, ws)  # noqa: E731
+        _time_case(args, fn, M * K * QUANT_BYTES[args.case], "GB/s", [M, N, K])
+        return
     if args.case in ("swiglu_quant", "swiglu_bwd"):
         # SwiGLU of an [M, 2I] gate/up output, I = N / 2 (N = the gate/up width)
         I = N // 2

@@ -258,6 +258,26 @@ jetfp8_status jetfp8_gemm_dgrad_quant(const uint8_t* dyq, const float* sdy, cons
   return from_cuda(launch_gemm(g, stream));
 }
 
+size_t jetfp8_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H) {
+  if (M <= 0 || H <= 0) return 0;
+  return rmsnorm_bwd_workspace_bytes(M, H);
+}
+
+jetfp8_status jetfp8_rmsnorm_bwd(const void* x_bf16, const void* gamma_bf16, const float* rstd,
+                                 const void* dy_bf16, int64_t M, int64_t H, void* dx_bf16,
+                                 float* dgamma, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+  Check c;
+  c.bf(x_bf16).bf(gamma_bf16).ptr(rstd).bf(dy_bf16).bf(dx_bf16).ptr(dgamma).ptr(workspace)
+      .positive(M).mult128(H).fits(M, H);
+  if (c.st == JETFP8_OK && workspace_bytes < rmsnorm_bwd_workspace_bytes(M, H))
+    c.st = JETFP8_ERR_INVALID_ARG;
+  c.device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_rmsnorm_bwd(x_bf16, gamma_bf16, rstd, dy_bf16, M, H, dx_bf16, dgamma,
+                                      static_cast<float*>(workspace), stream));
+}
+
 jetfp8_status jetfp8_swiglu_quant(const void* gu_bf16, int64_t M, int64_t I, uint8_t* q, float* s,
                                   void* h_bf16, cudaStream_t stream) {
   Check c;

@@ -20,6 +20,10 @@ cudaError_t launch_quant_grad_dual(const void* dy, int64_t M, int64_t N, uint8_t
 cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, int64_t M,
                                  int64_t H, uint8_t* q, float* s, float* rstd, void* y,
                                  cudaStream_t st);
+size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H);
+cudaError_t launch_rmsnorm_bwd(const void* x, const void* gamma, const float* rstd, const void* dy,
+                               int64_t M, int64_t H, void* dx, float* dgamma, float* ws,
+                               cudaStream_t st);
 cudaError_t launch_swiglu_quant(const void* gu, int64_t M, int64_t I, uint8_t* q, float* s,
                                 void* h, cudaStream_t st);
 cudaError_t launch_swiglu_bwd(const void* gu, const void* dh, int64_t M, int64_t I, void* dgu,

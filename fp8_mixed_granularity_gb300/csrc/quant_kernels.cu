@@ -473,6 +473,104 @@ k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gam
 }
 
 // ---------------------------------------------------------------------------
+// RMSNorm backward (decoder-layer support).  With the forward's saved r:
+//   ∇x_i = r·(dy_i·γ_i) − x_i·(r³·Σ_j dy_j·γ_j·x_j / H)
+//   ∇γ_j = Σ_rows dy_j·x_j·r
+// ∇x: one warp per row, 8 lanes per 128-wide group as in R1; the row sum is
+// accumulated like R1's Σx² (16-term FP32 chunk sums per lane, lanes in FP64).
+// ∇γ: deterministic two-stage column sums — FP32 partial sums over 128-row
+// chunks into the caller's workspace [chunks][H], then each column's partials
+// added in chunk order in FP64.
+// ---------------------------------------------------------------------------
+constexpr int kNormBwdRows = 128;   // rows per ∇γ partial sum
+
+__global__ void __launch_bounds__(kThreads)
+k_rmsnorm_bwd_dx(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
+                 const float* __restrict__ rstd, const uint16_t* __restrict__ dy, uint32_t M,
+                 uint32_t H, uint16_t* __restrict__ dx) {
+  constexpr int U = 4;
+  const uint32_t lane = threadIdx.x & 31u, g4 = lane >> 3, l8 = lane & 7u;
+  const uint32_t warp = (blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * kThreads) >> 5;
+  const uint32_t groups = H / 128;
+  for (uint32_t row = warp; row < M; row += nwarps) {
+    const uint16_t* xr = x + (size_t)row * H;
+    const uint16_t* dr = dy + (size_t)row * H;
+    float dot = 0.0f;
+    for (uint32_t g0 = 0; g0 < groups; g0 += 4 * U) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t grp = g0 + 4 * u + g4;
+        if (grp >= groups) continue;
+        uint32_t rx[8], rd[8], rg[8];
+        ld32_cached(xr + grp * 128 + l8 * 16, rx);
+        ld32_cached(dr + grp * 128 + l8 * 16, rd);
+        ld32_cached(gamma + grp * 128 + l8 * 16, rg);
+        float cs = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const float2 fx = bf2_to_f2(rx[w]), fd = bf2_to_f2(rd[w]), fg = bf2_to_f2(rg[w]);
+          cs = __fmaf_rn(__fmul_rn(fd.x, fg.x), fx.x, cs);
+          cs = __fmaf_rn(__fmul_rn(fd.y, fg.y), fx.y, cs);
+        }
+        dot = __fadd_rn(dot, cs);
+      }
+    }
+    double d = (double)dot;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(kFull, d, o);
+    const float r = rstd[row];
+    const float c = (float)((double)r * (double)r * (double)r * d / (double)H);
+    for (uint32_t g0 = 0; g0 < groups; g0 += 4) {
+      const uint32_t grp = g0 + g4;
+      if (grp >= groups) continue;
+      uint32_t rx[8], rd[8], rg[8], out[8];
+      ld32_cached(xr + grp * 128 + l8 * 16, rx);
+      ld32_cached(dr + grp * 128 + l8 * 16, rd);
+      ld32_cached(gamma + grp * 128 + l8 * 16, rg);
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float2 fx = bf2_to_f2(rx[w]), fd = bf2_to_f2(rd[w]), fg = bf2_to_f2(rg[w]);
+        const float a = __fsub_rn(__fmul_rn(r, __fmul_rn(fd.x, fg.x)), __fmul_rn(fx.x, c));
+        const float b = __fsub_rn(__fmul_rn(r, __fmul_rn(fd.y, fg.y)), __fmul_rn(fx.y, c));
+        out[w] = f2_to_bf2(a, b);
+      }
+      st32(dx + (size_t)row * H + grp * 128 + l8 * 16, out);
+    }
+  }
+}
+
+// Partial ∇γ over rows [128p, 128p + 128) for 512 columns per CTA (2 per thread).
+__global__ void __launch_bounds__(kThreads)
+k_rmsnorm_bwd_dgamma_partial(const uint16_t* __restrict__ x, const float* __restrict__ rstd,
+                             const uint16_t* __restrict__ dy, uint32_t M, uint32_t H,
+                             float* __restrict__ ws) {
+  const uint32_t col = blockIdx.x * 512u + 2u * threadIdx.x;
+  const uint32_t p = blockIdx.y;
+  const uint32_t r0 = p * kNormBwdRows, r1 = min(M, r0 + kNormBwdRows);
+  if (col >= H) return;
+  float ax = 0.0f, ay = 0.0f;
+  for (uint32_t m = r0; m < r1; ++m) {
+    const float2 fx = bf2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(x + (size_t)m * H + col)));
+    const float2 fd = bf2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(dy + (size_t)m * H + col)));
+    const float r = __ldg(rstd + m);
+    ax = __fadd_rn(ax, __fmul_rn(__fmul_rn(fd.x, fx.x), r));
+    ay = __fadd_rn(ay, __fmul_rn(__fmul_rn(fd.y, fx.y), r));
+  }
+  *reinterpret_cast<float2*>(ws + (size_t)p * H + col) = make_float2(ax, ay);
+}
+
+__global__ void __launch_bounds__(kThreads)
+k_rmsnorm_bwd_dgamma_reduce(const float* __restrict__ ws, uint32_t chunks, uint32_t H,
+                            float* __restrict__ dgamma) {
+  const uint32_t col = blockIdx.x * kThreads + threadIdx.x;
+  if (col >= H) return;
+  double s = 0.0;
+  for (uint32_t p = 0; p < chunks; ++p) s += (double)__ldg(ws + (size_t)p * H + col);
+  dgamma[col] = (float)s;
+}
+
+// ---------------------------------------------------------------------------
 // X1: SwiGLU fused with the 1×128 quantiser; one warp per row of h [M, I].
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
@@ -600,6 +698,26 @@ cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, in
   k_rmsnorm_quant<<<grid, kThreads, 0, st>>>(
       static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma), eps, (uint32_t)M,
       (uint32_t)H, (uint32_t)round_up4(M), q, s, rstd, static_cast<uint16_t*>(y));
+  return cudaGetLastError();
+}
+
+size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H) {
+  return (size_t)((M + kNormBwdRows - 1) / kNormBwdRows) * (size_t)H * sizeof(float);
+}
+
+cudaError_t launch_rmsnorm_bwd(const void* x, const void* gamma, const float* rstd, const void* dy,
+                               int64_t M, int64_t H, void* dx, float* dgamma, float* ws,
+                               cudaStream_t st) {
+  const auto* xb = static_cast<const uint16_t*>(x);
+  const auto* db = static_cast<const uint16_t*>(dy);
+  const unsigned grid = grid_for((size_t)M, kThreads / 32, 8);
+  k_rmsnorm_bwd_dx<<<grid, kThreads, 0, st>>>(xb, static_cast<const uint16_t*>(gamma), rstd, db,
+                                              (uint32_t)M, (uint32_t)H, static_cast<uint16_t*>(dx));
+  const uint32_t chunks = (uint32_t)((M + kNormBwdRows - 1) / kNormBwdRows);
+  const dim3 pgrid((unsigned)((H + 511) / 512), chunks);
+  k_rmsnorm_bwd_dgamma_partial<<<pgrid, kThreads, 0, st>>>(xb, rstd, db, (uint32_t)M, (uint32_t)H, ws);
+  k_rmsnorm_bwd_dgamma_reduce<<<(unsigned)((H + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+      ws, chunks, (uint32_t)H, dgamma);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,7 @@ SIGNATURES = {
     "jetfp8_gemm_wgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_fprop_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_gemm_dgrad_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
+    "jetfp8_rmsnorm_bwd": [_P, _P, _P, _P, _I64, _I64, _P, _P, _P, ctypes.c_size_t, _P],
     "jetfp8_swiglu_quant": [_P, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_swiglu_bwd": [_P, _P, _I64, _I64, _P, _P],
     "jetfp8_get_last_device_error": [_P],
@@ -67,6 +68,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         lib.jetfp8_status_string.argtypes = [ctypes.c_int]
         lib.jetfp8_status_string.restype = ctypes.c_char_p
+        lib.jetfp8_rmsnorm_bwd_workspace_bytes.argtypes = [_I64, _I64]
+        lib.jetfp8_rmsnorm_bwd_workspace_bytes.restype = ctypes.c_size_t
         _lib = lib
     return _lib
 
@@ -202,6 +205,21 @@ def jetfp8_gemm_dgrad_quant(dyq, sdy, wqT, sw, dxq, dxs, dx=None, stream=None):
         _ptr(sw, _F, (N // 128, K // 128), "sw"), M, N, K, _ptr(dx, _BF, (M, K), "dx"),
         _ptr(dxq, _U8, (M, K), "dxq"), _ptr(dxs, _F, scale_shape(M, K), "dxs"), _stream(stream)),
         "jetfp8_gemm_dgrad_quant")
+
+
+def jetfp8_rmsnorm_bwd_workspace_bytes(M: int, H: int) -> int:
+    return int(load_library().jetfp8_rmsnorm_bwd_workspace_bytes(M, H))
+
+
+def jetfp8_rmsnorm_bwd(x, gamma, rstd, dy, dx, dgamma, workspace, stream=None):
+    """RMSNorm backward; `workspace` is a device tensor of at least
+    jetfp8_rmsnorm_bwd_workspace_bytes(M, H) bytes (its contents are overwritten)."""
+    M, H = x.shape
+    _check(load_library().jetfp8_rmsnorm_bwd(
+        _ptr(x, _BF, None, "x"), _ptr(gamma, _BF, (H,), "gamma"), _ptr(rstd, _F, (M,), "rstd"),
+        _ptr(dy, _BF, (M, H), "dy"), M, H, _ptr(dx, _BF, (M, H), "dx"), _ptr(dgamma, _F, (H,), "dgamma"),
+        _ptr(workspace, None, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "jetfp8_rmsnorm_bwd")
 
 
 def jetfp8_swiglu_quant(gu, q, s, h=None, stream=None):

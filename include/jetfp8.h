@@ -178,6 +178,24 @@ jetfp8_status jetfp8_gemm_dgrad_quant(const uint8_t* dyq, const float* sdy, cons
                                       const float* sw, int64_t M, int64_t N, int64_t K,
                                       void* dx_bf16, uint8_t* dxq, float* dxs, cudaStream_t stream);
 
+/* RMSNorm backward, for the decoder layer around the quantised linears (the
+ * pages fuse the forward only; this is the exact derivative of R1's
+ * y = (x·r)·γ, r = 1/sqrt(mean(x²) + eps), using the r that R1 saved):
+ *   ∇x_i = r·(dy_i·γ_i) − x_i·r³·(Σ_j dy_j·γ_j·x_j)/H       (FP32, rounded to bf16)
+ *   ∇γ_j = Σ_rows dy_j·x_j·r                                 (deterministic: FP32 sums
+ *          over 128-row chunks, chunks added in order in FP64)
+ *   x bf16 [M, H], gamma bf16 [H], rstd fp32 [M] (R1's output), dy bf16 [M, H]
+ *   dx bf16 [M, H], dgamma fp32 [H]
+ *   workspace: caller-owned device memory of at least
+ *              jetfp8_rmsnorm_bwd_workspace_bytes(M, H) bytes (16-byte aligned),
+ *              overwritten by the call; JETFP8_ERR_INVALID_ARG if smaller.
+ * H multiple of 128, M >= 1. */
+size_t jetfp8_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H);
+jetfp8_status jetfp8_rmsnorm_bwd(const void* x_bf16, const void* gamma_bf16, const float* rstd,
+                                 const void* dy_bf16, int64_t M, int64_t H, void* dx_bf16,
+                                 float* dgamma, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
 /* X1 — SwiGLU fused with the 1×128 quantiser, for the decoder MLP between the
  * gate/up and down projections (not described by the pages):
  *   h = bf16(silu(g)·u), silu(g) = g/(1+exp(-g)), in FP32; then Q1 on h.

@@ -42,11 +42,13 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_binding_covers_every_declared_symbol():
     from fp8_mixed_granularity_gb300 import jetfp8
+    # entry points that return something other than a status are bound apart
+    not_status = {"jetfp8_status_string", "jetfp8_rmsnorm_bwd_workspace_bytes"}
     for name in _declared():
-        if name == "jetfp8_status_string":
-            continue
-        assert name in jetfp8.SIGNATURES, name
-        assert callable(getattr(jetfp8, name)), name
+        if name not in not_status:
+            assert name in jetfp8.SIGNATURES, name
+        if name != "jetfp8_status_string":
+            assert callable(getattr(jetfp8, name)), name
 
 
 def test_status_strings(lib):
@@ -68,6 +70,12 @@ def test_validation_rejects_before_touching_the_device(lib):
     # fused output quantiser: the output width must be a multiple of 256
     assert lib.jetfp8_gemm_fprop_quant(P(64), P(64), P(64), P(64), 4, 384, 128, None, P(64), P(64), None) == 2
     assert lib.jetfp8_gemm_dgrad_quant(P(64), P(64), P(64), P(64), 4, 256, 384, None, P(64), P(64), None) == 2
+    # RMSNorm backward: workspace size and a too-small workspace
+    lib.jetfp8_rmsnorm_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.jetfp8_rmsnorm_bwd_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(300, 256) == 3 * 256 * 4
+    assert lib.jetfp8_rmsnorm_bwd(P(64), P(64), P(64), P(64), ctypes.c_int64(300), ctypes.c_int64(256),
+                                  P(64), P(64), P(64), ctypes.c_size_t(3 * 256 * 4 - 4), None) == 1
     # WGrad needs M multiple of 128
     assert lib.jetfp8_gemm_wgrad(P(64), P(64), P(64), P(64), 100, 128, 128, P(64), 0, None) == 2
     # non-positive M
