@@ -11,6 +11,13 @@ namespace jetfp8 {
 // One error word per device, written by kernels whose bounded waits expire.
 __device__ unsigned g_device_error_word;
 
+// Scratch of jetfp8_rmsnorm_bwd_noalloc: a fixed device array (one per device,
+// created with the module), so that entry point allocates nothing.  Every
+// call uses the same array: calls that overlap in time (other streams, other
+// host threads) race on it.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -18,6 +25,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   std::once_flag once;
   unsigned* err_word = nullptr;
+  void* scratch = nullptr;   // this device's g_noalloc_scratch
   int sms = 0;
   bool sm103 = false;
   bool ok = false;
@@ -36,6 +44,9 @@ DeviceInfo* current_device() {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return;
     d->err_word = static_cast<unsigned*>(p);
+    void* sp = nullptr;
+    if (cudaGetSymbolAddress(&sp, g_noalloc_scratch) != cudaSuccess) return;
+    d->scratch = sp;
     d->ok = true;
   });
   return d->ok ? d : nullptr;
@@ -276,6 +287,24 @@ jetfp8_status jetfp8_rmsnorm_bwd(const void* x_bf16, const void* gamma_bf16, con
   if (c.st != JETFP8_OK) return c.st;
   return from_cuda(launch_rmsnorm_bwd(x_bf16, gamma_bf16, rstd, dy_bf16, M, H, dx_bf16, dgamma,
                                       static_cast<float*>(workspace), stream));
+}
+
+jetfp8_status jetfp8_rmsnorm_bwd_noalloc(const void* x_bf16, const void* gamma_bf16, const float* rstd,
+                                         const void* dy_bf16, int64_t M, int64_t H, void* dx_bf16,
+                                         float* dgamma, cudaStream_t stream) {
+  Check c;
+  c.bf(x_bf16).bf(gamma_bf16).ptr(rstd).bf(dy_bf16).bf(dx_bf16).ptr(dgamma).positive(M).mult128(H)
+      .fits(M, H);
+  if (c.st == JETFP8_OK && rmsnorm_bwd_workspace_bytes(M, H) > kNoAllocScratchBytes)
+    c.st = JETFP8_ERR_UNSUPPORTED_SHAPE;
+  c.device();
+  if (c.st != JETFP8_OK) return c.st;
+  // every partial sum the kernels read is written first in the same call, so
+  // nothing in the scratch needs clearing
+  DeviceInfo* d = current_device();
+  if (d == nullptr || d->scratch == nullptr) return JETFP8_ERR_CUDA;
+  return from_cuda(launch_rmsnorm_bwd(x_bf16, gamma_bf16, rstd, dy_bf16, M, H, dx_bf16, dgamma,
+                                      static_cast<float*>(d->scratch), stream));
 }
 
 jetfp8_status jetfp8_swiglu_quant(const void* gu_bf16, int64_t M, int64_t I, uint8_t* q, float* s,

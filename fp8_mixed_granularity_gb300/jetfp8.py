@@ -42,6 +42,7 @@ SIGNATURES = {
     "jetfp8_gemm_fprop_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_gemm_dgrad_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_rmsnorm_bwd": [_P, _P, _P, _P, _I64, _I64, _P, _P, _P, ctypes.c_size_t, _P],
+    "jetfp8_rmsnorm_bwd_noalloc": [_P, _P, _P, _P, _I64, _I64, _P, _P, _P],
     "jetfp8_swiglu_quant": [_P, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_swiglu_bwd": [_P, _P, _I64, _I64, _P, _P],
     "jetfp8_get_last_device_error": [_P],
@@ -220,6 +221,16 @@ def jetfp8_rmsnorm_bwd(x, gamma, rstd, dy, dx, dgamma, workspace, stream=None):
         _ptr(dy, _BF, (M, H), "dy"), M, H, _ptr(dx, _BF, (M, H), "dx"), _ptr(dgamma, _F, (H,), "dgamma"),
         _ptr(workspace, None, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)), "jetfp8_rmsnorm_bwd")
+
+
+def jetfp8_rmsnorm_bwd_noalloc(x, gamma, rstd, dy, dx, dgamma, stream=None):
+    """RMSNorm backward using the library's fixed scratch (no workspace; calls
+    that overlap in time race on that scratch)."""
+    M, H = x.shape
+    _check(load_library().jetfp8_rmsnorm_bwd_noalloc(
+        _ptr(x, _BF, None, "x"), _ptr(gamma, _BF, (H,), "gamma"), _ptr(rstd, _F, (M,), "rstd"),
+        _ptr(dy, _BF, (M, H), "dy"), M, H, _ptr(dx, _BF, (M, H), "dx"), _ptr(dgamma, _F, (H,), "dgamma"),
+        _stream(stream)), "jetfp8_rmsnorm_bwd_noalloc")
 
 
 def jetfp8_swiglu_quant(gu, q, s, h=None, stream=None):

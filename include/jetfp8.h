@@ -196,6 +196,21 @@ jetfp8_status jetfp8_rmsnorm_bwd(const void* x_bf16, const void* gamma_bf16, con
                                  float* dgamma, void* workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
 
+/* jetfp8_rmsnorm_bwd without a workspace argument: the library's own scratch
+ * is a fixed device array of 8 MiB per device (created with the library, no
+ * allocation at the call), so this entry point allocates nothing.  The pages
+ * have no counterpart; it exists for callers that cannot hand the library
+ * memory.  Results equal jetfp8_rmsnorm_bwd's bit for bit.
+ *   Arguments as jetfp8_rmsnorm_bwd without workspace / workspace_bytes.
+ *   JETFP8_ERR_UNSUPPORTED_SHAPE when jetfp8_rmsnorm_bwd_workspace_bytes(M, H)
+ *   exceeds 8 MiB (ceil(M/128)·H·4 bytes; e.g. M <= 65536 rows at H = 4096).
+ *   All calls share the one scratch array: calls that overlap in time (on
+ *   other streams or from other host threads) race and must be serialised by
+ *   the caller; calls on one stream are ordered and safe. */
+jetfp8_status jetfp8_rmsnorm_bwd_noalloc(const void* x_bf16, const void* gamma_bf16, const float* rstd,
+                                         const void* dy_bf16, int64_t M, int64_t H, void* dx_bf16,
+                                         float* dgamma, cudaStream_t stream);
+
 /* X1 — SwiGLU fused with the 1×128 quantiser, for the decoder MLP between the
  * gate/up and down projections (not described by the pages):
  *   h = bf16(silu(g)·u), silu(g) = g/(1+exp(-g)), in FP32; then Q1 on h.
