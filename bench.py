@@ -496,7 +496,7 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
 # ---------------------------------------------------------------------------
 CASES = {"fprop", "dgrad", "wgrad", "quant_act", "rmsnorm_quant", "quant_weight",
          "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd", "fprop_quant", "fprop_then_quant",
-         "rmsnorm_bwd"}
+         "rmsnorm_bwd", "decoder_layer"}
 
 
 def run_case(args):
@@ -509,6 +509,32 @@ def run_case(args):
     from fp8_mixed_granularity_gb300 import workloads as W
     from fp8_mixed_granularity_gb300.linear import LinearBuffers
     M, N, K = (int(v) for v in args.shape.split(","))
+    if args.case == "decoder_layer":
+        # a Llama-3.1-8B-shaped decoder layer (BF16 attention core), forward +
+        # backward, on M tokens = M/1024 sequences of 1024; the rate counts the
+        # four linear layers' GEMM FLOPs (6·M·N·K each) over the whole layer time
+        from fp8_mixed_granularity_gb300.decoder_layer import DecoderLayerFP8, llama8b
+        shape = llama8b()
+        S = 1024
+        Bq = max(1, M // S)
+        T = Bq * S
+        D, I = shape.hidden, shape.intermediate
+        w = {"wqkv": W.device_normal((shape.qkv_width, D), 0.02, dev, seed=11),
+             "wo": W.device_normal((D, shape.attn_width), 0.02, dev, seed=12),
+             "wgu": W.device_normal((2 * I, D), 0.02, dev, seed=13),
+             "wd": W.device_normal((D, I), 0.02, dev, seed=14),
+             "gamma1": W.device_uniform((D,), 0.5, 1.5, dev, seed=15),
+             "gamma2": W.device_uniform((D,), 0.5, 1.5, dev, seed=16)}
+        x = W.device_activations(T, D, dev, seed=17)
+        dy = W.device_normal((T, D), 1e-3, dev, seed=18)
+        layer = DecoderLayerFP8(shape, w, dev)
+
+        def fwd_bwd():
+            layer.forward(x, Bq, S)
+            layer.backward(dy)
+        flops = sum(6 * m * n * k for _, m, n, k in shape.linears(T))
+        _time_case(args, fwd_bwd, flops, "TFLOP/s", [T, D, D])
+        return
     if args.case == "rmsnorm_bwd":
         # RMSNorm backward on an [M, H] = [M, K] activation with its forward's r
         x = W.device_activations(M, K, dev, seed=1)
