@@ -275,7 +275,7 @@ def run_ours(args):
     g.build()
     from fp8_mixed_granularity_gb300 import jetfp8 as J
     from fp8_mixed_granularity_gb300 import workloads as W
-    from fp8_mixed_granularity_gb300.linear import LinearBuffers
+    from fp8_mixed_granularity_gb300.linear import LinearBuffers, wgrad_grouped
 
     lins = W.llama8b_training()
     norm_fed = {"qkv", "gate_up"}
@@ -291,11 +291,14 @@ def run_ours(args):
     gemm_flops = sum(3 * l.gemm_flops for l in lins)
 
     def step(events=None):
+        # forward and backward of each linear; the four WGrads (independent of
+        # everything after them) go out together as one grouped launch
         n = 0
         for b, (x, w, dy, gamma) in zip(bufs, inputs):
             ev = None if events is None else events.setdefault(b.lin.name, [])
             n += b.forward(x, w, gamma, events=ev)
-            n += b.backward(dy, events=ev)
+            n += b.backward(dy, events=ev, wgrad=False)
+        n += wgrad_grouped(bufs, events=None if events is None else events.setdefault("all", []))
         return n
 
     for _ in range(args.warmup):
@@ -358,7 +361,8 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3", "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens": 8192, "linears": {l.name: [l.K, l.N] for l in lins},
-                   "step": "fwd+bwd of the 4 linears incl. all quantisers", "parallelism": f"replicas{world}",
+                   "step": "fwd+bwd of the 4 linears incl. all quantisers; the 4 WGrads in one grouped launch",
+                   "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (no flush)"},
         "roofline": {
             "kernel": f"k_gemm_e4m3_blockscaled gate/up FProp {dom.M}x{dom.N}x{dom.K}",
@@ -496,7 +500,7 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
 # ---------------------------------------------------------------------------
 CASES = {"fprop", "dgrad", "wgrad", "quant_act", "rmsnorm_quant", "quant_weight",
          "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd", "fprop_quant", "fprop_then_quant",
-         "rmsnorm_bwd", "decoder_layer"}
+         "rmsnorm_bwd", "decoder_layer", "wgrad_grouped", "wgrad_separate"}
 
 
 def run_case(args):
@@ -534,6 +538,26 @@ def run_case(args):
             layer.backward(dy)
         flops = sum(6 * m * n * k for _, m, n, k in shape.linears(T))
         _time_case(args, fwd_bwd, flops, "TFLOP/s", [T, D, D])
+        return
+    if args.case in ("wgrad_grouped", "wgrad_separate"):
+        # the WGrads of a Llama-3.1-8B layer's four linears on M tokens: one
+        # grouped launch, or four launches one after another
+        from fp8_mixed_granularity_gb300.linear import wgrad_grouped
+        lins = W.llama8b_training(M)
+        bufs = []
+        for i, lin in enumerate(lins):
+            b = LinearBuffers(lin, dev)
+            b.forward(W.device_activations(M, lin.K, dev, seed=1 + i), W.device_normal((lin.N, lin.K), 0.02, dev, seed=5 + i))
+            b.backward(W.device_normal((M, lin.N), 1e-3, dev, seed=9 + i), wgrad=False)
+            bufs.append(b)
+        if args.case == "wgrad_grouped":
+            fn = lambda: wgrad_grouped(bufs)  # noqa: E731
+        else:
+            def fn():
+                for b in bufs:
+                    t = b.t
+                    J.jetfp8_gemm_wgrad(t["dyqT"], t["sdyT"], t["xqT"], t["sxT"], t["dw"])
+        _time_case(args, fn, sum(l.gemm_flops for l in lins), "TFLOP/s", [M, 0, 0])
         return
     if args.case == "rmsnorm_bwd":
         # RMSNorm backward on an [M, H] = [M, K] activation with its forward's r

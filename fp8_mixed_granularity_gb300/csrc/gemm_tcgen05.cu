@@ -43,6 +43,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstddef>
+#include <cstring>
 #include <type_traits>
 
 #include "jetfp8_common.cuh"
@@ -62,9 +64,12 @@ constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 384
 // the launch total, or setmaxnreg.inc would wait forever.  The host refuses to
 // launch unless the compiled kernel uses exactly LAUNCH_REGS.
 constexpr int LAUNCH_REGS = 168;
-constexpr int CTRL_REGS = 24;
-constexpr int EPI_REGS = 240;
-static_assert(128 * CTRL_REGS + 256 * EPI_REGS <= THREADS * LAUNCH_REGS, "register split");
+// Grouped launches (several problems per launch) give the control warps 32:
+// the TMA producer then also tracks which problem a tile belongs to.
+template <int G> constexpr int CTRL_REGS = G > 1 ? 32 : 24;
+template <int G> constexpr int EPI_REGS = G > 1 ? 232 : 240;
+static_assert(128 * CTRL_REGS<1> + 256 * EPI_REGS<1> <= THREADS * LAUNCH_REGS, "register split");
+static_assert(128 * CTRL_REGS<2> + 256 * EPI_REGS<2> <= THREADS * LAUNCH_REGS, "register split");
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int MAX_STAGES = 8, MAX_BUFS = 4;
 // bf16 output leaves through shared memory in 32-row × 32-column chunks, one
@@ -135,6 +140,35 @@ struct DevArgs {
   unsigned* err;
 };
 
+// Kernel parameters: G problems of one tile configuration run as a single
+// persistent tile sequence; problem g owns the tiles [tile_end[g-1], tile_end[g]).
+// A plain GEMM is G = 1.  Grouping lets the last wave of one problem's tiles be
+// filled with another's (the WGrads of a layer's linears share the token
+// count, so their tiles cost the same).  tmQ serves the fused output
+// quantiser, which only single-problem launches use.
+constexpr int MAX_GROUP = 4;
+template <int G>
+struct KParams {
+  CUtensorMap tmA[G], tmB[G], tmOut[G];
+  CUtensorMap tmQ;
+  DevArgs p[G];
+  int tile_end[G];
+};
+
+// Global tile index -> (problem, tile index within that problem).
+template <int G>
+__device__ __forceinline__ int problem_of(const KParams<G>& kp, int tile, int& local) {
+  int g = 0, start = 0;
+#pragma unroll
+  for (int i = 0; i + 1 < G; ++i)
+    if (tile >= kp.tile_end[i]) {
+      g = i + 1;
+      start = kp.tile_end[i];
+    }
+  local = tile - start;
+  return g;
+}
+
 // Tile index -> (m tile, n tile).  Consecutive tiles (which run at the same
 // time on neighbouring SMs) share one operand tile; the other operand is
 // streamed once per band, so the order keeps the re-streamed operand the
@@ -156,8 +190,8 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -189,17 +223,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// The same wait on 32-bit shared-memory addresses (barrier and abort flag),
+// for the TMA producer, which runs on few registers.
+__device__ __forceinline__ bool mbar_wait_s(uint32_t bar, uint32_t parity, uint32_t abort_addr) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    int flag;
+    asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(flag) : "r"(abort_addr) : "memory");
+    if (flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_NS) return false;
+  }
+}
+
 __device__ __forceinline__ void record_abort(volatile int* abort_flag, unsigned* err) {
   *abort_flag = 1;
   atomicOr(err, kErrTimeout);
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      "l"(map), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
 
@@ -428,12 +478,9 @@ struct ColScaleVec<128> {
   using T = float4;
 };
 
-template <int BN_, bool COLS>
+template <int BN_, bool COLS, int G>
 __global__ void __launch_bounds__(THREADS, 1)
-k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmOut,
-                        const __grid_constant__ CUtensorMap tmQ, const DevArgs p) {
+k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
   using C = Cfg<BN_>;
   constexpr int BN = C::BN, STAGES = C::STAGES, ACC_BUFS = C::ACC_BUFS;
   constexpr int EPI_COLS = C::EPI_COLS, CHUNKS = C::CHUNKS;
@@ -452,7 +499,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int num_tiles = kp.tile_end[G - 1];
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -479,28 +526,44 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
   const uint32_t tmem = bars->tmem_base;
 
   if (warp < EPI_WARP0) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS<G>));
     if (warp == 0) {
       // ---------------- TMA producer ----------------
+      // (32-bit shared-memory addresses throughout: this warp has few registers)
       if (lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          asm volatile("prefetch.tensormap [%0];" ::"l"(&kp.tmA[g]) : "memory");
+          asm volatile("prefetch.tensormap [%0];" ::"l"(&kp.tmB[g]) : "memory");
+        }
+        // the stages sit right below the barriers
+        const uint32_t full0 = smem_u32(&bars->full[0]);
+        constexpr uint32_t STAGE0_OFF = STAGES * C::STAGE_BYTES + offsetof(Barriers, full);
+        constexpr uint32_t EMPTY_OFF = offsetof(Barriers, empty) - offsetof(Barriers, full);
+        constexpr uint32_t ABORT_OFF = offsetof(Barriers, abort_flag) - offsetof(Barriers, full);
         uint32_t it = 0;
         bool ok = true;
+        static_assert(offsetof(KParams<G>, tmB) == offsetof(KParams<G>, tmA) + G * sizeof(CUtensorMap),
+                      "map arrays are contiguous");
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-          int mt, nt;
-          tile_coords(p, tile, mt, nt);
-          for (int kb = 0; kb < p.nKB; ++kb, ++it) {
+          int local, mt, nt;
+          const int g = problem_of(kp, tile, local);
+          tile_coords(kp.p[g], local, mt, nt);
+          const int nkb = kp.p[g].nKB;
+          // tmB[g] lies G maps after tmA[g]: one live pointer
+          const CUtensorMap* const mA = &kp.tmA[g];
+          for (int kb = 0; kb < nkb; ++kb, ++it) {
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-            if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort_flag, true)) {
-              record_abort(abort_flag, p.err);
+            const uint32_t full = full0 + 8 * s;
+            if (!mbar_wait_s(full + EMPTY_OFF, ph ^ 1u, full0 + ABORT_OFF)) {
+              record_abort(abort_flag, kp.p[0].err);
               ok = false;
               break;
             }
-            uint8_t* st = smem + s * C::STAGE_BYTES;
-            mbar_arrive_expect_tx(&bars->full[s], C::STAGE_BYTES);
-            tma_load_2d(smem_u32(st), &tmA, &bars->full[s], kb * BK, mt * BM);
-            tma_load_2d(smem_u32(st + C::A_BYTES), &tmB, &bars->full[s], kb * BK, nt * BN);
+            const uint32_t st = full0 - STAGE0_OFF + s * C::STAGE_BYTES;
+            mbar_arrive_expect_tx(full, C::STAGE_BYTES);
+            tma_load_2d(st, mA, full, kb * BK, mt * BM);
+            tma_load_2d(st + C::A_BYTES, mA + G, full, kb * BK, nt * BN);
           }
         }
         if (!ok) {
@@ -516,12 +579,14 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
         uint32_t it = 0, acc_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-          for (int kb = 0; kb < p.nKB; ++kb, ++it, ++acc_it) {
+          int local;
+          const int nkb = kp.p[problem_of(kp, tile, local)].nKB;
+          for (int kb = 0; kb < nkb; ++kb, ++it, ++acc_it) {
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             const uint32_t b = acc_it % ACC_BUFS, bph = (acc_it / ACC_BUFS) & 1u;
             if (!mbar_wait(&bars->tempty[b], bph ^ 1u, abort_flag, true) ||
                 !mbar_wait(&bars->full[s], ph, abort_flag, true)) {
-              record_abort(abort_flag, p.err);
+              record_abort(abort_flag, kp.p[0].err);
               ok = false;
               break;
             }
@@ -538,11 +603,11 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
         }
         // all MMAs issued by this thread complete before TMEM is released
         umma_commit(&bars->done);
-        if (!mbar_wait(&bars->done, 0, abort_flag, false)) record_abort(abort_flag, p.err);
+        if (!mbar_wait(&bars->done, 0, abort_flag, false)) record_abort(abort_flag, kp.p[0].err);
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS<G>));
     // ---------------- promotion + epilogue ----------------
     const int ew = warp - EPI_WARP0;
     const int wg = ew >> 2;                 // column half of the tile
@@ -552,8 +617,10 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
     uint32_t acc_it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      int mt, nt;
-      tile_coords(p, tile, mt, nt);
+      int local, mt, nt;
+      const int g = problem_of(kp, tile, local);
+      const DevArgs& p = kp.p[g];
+      tile_coords(p, local, mt, nt);
       const int wrow0 = mt * BM + lq * 32;   // first tile row of this warp
       const int row = wrow0 + lane;          // the row whose sA this lane fetches
       const int col0 = nt * BN + wg * EPI_COLS;
@@ -642,7 +709,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
           sb_r[SL] = load_sb(kb + 2);
         }
         bool good = mbar_wait(&bars->tfull[b], bph, abort_flag, true);
-        if (!good) record_abort(abort_flag, p.err);
+        if (!good) record_abort(abort_flag, kp.p[0].err);
         if (__any_sync(0xffffffffu, !good)) return false;
         tc_fence_after();
         const uint32_t tbase = taddr_w + b * BN;
@@ -750,7 +817,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
                 }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0 && wrow0 < p.R) tma_store_2d(&tmOut, smem_u32(ob), col0 + cq * 32, wrow0);
+            if (lane == 0 && wrow0 < p.R) tma_store_2d(&kp.tmOut[g], smem_u32(ob), col0 + cq * 32, wrow0);
           }
         }
       } else if (p.out_fp32) {
@@ -817,8 +884,8 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ CUtensorMap tmA,
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && wrow0 < p.R) {
-            if (p.out != nullptr) tma_store_2d(&tmOut, smem_u32(ob), col0 + c * 32, wrow0);
-            if (fuse_q) tma_store_2d(&tmQ, smem_u32(qb), col0 + c * 32, wrow0);
+            if (p.out != nullptr) tma_store_2d(&kp.tmOut[g], smem_u32(ob), col0 + c * 32, wrow0);
+            if (fuse_q) tma_store_2d(&kp.tmQ, smem_u32(qb), col0 + c * 32, wrow0);
           }
         }
       }
@@ -905,10 +972,10 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 
 namespace {
 
-template <int BN, bool COLS>
-cudaError_t launch_cfg(const GemmArgs& a, int dev, cudaStream_t st) {
+template <int BN, bool COLS, int G>
+cudaError_t launch_cfg(const GemmArgs* a, int count, int dev, cudaStream_t st) {
   using C = Cfg<BN>;
-  auto kern = k_gemm_e4m3_blockscaled<BN, COLS>;
+  auto kern = k_gemm_e4m3_blockscaled<BN, COLS, G>;
   static int ready[64] = {0};   // 0 = unchecked, 1 = ok, -1 = unusable
   if (ready[dev] == 0) {
     // The setmaxnreg split assumes the kernel launches with LAUNCH_REGS
@@ -925,42 +992,60 @@ cudaError_t launch_cfg(const GemmArgs& a, int dev, cudaStream_t st) {
     }
   }
   if (ready[dev] != 1) return cudaErrorInvalidConfiguration;
-  CUtensorMap ta, tb, to, tq;
-  if (!make_map(&ta, a.A, (uint64_t)a.Kc, (uint64_t)a.R, BM) ||
-      !make_map(&tb, a.B, (uint64_t)a.Kc, (uint64_t)a.C, BN))
-    return cudaErrorInvalidValue;
-  if (a.out_fp32 || a.out == nullptr) {
-    to = ta;   // unused: fp32 epilogue, or no bf16 output
-  } else if (!make_out_map(&to, a.out, (uint64_t)a.C, (uint64_t)a.R)) {
+  if (count < 1 || count > G || (count > 1 && a[0].out_q != nullptr)) return cudaErrorInvalidValue;
+  unsigned* err = device_error_word();
+  if (err == nullptr) return cudaErrorInvalidValue;
+  KParams<G> kp;
+  memset(&kp, 0, sizeof(kp));
+  int tiles = 0;
+  for (int g = 0; g < G; ++g) {
+    if (g >= count) {
+      // unused slots own no tiles
+      kp.tmA[g] = kp.tmA[0];
+      kp.tmB[g] = kp.tmB[0];
+      kp.tmOut[g] = kp.tmOut[0];
+      kp.p[g] = kp.p[0];
+      kp.tile_end[g] = tiles;
+      continue;
+    }
+    const GemmArgs& x = a[g];
+    if (!make_map(&kp.tmA[g], x.A, (uint64_t)x.Kc, (uint64_t)x.R, BM) ||
+        !make_map(&kp.tmB[g], x.B, (uint64_t)x.Kc, (uint64_t)x.C, BN))
+      return cudaErrorInvalidValue;
+    if (x.out_fp32 || x.out == nullptr) {
+      kp.tmOut[g] = kp.tmA[g];   // unused: fp32 epilogue, or no bf16 output
+    } else if (!make_out_map(&kp.tmOut[g], x.out, (uint64_t)x.C, (uint64_t)x.R)) {
+      return cudaErrorInvalidValue;
+    }
+    DevArgs& d = kp.p[g];
+    d.sA = x.sA;
+    d.ld_sA = x.ld_sA;
+    d.sB = x.sB;
+    d.sb_j = x.sb_j;
+    d.sb_k = x.sb_k;
+    d.out = x.out;
+    d.R = (int)x.R;
+    d.C = (int)x.C;
+    d.nKB = (int)(x.Kc / BK);
+    d.tiles_m = (int)((x.R + BM - 1) / BM);
+    d.tiles_n = (int)(x.C / BN);
+    d.m_fastest = x.R <= x.C ? 1 : 0;
+    d.out_fp32 = x.out_fp32 ? 1 : 0;
+    d.out_q = x.out_q;
+    d.out_s = x.out_s;
+    d.ld_out_s = x.ld_out_s;
+    d.err = err;
+    tiles += d.tiles_m * d.tiles_n;
+    kp.tile_end[g] = tiles;
+  }
+  if (a[0].out_q == nullptr) {
+    kp.tmQ = kp.tmA[0];   // unused
+  } else if (!encode_codes_map(&kp.tmQ, a[0].out_q, (uint64_t)a[0].C, (uint64_t)a[0].R)) {
     return cudaErrorInvalidValue;
   }
-  if (a.out_q == nullptr) {
-    tq = ta;   // unused
-  } else if (!encode_codes_map(&tq, a.out_q, (uint64_t)a.C, (uint64_t)a.R)) {
-    return cudaErrorInvalidValue;
-  }
-  DevArgs d;
-  d.sA = a.sA;
-  d.ld_sA = a.ld_sA;
-  d.sB = a.sB;
-  d.sb_j = a.sb_j;
-  d.sb_k = a.sb_k;
-  d.out = a.out;
-  d.R = (int)a.R;
-  d.C = (int)a.C;
-  d.nKB = (int)(a.Kc / BK);
-  d.tiles_m = (int)((a.R + BM - 1) / BM);
-  d.tiles_n = (int)(a.C / BN);
-  d.m_fastest = a.R <= a.C ? 1 : 0;
-  d.out_fp32 = a.out_fp32 ? 1 : 0;
-  d.out_q = a.out_q;
-  d.out_s = a.out_s;
-  d.ld_out_s = a.ld_out_s;
-  d.err = device_error_word();
-  if (d.err == nullptr) return cudaErrorInvalidValue;
-  const int tiles = d.tiles_m * d.tiles_n;
+  if (tiles == 0) return cudaSuccess;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, THREADS, C::SMEM_BYTES, st>>>(ta, tb, to, tq, d);
+  kern<<<grid, THREADS, C::SMEM_BYTES, st>>>(kp);
   return cudaGetLastError();
 }
 
@@ -978,14 +1063,34 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   // SMs stream the weights; the arithmetic of every output element (its MMA
   // blocks and promotion order) does not depend on the tile width.
   const bool cols = a.b_mode == BScale::kColumn;
-  if (cols) return a.C % 256 == 0 ? launch_cfg<256, true>(a, dev, st) : launch_cfg<128, true>(a, dev, st);
+  if (cols)
+    return a.C % 256 == 0 ? launch_cfg<256, true, 1>(&a, 1, dev, st) : launch_cfg<128, true, 1>(&a, 1, dev, st);
   // the fused quantiser needs a thread's 128 columns to be a whole 1×128 group
   if (a.out_q != nullptr)
-    return a.C % 256 == 0 ? launch_cfg<256, false>(a, dev, st) : cudaErrorInvalidValue;
+    return a.C % 256 == 0 ? launch_cfg<256, false, 1>(&a, 1, dev, st) : cudaErrorInvalidValue;
   const int64_t tiles_m = (a.R + BM - 1) / BM, sms = num_sms();
-  if (a.C % 256 == 0 && tiles_m * (a.C / 256) >= sms) return launch_cfg<256, false>(a, dev, st);
-  if (a.C % 256 != 0 || tiles_m * (a.C / 128) >= sms) return launch_cfg<128, false>(a, dev, st);
-  return launch_cfg<64, false>(a, dev, st);
+  if (a.C % 256 == 0 && tiles_m * (a.C / 256) >= sms) return launch_cfg<256, false, 1>(&a, 1, dev, st);
+  if (a.C % 256 != 0 || tiles_m * (a.C / 128) >= sms) return launch_cfg<128, false, 1>(&a, 1, dev, st);
+  return launch_cfg<64, false, 1>(&a, 1, dev, st);
+}
+
+cudaError_t launch_gemm_grouped(const GemmArgs* a, int count, cudaStream_t st) {
+  if (count < 1 || count > MAX_GROUP) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  // one tile configuration for all problems: 256-wide tiles when every output
+  // width allows, else 128-wide (an element's arithmetic does not depend on
+  // the tile width, so each problem's result equals its single launch's)
+  bool all256 = true;
+  for (int g = 0; g < count; ++g) {
+    if (a[g].b_mode != BScale::kColumn || a[g].out_q != nullptr || a[g].out_fp32 != a[0].out_fp32)
+      return cudaErrorInvalidValue;
+    all256 = all256 && a[g].C % 256 == 0;
+  }
+  return all256 ? launch_cfg<256, true, MAX_GROUP>(a, count, dev, st)
+                : launch_cfg<128, true, MAX_GROUP>(a, count, dev, st);
 }
 
 }  // namespace jetfp8

@@ -235,6 +235,31 @@ jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const ui
   return gemm_common(g, out_dtype, stream);
 }
 
+jetfp8_status jetfp8_gemm_wgrad_grouped(int count, const uint8_t* const* dyqT,
+                                        const float* const* sdyT, const uint8_t* const* xqT,
+                                        const float* const* sxT, int64_t M, const int64_t* N,
+                                        const int64_t* K, void* const* dw,
+                                        jetfp8_out_dtype out_dtype, cudaStream_t stream) {
+  if (count < 1 || count > JETFP8_MAX_GROUP || dyqT == nullptr || sdyT == nullptr ||
+      xqT == nullptr || sxT == nullptr || N == nullptr || K == nullptr || dw == nullptr ||
+      (out_dtype != JETFP8_OUT_BF16 && out_dtype != JETFP8_OUT_FP32))
+    return JETFP8_ERR_INVALID_ARG;
+  GemmArgs g[JETFP8_MAX_GROUP];
+  Check c;
+  c.mult128(M);
+  for (int i = 0; i < count; ++i) {
+    c.ptr(dyqT[i]).ptr(sdyT[i]).ptr(xqT[i]).ptr(sxT[i]).bf(dw[i]).mult128(N[i]).mult128(K[i])
+        .fits(M, N[i]).fits(M, K[i]).fits(N[i], K[i]);
+    if (c.st != JETFP8_OK) return c.st;
+    // as jetfp8_gemm_wgrad, problem by problem
+    g[i] = GemmArgs{dyqT[i], xqT[i], sdyT[i], N[i], sxT[i], 0, K[i], BScale::kColumn,
+                    dw[i], out_dtype == JETFP8_OUT_FP32, N[i], K[i], M};
+  }
+  c.device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_gemm_grouped(g, count, stream));
+}
+
 jetfp8_status jetfp8_gemm_fprop_quant(const uint8_t* xq, const float* sx, const uint8_t* wq,
                                       const float* sw, int64_t M, int64_t N, int64_t K,
                                       void* y_bf16, uint8_t* yq, float* ys, cudaStream_t stream) {

@@ -55,5 +55,8 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
+// `count` (1..4) column-scale (WGrad) problems in one persistent launch; each
+// problem's output equals that of its own launch_gemm, bit for bit.
+cudaError_t launch_gemm_grouped(const GemmArgs* a, int count, cudaStream_t st);
 
 }  // namespace jetfp8

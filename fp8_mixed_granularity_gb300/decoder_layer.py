@@ -74,8 +74,10 @@ class _QLinear:
         return y
 
     def backward(self, dy, xq, sx):
-        """dy bf16 [M, N] -> (dx bf16 [M, K], dW fp32 [N, K]); xq, sx: the saved
-        quantised input (requantised here into 128-token groups for WGrad)."""
+        """dy bf16 [M, N] -> (dx bf16 [M, K], WGrad problem); xq, sx: the saved
+        quantised input (requantised here into 128-token groups for WGrad).
+        The WGrad problem (dyqT, sdyT, xqT, sxT, dW fp32 [N, K]) is computed
+        later, with the layer's other WGrads, in one grouped launch."""
         M = dy.shape[0]
         dev = dy.device
         dyq, sdy = J.empty_rowgroup_quant(M, self.N, dev)
@@ -86,8 +88,7 @@ class _QLinear:
         xqT, sxT = J.empty_rowgroup_quant(self.K, M, dev)
         J.jetfp8_requant_rowgrp_to_colgrp(xq, sx, xqT, sxT)
         dw = torch.empty(self.N, self.K, dtype=_F32, device=dev)
-        J.jetfp8_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw)
-        return dx, dw
+        return dx, (dyqT, sdyT, xqT, sxT, dw)
 
 
 class DecoderLayerFP8:
@@ -146,30 +147,34 @@ class DecoderLayerFP8:
         return y
 
     def backward(self, dy):
-        """dy bf16 [T, D] -> (dx bf16 [T, D], grads dict: fp32 weight and γ gradients)."""
+        """dy bf16 [T, D] -> (dx bf16 [T, D], grads dict: fp32 weight and γ gradients).
+        The four weight gradients do not feed anything later in the backward:
+        they are computed at the end, in one grouped WGrad launch."""
         sv, w, s, dev = self.saved, self.w, self.s, self.dev
         T, D = dy.shape
-        grads = {}
+        grads, wgrads = {}, {}
         ws = torch.empty(J.jetfp8_rmsnorm_bwd_workspace_bytes(T, D), dtype=_U8, device=dev)
         # MLP block
-        dh, grads["wd"] = self.down.backward(dy, sv["hq"], sv["hs"])
+        dh, wgrads["wd"] = self.down.backward(dy, sv["hq"], sv["hs"])
         dgu = torch.empty(T, 2 * s.intermediate, dtype=_BF, device=dev)
         J.jetfp8_swiglu_bwd(sv["gu"], dh, dgu)
-        dxn2, grads["wgu"] = self.gu.backward(dgu, sv["xq2"], sv["sx2"])
+        dxn2, wgrads["wgu"] = self.gu.backward(dgu, sv["xq2"], sv["sx2"])
         dn2 = torch.empty(T, D, dtype=_BF, device=dev)
         grads["gamma2"] = torch.empty(D, dtype=_F32, device=dev)
         J.jetfp8_rmsnorm_bwd(sv["h1"], w["gamma2"], sv["rstd2"], dxn2, dn2, grads["gamma2"], ws)
         dh1 = dy + dn2
         # attention block
-        dattn, grads["wo"] = self.o.backward(dh1, sv["aq"], sv["sa"])
+        dattn, wgrads["wo"] = self.o.backward(dh1, sv["aq"], sv["sa"])
         q, k, v, a = sv["graph"]
         B, S, hq, d = sv["batch"], sv["seq"], s.heads, s.head_dim
         da = dattn.view(B, S, hq, d).permute(0, 2, 1, 3)
         dq, dk, dv = torch.autograd.grad(a, (q, k, v), da)
         dqkv = torch.cat([dq, dk, dv], 1).permute(0, 2, 1, 3).reshape(T, s.qkv_width).contiguous()
-        dxn1, grads["wqkv"] = self.qkv.backward(dqkv, sv["xq1"], sv["sx1"])
+        dxn1, wgrads["wqkv"] = self.qkv.backward(dqkv, sv["xq1"], sv["sx1"])
         dn1 = torch.empty(T, D, dtype=_BF, device=dev)
         grads["gamma1"] = torch.empty(D, dtype=_F32, device=dev)
         J.jetfp8_rmsnorm_bwd(sv["x"], w["gamma1"], sv["rstd1"], dxn1, dn1, grads["gamma1"], ws)
         dx = dh1 + dn1
+        J.jetfp8_gemm_wgrad_grouped(list(wgrads.values()))
+        grads.update({k: p[4] for k, p in wgrads.items()})
         return dx, grads

@@ -39,6 +39,7 @@ SIGNATURES = {
     "jetfp8_gemm_fprop": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_dgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_wgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
+    "jetfp8_gemm_wgrad_grouped": [_INT, _P, _P, _P, _P, _I64, _P, _P, _P, _INT, _P],
     "jetfp8_gemm_fprop_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_gemm_dgrad_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_rmsnorm_bwd": [_P, _P, _P, _P, _I64, _I64, _P, _P, _P, ctypes.c_size_t, _P],
@@ -184,6 +185,36 @@ def jetfp8_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw, stream=None):
         _ptr(dyqT, _U8, None, "dyqT"), _ptr(sdyT, _F, scale_shape(N, M), "sdyT"),
         _ptr(xqT, _U8, (K, M), "xqT"), _ptr(sxT, _F, scale_shape(K, M), "sxT"), M, N, K,
         _ptr(dw, None, (N, K), "dw"), _out_dt(dw), _stream(stream)), "jetfp8_gemm_wgrad")
+
+
+MAX_GROUP = 4
+
+
+def jetfp8_gemm_wgrad_grouped(problems, stream=None):
+    """WGrads of up to MAX_GROUP linears sharing the token count M in one launch.
+    `problems`: a list of (dyqT, sdyT, xqT, sxT, dw) as for jetfp8_gemm_wgrad;
+    every dw has the same dtype."""
+    n = len(problems)
+    if not 1 <= n <= MAX_GROUP:
+        raise JetFP8Error(f"jetfp8_gemm_wgrad_grouped: {n} problems (1..{MAX_GROUP})")
+    M = problems[0][0].shape[1]
+    cols = [[] for _ in range(5)]
+    Ns, Ks = [], []
+    for dyqT, sdyT, xqT, sxT, dw in problems:
+        N, K = dyqT.shape[0], xqT.shape[0]
+        if dyqT.shape[1] != M or dw.dtype != problems[0][4].dtype:
+            raise JetFP8Error("jetfp8_gemm_wgrad_grouped: problems differ in M or output dtype")
+        cols[0].append(_ptr(dyqT, _U8, (N, M), "dyqT"))
+        cols[1].append(_ptr(sdyT, _F, scale_shape(N, M), "sdyT"))
+        cols[2].append(_ptr(xqT, _U8, (K, M), "xqT"))
+        cols[3].append(_ptr(sxT, _F, scale_shape(K, M), "sxT"))
+        cols[4].append(_ptr(dw, None, (N, K), "dw"))
+        Ns.append(N)
+        Ks.append(K)
+    arrs = [(ctypes.c_void_p * n)(*c) for c in cols]
+    _check(load_library().jetfp8_gemm_wgrad_grouped(
+        n, arrs[0], arrs[1], arrs[2], arrs[3], M, (ctypes.c_int64 * n)(*Ns), (ctypes.c_int64 * n)(*Ks),
+        arrs[4], _out_dt(problems[0][4]), _stream(stream)), "jetfp8_gemm_wgrad_grouped")
 
 
 def jetfp8_gemm_fprop_quant(xq, sx, wq, sw, yq, ys, y=None, stream=None):

@@ -62,13 +62,29 @@ class LinearBuffers:
         _timed(events, "gemm_fprop", lambda: J.jetfp8_gemm_fprop(t["xq"], t["sx"], t["wq"], t["sw"], t["y"], stream))
         return 3
 
-    def backward(self, dy: torch.Tensor, stream=None, events=None) -> int:
+    def backward(self, dy: torch.Tensor, stream=None, events=None, wgrad: bool = True) -> int:
+        """Q4, F2, Q3 and (unless `wgrad` is False, for a later grouped
+        launch by `wgrad_grouped`) F3.  Returns the number of launches."""
         t = self.t
         J.jetfp8_quant_grad_dual(dy, t["dyq"], t["sdy"], t["dyqT"], t["sdyT"], stream)
         _timed(events, "gemm_dgrad", lambda: J.jetfp8_gemm_dgrad(t["dyq"], t["sdy"], t["wqT"], t["sw"], t["dx"], stream))
         J.jetfp8_requant_rowgrp_to_colgrp(t["xq"], t["sx"], t["xqT"], t["sxT"], stream)
+        if not wgrad:
+            return 3
         _timed(events, "gemm_wgrad", lambda: J.jetfp8_gemm_wgrad(t["dyqT"], t["sdyT"], t["xqT"], t["sxT"], t["dw"], stream))
         return 4
+
+
+def wgrad_grouped(bufs, stream=None, events=None) -> int:
+    """F3 of several linears (same token count; their backward already ran
+    with wgrad=False) in grouped launches of up to MAX_GROUP problems each.
+    Returns the number of launches."""
+    n = 0
+    for i in range(0, len(bufs), J.MAX_GROUP):
+        probs = [(b.t["dyqT"], b.t["sdyT"], b.t["xqT"], b.t["sxT"], b.t["dw"]) for b in bufs[i:i + J.MAX_GROUP]]
+        _timed(events, "gemm_wgrad_grouped", lambda: J.jetfp8_gemm_wgrad_grouped(probs, stream))
+        n += 1
+    return n
 
 
 def _timed(events, name, fn):

@@ -160,6 +160,26 @@ jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const ui
                                 const float* sxT, int64_t M, int64_t N, int64_t K, void* dw,
                                 jetfp8_out_dtype out_dtype, cudaStream_t stream);
 
+/* F3 for up to JETFP8_MAX_GROUP linear layers at once (the operation is F3's,
+ * [digest] 核心方法; 方法步骤详情, step 4; grouping them is a scheduling choice
+ * the pages do not discuss): the WGrads of the linears of one layer (they share the token count M and do not depend on one
+ * another) in one persistent launch, so the tiles of one fill the last wave of
+ * another.  Problem i is the jetfp8_gemm_wgrad call
+ *   (dyqT[i], sdyT[i], xqT[i], sxT[i], M, N[i], K[i], dw[i], out_dtype)
+ * and its output equals that call's bit for bit (the same 128-token blocks in
+ * the same order for every element).  dyqT, sdyT, xqT, sxT, N, K and dw are
+ * HOST arrays of `count` entries; the pointers they hold are device pointers
+ * with the layouts and alignment of jetfp8_gemm_wgrad.  Outputs must not
+ * overlap one another or any input.  1 <= count <= JETFP8_MAX_GROUP, else
+ * JETFP8_ERR_INVALID_ARG; shape errors as jetfp8_gemm_wgrad.  The arrays are
+ * read before the call returns; the launch is asynchronous on `stream`. */
+#define JETFP8_MAX_GROUP 4
+jetfp8_status jetfp8_gemm_wgrad_grouped(int count, const uint8_t* const* dyqT,
+                                        const float* const* sdyT, const uint8_t* const* xqT,
+                                        const float* const* sxT, int64_t M, const int64_t* N,
+                                        const int64_t* K, void* const* dw,
+                                        jetfp8_out_dtype out_dtype, cudaStream_t stream);
+
 /* F1 and F2 with the 1×128 quantiser fused into the epilogue ([digest] 方法步骤详情,
  * step 5: the quantisation is fused into the neighbouring kernels to cut its
  * overhead).  The output tile is rounded to bf16 as by jetfp8_gemm_fprop /

@@ -80,3 +80,26 @@ def test_validation_rejects_before_touching_the_device(lib):
     assert lib.jetfp8_gemm_wgrad(P(64), P(64), P(64), P(64), 100, 128, 128, P(64), 0, None) == 2
     # non-positive M
     assert lib.jetfp8_gemm_fprop(P(64), P(64), P(64), P(64), 0, 128, 128, P(64), 0, None) == 1
+
+
+def test_grouped_wgrad_validation(lib):
+    """The grouped WGrad refuses a bad problem count, null arrays and any
+    problem's bad shape or alignment before touching the device."""
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    fn = lib.jetfp8_gemm_wgrad_grouped
+    fn.argtypes = [ctypes.c_int, P, P, P, P, I64, P, P, P, ctypes.c_int, P]
+
+    def call(count, M, Ns, Ks, ptr=64, out_dtype=0, arrays=True):
+        n = max(len(Ns), 1)
+        arr = (P * n)(*([ptr] * n))
+        if not arrays:
+            return fn(count, None, arr, arr, arr, M, (I64 * n)(*Ns), (I64 * n)(*Ks), arr, out_dtype, None)
+        return fn(count, arr, arr, arr, arr, M, (I64 * n)(*Ns), (I64 * n)(*Ks), arr, out_dtype, None)
+
+    assert call(0, 128, [128], [128]) == 1                                 # no problems
+    assert call(5, 128, [128] * 5, [128] * 5) == 1                         # above the group limit
+    assert call(2, 128, [128, 128], [128, 128], arrays=False) == 1         # null array
+    assert call(2, 128, [128, 128], [128, 128], out_dtype=7) == 1          # bad output type
+    assert call(2, 100, [128, 128], [128, 128]) == 2                       # M not a multiple of 128
+    assert call(3, 256, [128, 384, 200], [128, 128, 128]) == 2             # problem 2's N
+    assert call(2, 256, [128, 128], [128, 128], ptr=72) == 3               # misaligned pointers
