@@ -158,36 +158,35 @@ __device__ __forceinline__ void ttile_store(const uint8_t* T, uint8_t* __restric
 // scale takes the division-free exact path.
 struct ColScales {
   float red[16][128];
-  float s[128], ra[128], rb[128];
-  int exact[128];
+  // column c's (S, ra, rb, exact) at g[c + c/8]: one 16-byte read per column,
+  // and the 16 columns a warp reads together fall on distinct banks
+  float4 g[128 + 16];
 };
 
 template <bool BF16_AMAX>
 __device__ __forceinline__ void col_scales(const float (&cm)[8], ColScales& cs, float* sT_out) {
   const uint32_t rowgrp = threadIdx.x >> 4, c0 = 8u * (threadIdx.x & 15u);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) cs.red[rowgrp][c0 + j] = cm[j];
+  *reinterpret_cast<float4*>(&cs.red[rowgrp][c0]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
+  *reinterpret_cast<float4*>(&cs.red[rowgrp][c0 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
   __syncthreads();
   if (threadIdx.x < 128) {
     float m = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) m = fmaxf(m, cs.red[i][threadIdx.x]);
     const GroupScale g = BF16_AMAX ? make_scale_bf16(m) : make_scale(m);
-    cs.s[threadIdx.x] = g.s;
-    cs.ra[threadIdx.x] = g.ra;
-    cs.rb[threadIdx.x] = g.rb;
-    cs.exact[threadIdx.x] = g.exact;
+    cs.g[threadIdx.x + (threadIdx.x >> 3)] = make_float4(g.s, g.ra, g.rb, g.exact ? 1.0f : 0.0f);
     sT_out[threadIdx.x] = g.s;
   }
   __syncthreads();
 }
 
 __device__ __forceinline__ GroupScale load_col_scale(const ColScales& cs, uint32_t c) {
+  const float4 v = cs.g[c + (c >> 3)];
   GroupScale g;
-  g.s = cs.s[c];
-  g.ra = cs.ra[c];
-  g.rb = cs.rb[c];
-  g.exact = cs.exact[c] != 0;
+  g.s = v.x;
+  g.ra = v.y;
+  g.rb = v.z;
+  g.exact = v.w != 0.0f;
   return g;
 }
 
