@@ -38,6 +38,9 @@
 //               column scales once through shared memory in that order.
 //               Promotion is (partial·sB)·sA, a multiply and an FMA per
 //               element, with the TMEM loads of the next two fragments in flight.
+// A launch may carry up to four problems of one configuration (the WGrads of a
+// layer's linears, which share the token count): their tiles form one
+// persistent sequence, each tile computed exactly as in a launch of its own.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records an
 // error word, lets copies and MMAs in flight land, frees TMEM and returns.
 #include <cuda.h>
