@@ -141,6 +141,7 @@ struct DevArgs {
   float* out_s;
   long long ld_out_s;
   unsigned* err;
+  int drop_kb;     // test hook: the producer never loads this block (-1: none)
 };
 
 // Kernel parameters: G problems of one tile configuration run as a single
@@ -556,6 +557,8 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
           // tmB[g] lies G maps after tmA[g]: one live pointer
           const CUtensorMap* const mA = &kp.tmA[g];
           for (int kb = 0; kb < nkb; ++kb, ++it) {
+            // test hook: leave this stage unfilled, so the MMA's bounded wait runs out
+            if (kb == kp.p[g].drop_kb) continue;
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             const uint32_t full = full0 + 8 * s;
             if (!mbar_wait_s(full + EMPTY_OFF, ph ^ 1u, full0 + ABORT_OFF)) {
@@ -569,12 +572,12 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
             tma_load_2d(st + C::A_BYTES, mA + G, full, kb * BK, nt * BN);
           }
         }
-        if (!ok) {
-          // let the copies still in flight land before the CTA's shared memory goes away
-          const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
-          for (uint32_t j = first; j < it; ++j)
-            mbar_wait(&bars->full[j % STAGES], (j / STAGES) & 1u, abort_flag, false);
-        }
+        // every copy issued has landed before the CTA's shared memory goes away
+        // (after an abort the tensor core may not have consumed the last ones;
+        // otherwise these phases are complete and each poll returns at once)
+        const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          mbar_wait(&bars->full[j % STAGES], (j / STAGES) & 1u, abort_flag, false);
       }
     } else if (warp == 1) {
       // ---------------- MMA issuer ----------------
@@ -1038,6 +1041,7 @@ cudaError_t launch_cfg(const GemmArgs* a, int count, int dev, cudaStream_t st) {
     d.out_s = x.out_s;
     d.ld_out_s = x.ld_out_s;
     d.err = err;
+    d.drop_kb = x.drop_kb;
     tiles += d.tiles_m * d.tiles_n;
     kp.tile_end[g] = tiles;
   }

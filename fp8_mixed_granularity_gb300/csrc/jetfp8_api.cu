@@ -1,6 +1,8 @@
 // C ABI of the jetfp8 library: argument validation, per-device set-up and the
 // dispatch of each entry point to its kernel.  Declarations and the contract
 // of every function are in include/jetfp8.h.
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "jetfp8_common.cuh"
@@ -116,6 +118,27 @@ bool device_is_sm103() {
 
 using namespace jetfp8;
 
+namespace {
+
+// JETFP8_LOG set to anything but "" or "0": every entry point prints its name and
+// sizes to stderr when called (before its arguments are checked).
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("JETFP8_LOG");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
+
+void log_call(const char* name, int64_t a, int64_t b = -1, int64_t c = -1) {
+  if (!log_enabled()) return;
+  if (c >= 0) std::fprintf(stderr, "jetfp8: %s %lld %lld %lld\n", name, (long long)a, (long long)b, (long long)c);
+  else if (b >= 0) std::fprintf(stderr, "jetfp8: %s %lld %lld\n", name, (long long)a, (long long)b);
+  else std::fprintf(stderr, "jetfp8: %s %lld\n", name, (long long)a);
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* jetfp8_status_string(jetfp8_status st) {
@@ -146,6 +169,7 @@ jetfp8_status jetfp8_get_last_device_error(cudaStream_t stream) {
 
 jetfp8_status jetfp8_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, uint8_t* q,
                                      float* s, cudaStream_t stream) {
+  log_call("jetfp8_quant_act_1x128", M, K);
   Check c;
   c.bf(x_bf16).ptr(q).ptr(s).positive(M).mult128(K).fits(M, K).device();
   if (c.st != JETFP8_OK) return c.st;
@@ -154,6 +178,7 @@ jetfp8_status jetfp8_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, u
 
 jetfp8_status jetfp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K, uint8_t* q,
                                           float* s, uint8_t* qT, cudaStream_t stream) {
+  log_call("jetfp8_quant_weight_128x128", N, K);
   Check c;
   c.bf(w_bf16).ptr(q).ptr(s).ptr(qT, false).mult128(N).mult128(K).fits(N, K).device();
   if (c.st != JETFP8_OK) return c.st;
@@ -163,6 +188,7 @@ jetfp8_status jetfp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t
 jetfp8_status jetfp8_requant_rowgrp_to_colgrp(const uint8_t* q, const float* s, int64_t M,
                                               int64_t K, uint8_t* qT, float* sT,
                                               cudaStream_t stream) {
+  log_call("jetfp8_requant_rowgrp_to_colgrp", M, K);
   Check c;
   c.ptr(q).ptr(s).ptr(qT).ptr(sT).mult128(M).mult128(K).fits(M, K).device();
   if (c.st != JETFP8_OK) return c.st;
@@ -172,6 +198,7 @@ jetfp8_status jetfp8_requant_rowgrp_to_colgrp(const uint8_t* q, const float* s, 
 jetfp8_status jetfp8_quant_grad_dual(const void* dy_bf16, int64_t M, int64_t N, uint8_t* q_row,
                                      float* s_row, uint8_t* qT_col, float* sT_col,
                                      cudaStream_t stream) {
+  log_call("jetfp8_quant_grad_dual", M, N);
   Check c;
   c.bf(dy_bf16).ptr(q_row).ptr(s_row).ptr(qT_col, false).ptr(sT_col, false).positive(M)
       .mult128(N).fits(M, N).device();
@@ -184,6 +211,7 @@ jetfp8_status jetfp8_quant_grad_dual(const void* dy_bf16, int64_t M, int64_t N, 
 jetfp8_status jetfp8_rmsnorm_quant(const void* x_bf16, const void* gamma_bf16, float eps,
                                    int64_t M, int64_t H, uint8_t* q, float* s, float* rstd,
                                    void* y_bf16, cudaStream_t stream) {
+  log_call("jetfp8_rmsnorm_quant", M, H);
   Check c;
   c.bf(x_bf16).bf(gamma_bf16).ptr(q).ptr(s).ptr(rstd).bf(y_bf16, false).positive(M)
       .mult128(H).fits(M, H).device();
@@ -200,6 +228,7 @@ static jetfp8_status gemm_common(const GemmArgs& g, jetfp8_out_dtype dt, cudaStr
 jetfp8_status jetfp8_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq,
                                 const float* sw, int64_t M, int64_t N, int64_t K, void* y,
                                 jetfp8_out_dtype out_dtype, cudaStream_t stream) {
+  log_call("jetfp8_gemm_fprop", M, N, K);
   Check c;
   c.ptr(xq).ptr(sx).ptr(wq).ptr(sw).bf(y).positive(M).mult128(N).mult128(K).fits(M, K)
       .fits(N, K).fits(M, N).device();
@@ -212,6 +241,7 @@ jetfp8_status jetfp8_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_
 jetfp8_status jetfp8_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT,
                                 const float* sw, int64_t M, int64_t N, int64_t K, void* dx,
                                 jetfp8_out_dtype out_dtype, cudaStream_t stream) {
+  log_call("jetfp8_gemm_dgrad", M, N, K);
   Check c;
   c.ptr(dyq).ptr(sdy).ptr(wqT).ptr(sw).bf(dx).positive(M).mult128(N).mult128(K).fits(M, N)
       .fits(N, K).fits(M, K).device();
@@ -225,6 +255,7 @@ jetfp8_status jetfp8_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint
 jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,
                                 const float* sxT, int64_t M, int64_t N, int64_t K, void* dw,
                                 jetfp8_out_dtype out_dtype, cudaStream_t stream) {
+  log_call("jetfp8_gemm_wgrad", M, N, K);
   Check c;
   c.ptr(dyqT).ptr(sdyT).ptr(xqT).ptr(sxT).bf(dw).mult128(M).mult128(N).mult128(K).fits(M, N)
       .fits(M, K).fits(N, K).device();
@@ -240,6 +271,7 @@ jetfp8_status jetfp8_gemm_wgrad_grouped(int count, const uint8_t* const* dyqT,
                                         const float* const* sxT, int64_t M, const int64_t* N,
                                         const int64_t* K, void* const* dw,
                                         jetfp8_out_dtype out_dtype, cudaStream_t stream) {
+  log_call("jetfp8_gemm_wgrad_grouped", count, M);
   if (count < 1 || count > JETFP8_MAX_GROUP || dyqT == nullptr || sdyT == nullptr ||
       xqT == nullptr || sxT == nullptr || N == nullptr || K == nullptr || dw == nullptr ||
       (out_dtype != JETFP8_OUT_BF16 && out_dtype != JETFP8_OUT_FP32))
@@ -263,6 +295,7 @@ jetfp8_status jetfp8_gemm_wgrad_grouped(int count, const uint8_t* const* dyqT,
 jetfp8_status jetfp8_gemm_fprop_quant(const uint8_t* xq, const float* sx, const uint8_t* wq,
                                       const float* sw, int64_t M, int64_t N, int64_t K,
                                       void* y_bf16, uint8_t* yq, float* ys, cudaStream_t stream) {
+  log_call("jetfp8_gemm_fprop_quant", M, N, K);
   Check c;
   c.ptr(xq).ptr(sx).ptr(wq).ptr(sw).bf(y_bf16, false).ptr(yq).ptr(ys).positive(M).mult128(N)
       .mult128(K).fits(M, K).fits(N, K).fits(M, N);
@@ -280,6 +313,7 @@ jetfp8_status jetfp8_gemm_fprop_quant(const uint8_t* xq, const float* sx, const 
 jetfp8_status jetfp8_gemm_dgrad_quant(const uint8_t* dyq, const float* sdy, const uint8_t* wqT,
                                       const float* sw, int64_t M, int64_t N, int64_t K,
                                       void* dx_bf16, uint8_t* dxq, float* dxs, cudaStream_t stream) {
+  log_call("jetfp8_gemm_dgrad_quant", M, N, K);
   Check c;
   c.ptr(dyq).ptr(sdy).ptr(wqT).ptr(sw).bf(dx_bf16, false).ptr(dxq).ptr(dxs).positive(M).mult128(N)
       .mult128(K).fits(M, N).fits(N, K).fits(M, K);
@@ -294,6 +328,22 @@ jetfp8_status jetfp8_gemm_dgrad_quant(const uint8_t* dyq, const float* sdy, cons
   return from_cuda(launch_gemm(g, stream));
 }
 
+jetfp8_status jetfp8_test_gemm_fprop_drop_block(const uint8_t* xq, const float* sx,
+                                               const uint8_t* wq, const float* sw, int64_t M,
+                                               int64_t N, int64_t K, void* y, int drop_kb,
+                                               cudaStream_t stream) {
+  log_call("jetfp8_test_gemm_fprop_drop_block", M, N, K);
+  Check c;
+  c.ptr(xq).ptr(sx).ptr(wq).ptr(sw).bf(y).positive(M).mult128(N).mult128(K).fits(M, K)
+      .fits(N, K).fits(M, N);
+  if (c.st == JETFP8_OK && (drop_kb < 0 || drop_kb >= K / 128)) c.st = JETFP8_ERR_INVALID_ARG;
+  c.device();
+  if (c.st != JETFP8_OK) return c.st;
+  GemmArgs g{xq, wq, sx, round_up4(M), sw, K / 128, 1, BScale::kBlock, y, false, M, N, K};
+  g.drop_kb = drop_kb;
+  return from_cuda(launch_gemm(g, stream));
+}
+
 size_t jetfp8_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H) {
   if (M <= 0 || H <= 0) return 0;
   return rmsnorm_bwd_workspace_bytes(M, H);
@@ -303,6 +353,7 @@ jetfp8_status jetfp8_rmsnorm_bwd(const void* x_bf16, const void* gamma_bf16, con
                                  const void* dy_bf16, int64_t M, int64_t H, void* dx_bf16,
                                  float* dgamma, void* workspace, size_t workspace_bytes,
                                  cudaStream_t stream) {
+  log_call("jetfp8_rmsnorm_bwd", M, H);
   Check c;
   c.bf(x_bf16).bf(gamma_bf16).ptr(rstd).bf(dy_bf16).bf(dx_bf16).ptr(dgamma).ptr(workspace)
       .positive(M).mult128(H).fits(M, H);
@@ -317,6 +368,7 @@ jetfp8_status jetfp8_rmsnorm_bwd(const void* x_bf16, const void* gamma_bf16, con
 jetfp8_status jetfp8_rmsnorm_bwd_noalloc(const void* x_bf16, const void* gamma_bf16, const float* rstd,
                                          const void* dy_bf16, int64_t M, int64_t H, void* dx_bf16,
                                          float* dgamma, cudaStream_t stream) {
+  log_call("jetfp8_rmsnorm_bwd_noalloc", M, H);
   Check c;
   c.bf(x_bf16).bf(gamma_bf16).ptr(rstd).bf(dy_bf16).bf(dx_bf16).ptr(dgamma).positive(M).mult128(H)
       .fits(M, H);
@@ -334,6 +386,7 @@ jetfp8_status jetfp8_rmsnorm_bwd_noalloc(const void* x_bf16, const void* gamma_b
 
 jetfp8_status jetfp8_swiglu_quant(const void* gu_bf16, int64_t M, int64_t I, uint8_t* q, float* s,
                                   void* h_bf16, cudaStream_t stream) {
+  log_call("jetfp8_swiglu_quant", M, I);
   Check c;
   c.bf(gu_bf16).ptr(q).ptr(s).bf(h_bf16, false).positive(M).mult128(I).fits(M, 2 * I).device();
   if (c.st != JETFP8_OK) return c.st;
@@ -342,6 +395,7 @@ jetfp8_status jetfp8_swiglu_quant(const void* gu_bf16, int64_t M, int64_t I, uin
 
 jetfp8_status jetfp8_swiglu_bwd(const void* gu_bf16, const void* dh_bf16, int64_t M, int64_t I,
                                 void* dgu_bf16, cudaStream_t stream) {
+  log_call("jetfp8_swiglu_bwd", M, I);
   Check c;
   c.bf(gu_bf16).bf(dh_bf16).bf(dgu_bf16).positive(M).mult128(I).fits(M, 2 * I).device();
   if (c.st != JETFP8_OK) return c.st;

@@ -52,6 +52,8 @@ struct GemmArgs {
   uint8_t* out_q = nullptr;
   float* out_s = nullptr;
   int64_t ld_out_s = 0;
+  // test hook: the 128-deep block the TMA producer leaves unloaded (-1: none)
+  int drop_kb = -1;
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);

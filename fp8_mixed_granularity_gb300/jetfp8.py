@@ -40,6 +40,7 @@ SIGNATURES = {
     "jetfp8_gemm_dgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_wgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_wgrad_grouped": [_INT, _P, _P, _P, _P, _I64, _P, _P, _P, _INT, _P],
+    "jetfp8_test_gemm_fprop_drop_block": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_fprop_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_gemm_dgrad_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_rmsnorm_bwd": [_P, _P, _P, _P, _I64, _I64, _P, _P, _P, ctypes.c_size_t, _P],
@@ -185,6 +186,17 @@ def jetfp8_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw, stream=None):
         _ptr(dyqT, _U8, None, "dyqT"), _ptr(sdyT, _F, scale_shape(N, M), "sdyT"),
         _ptr(xqT, _U8, (K, M), "xqT"), _ptr(sxT, _F, scale_shape(K, M), "sxT"), M, N, K,
         _ptr(dw, None, (N, K), "dw"), _out_dt(dw), _stream(stream)), "jetfp8_gemm_wgrad")
+
+
+def jetfp8_test_gemm_fprop_drop_block(xq, sx, wq, sw, y, drop_kb, stream=None):
+    """Failure-path test hook: FProp whose producer never loads block `drop_kb`;
+    the bounded wait runs out and jetfp8_get_last_device_error reports it."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _check(load_library().jetfp8_test_gemm_fprop_drop_block(
+        _ptr(xq, _U8, None, "xq"), _ptr(sx, _F, scale_shape(M, K), "sx"), _ptr(wq, _U8, (N, K), "wq"),
+        _ptr(sw, _F, (N // 128, K // 128), "sw"), M, N, K, _ptr(y, _BF, (M, N), "y"), int(drop_kb),
+        _stream(stream)), "jetfp8_test_gemm_fprop_drop_block")
 
 
 MAX_GROUP = 4

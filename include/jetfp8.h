@@ -198,6 +198,22 @@ jetfp8_status jetfp8_gemm_dgrad_quant(const uint8_t* dyq, const float* sdy, cons
                                       const float* sw, int64_t M, int64_t N, int64_t K,
                                       void* dx_bf16, uint8_t* dxq, float* dxs, cudaStream_t stream);
 
+/* Test hook for the failure path (no counterpart on the pages).  As
+ * jetfp8_gemm_fprop with a bf16 output, except that the kernel's TMA producer
+ * never loads 128-deep block `drop_kb` (0 <= drop_kb < K/128, else
+ * JETFP8_ERR_INVALID_ARG): the tensor core's bounded wait for that block's data
+ * runs out (about 2 s), the kernel records JETFP8_ERR_TIMEOUT in the device error
+ * word, lets the copies and MMAs in flight land, frees its TMEM and returns, and
+ * the CUDA context stays usable.  y is left undefined.  The call itself returns
+ * JETFP8_OK once launched; jetfp8_get_last_device_error reports the timeout. */
+jetfp8_status jetfp8_test_gemm_fprop_drop_block(const uint8_t* xq, const float* sx,
+                                               const uint8_t* wq, const float* sw, int64_t M,
+                                               int64_t N, int64_t K, void* y, int drop_kb,
+                                               cudaStream_t stream);
+
+/* Set the environment variable JETFP8_LOG (to anything but "" or "0") and every
+ * entry point prints its name and sizes to stderr when called. */
+
 /* RMSNorm backward, for the decoder layer around the quantised linears (the
  * pages fuse the forward only; this is the exact derivative of R1's
  * y = (x·r)·γ, r = 1/sqrt(mean(x²) + eps), using the r that R1 saved):

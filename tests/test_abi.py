@@ -103,3 +103,34 @@ def test_grouped_wgrad_validation(lib):
     assert call(2, 100, [128, 128], [128, 128]) == 2                       # M not a multiple of 128
     assert call(3, 256, [128, 384, 200], [128, 128, 128]) == 2             # problem 2's N
     assert call(2, 256, [128, 128], [128, 128], ptr=72) == 3               # misaligned pointers
+
+
+def test_failure_hook_validation(lib):
+    """The failure-path test hook checks its block index before the device."""
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    fn = lib.jetfp8_test_gemm_fprop_drop_block
+    fn.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_int, P]
+    assert fn(P(64), P(64), P(64), P(64), 4, 128, 256, P(64), 2, None) == 1    # K/128 = 2 blocks
+    assert fn(P(64), P(64), P(64), P(64), 4, 128, 256, P(64), -1, None) == 1
+    assert fn(P(64), P(64), P(64), P(64), 4, 128, 200, P(64), 0, None) == 2    # K not a multiple of 128
+
+
+def test_launch_logging(tmp_path):
+    """JETFP8_LOG=1 makes every entry point print its name and sizes to stderr
+    (before its arguments are checked, so no GPU is needed); unset, nothing."""
+    import subprocess
+    import sys
+    code = ("import ctypes\n"
+            "from fp8_mixed_granularity_gb300 import jetfp8 as J\n"
+            "lib = J.load_library()\n"
+            "P = ctypes.c_void_p\n"
+            "assert lib.jetfp8_quant_act_1x128(P(64), 4, 100, P(64), P(64), None) == 2\n")
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    env.pop("JETFP8_LOG", None)
+    quiet = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert quiet.returncode == 0, quiet.stderr
+    assert "jetfp8:" not in quiet.stderr
+    env["JETFP8_LOG"] = "1"
+    loud = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert loud.returncode == 0, loud.stderr
+    assert "jetfp8: jetfp8_quant_act_1x128 4 100" in loud.stderr
