@@ -500,7 +500,7 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
 # ---------------------------------------------------------------------------
 CASES = {"fprop", "dgrad", "wgrad", "quant_act", "rmsnorm_quant", "quant_weight",
          "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd", "fprop_quant", "fprop_then_quant",
-         "rmsnorm_bwd", "decoder_layer", "wgrad_grouped", "wgrad_separate"}
+         "rmsnorm_bwd", "decoder_layer", "wgrad_grouped", "wgrad_separate", "fp8_library_probe"}
 
 
 def run_case(args):
@@ -538,6 +538,15 @@ def run_case(args):
             layer.backward(dy)
         flops = sum(6 * m * n * k for _, m, n, k in shape.linears(T))
         _time_case(args, fwd_bwd, flops, "TFLOP/s", [T, D, D])
+        return
+    if args.case == "fp8_library_probe":
+        # context for the roofline only (not this library's path): the PyTorch /
+        # cuBLASLt dense E4M3 GEMM with per-tensor scales on M x N x K, bf16 out
+        a8 = (torch.randn(M, K, device=dev) * 0.5).to(torch.float8_e4m3fn)
+        b8 = (torch.randn(N, K, device=dev) * 0.5).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev)
+        fn = lambda: torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)  # noqa: E731
+        _time_case(args, fn, 2 * M * N * K, "TFLOP/s", [M, N, K])
         return
     if args.case in ("wgrad_grouped", "wgrad_separate"):
         # the WGrads of a Llama-3.1-8B layer's four linears on M tokens: one
