@@ -439,8 +439,14 @@ k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gam
     double d = (double)ss;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(kFull, d, o);
-    const float r = (float)(1.0 / sqrt(d / (double)H + (double)eps));
-    if (lane == 0) rstd[row] = r;
+    // every lane holds the same d; FP64 division and square root are slow on
+    // this GPU, so one lane forms r and passes it on
+    float r = 0.0f;
+    if (lane == 0) {
+      r = (float)(1.0 / sqrt(d / (double)H + (double)eps));
+      rstd[row] = r;
+    }
+    r = __shfl_sync(kFull, r, 0);
     for (uint32_t g0 = 0; g0 < groups; g0 += 4) {
       const uint32_t grp = g0 + g4;
       const bool valid = grp < groups;
@@ -519,7 +525,10 @@ k_rmsnorm_bwd_dx(const uint16_t* __restrict__ x, const uint16_t* __restrict__ ga
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(kFull, d, o);
     const float r = rstd[row];
-    const float c = (float)((double)r * (double)r * (double)r * d / (double)H);
+    // every lane holds the same d: one lane forms c (FP64 is slow on this GPU)
+    float c = 0.0f;
+    if (lane == 0) c = (float)((double)r * (double)r * (double)r * d / (double)H);
+    c = __shfl_sync(kFull, c, 0);
     for (uint32_t g0 = 0; g0 < groups; g0 += 4) {
       const uint32_t grp = g0 + g4;
       if (grp >= groups) continue;
