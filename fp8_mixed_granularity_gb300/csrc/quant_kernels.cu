@@ -608,8 +608,11 @@ k_swiglu_quant(const uint16_t* __restrict__ gu, uint32_t M, uint32_t I, uint32_t
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         const float2 gg = bf2_to_f2(rg[w]), uu = bf2_to_f2(ru[w]);
-        const float a = __fmul_rn(gg.x / (1.0f + expf(-gg.x)), uu.x);
-        const float b = __fmul_rn(gg.y / (1.0f + expf(-gg.y)), uu.y);
+        // SiLU with the fast exponential and division (a few FP32 ulps, far below
+        // the bf16 rounding of h that follows; the exact IEEE forms made this
+        // kernel issue-bound)
+        const float a = __fmul_rn(__fdividef(gg.x, 1.0f + __expf(-gg.x)), uu.x);
+        const float b = __fmul_rn(__fdividef(gg.y, 1.0f + __expf(-gg.y)), uu.y);
         hb[w] = f2_to_bf2(a, b);
         f[w] = bf2_to_f2(hb[w]);
       }
