@@ -485,7 +485,7 @@ k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gam
 // accumulated like R1's Σx² (16-term FP32 chunk sums per lane, lanes in FP64).
 // ∇γ: deterministic two-stage column sums — FP32 partial sums over 128-row
 // chunks into the caller's workspace [chunks][H], then each column's partials
-// added in chunk order in FP64.
+// added in a fixed order in FP64.
 // ---------------------------------------------------------------------------
 constexpr int kNormBwdRows = 128;   // rows per ∇γ partial sum
 
@@ -570,14 +570,28 @@ k_rmsnorm_bwd_dgamma_partial(const uint16_t* __restrict__ x, const float* __rest
   *reinterpret_cast<float2*>(ws + (size_t)p * H + col) = make_float2(ax, ay);
 }
 
+// 32 columns per CTA, eight threads per column (one per warp): thread j adds
+// the partials of chunks j, j + 8, j + 16, ... in FP64, then the eight sums are
+// added in j order.  The order is fixed, so the result is deterministic; the
+// dependent FP64 chain per thread is chunks/8 long (FP64 is slow on this GPU).
+constexpr uint32_t kReduceWays = kThreads / 32;
 __global__ void __launch_bounds__(kThreads)
 k_rmsnorm_bwd_dgamma_reduce(const float* __restrict__ ws, uint32_t chunks, uint32_t H,
                             float* __restrict__ dgamma) {
-  const uint32_t col = blockIdx.x * kThreads + threadIdx.x;
-  if (col >= H) return;
+  __shared__ double part[kReduceWays][32];
+  const uint32_t cl = threadIdx.x & 31u, j = threadIdx.x >> 5;
+  const uint32_t col = blockIdx.x * 32 + cl;
   double s = 0.0;
-  for (uint32_t p = 0; p < chunks; ++p) s += (double)__ldg(ws + (size_t)p * H + col);
-  dgamma[col] = (float)s;
+  if (col < H)
+    for (uint32_t p = j; p < chunks; p += kReduceWays) s += (double)__ldg(ws + (size_t)p * H + col);
+  part[j][cl] = s;
+  __syncthreads();
+  if (j == 0 && col < H) {
+    double t = 0.0;
+#pragma unroll
+    for (uint32_t i = 0; i < kReduceWays; ++i) t += part[i][cl];
+    dgamma[col] = (float)t;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -729,7 +743,7 @@ cudaError_t launch_rmsnorm_bwd(const void* x, const void* gamma, const float* rs
   const uint32_t chunks = (uint32_t)((M + kNormBwdRows - 1) / kNormBwdRows);
   const dim3 pgrid((unsigned)((H + 511) / 512), chunks);
   k_rmsnorm_bwd_dgamma_partial<<<pgrid, kThreads, 0, st>>>(xb, rstd, db, (uint32_t)M, (uint32_t)H, ws);
-  k_rmsnorm_bwd_dgamma_reduce<<<(unsigned)((H + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+  k_rmsnorm_bwd_dgamma_reduce<<<(unsigned)((H + 31) / 32), kThreads, 0, st>>>(
       ws, chunks, (uint32_t)H, dgamma);
   return cudaGetLastError();
 }

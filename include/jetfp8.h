@@ -219,7 +219,7 @@ jetfp8_status jetfp8_test_gemm_fprop_drop_block(const uint8_t* xq, const float* 
  * y = (x·r)·γ, r = 1/sqrt(mean(x²) + eps), using the r that R1 saved):
  *   ∇x_i = r·(dy_i·γ_i) − x_i·r³·(Σ_j dy_j·γ_j·x_j)/H       (FP32, rounded to bf16)
  *   ∇γ_j = Σ_rows dy_j·x_j·r                                 (deterministic: FP32 sums
- *          over 128-row chunks, chunks added in order in FP64)
+ *          over 128-row chunks, chunks added in a fixed order in FP64)
  *   x bf16 [M, H], gamma bf16 [H], rstd fp32 [M] (R1's output), dy bf16 [M, H]
  *   dx bf16 [M, H], dgamma fp32 [H]
  *   workspace: caller-owned device memory of at least
