@@ -44,6 +44,13 @@ __device__ __forceinline__ void st32(void* p, const uint32_t (&r)[8]) {
                "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
 }
+// 256-bit read-only load under an L2 eviction policy (createpolicy).
+__device__ __forceinline__ void ld32_policy(const void* p, uint32_t (&r)[8], uint64_t pol) {
+  asm volatile("ld.global.nc.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(p), "l"(pol));
+}
 // 16-byte read that stays in L1 for a second pass over the same tile.
 __device__ __forceinline__ uint4 ldg_cached16(const void* p) {
   uint4 v;
@@ -498,6 +505,12 @@ k_rmsnorm_bwd_dx(const uint16_t* __restrict__ x, const uint16_t* __restrict__ ga
   const uint32_t warp = (blockIdx.x * kThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kThreads) >> 5;
   const uint32_t groups = H / 128;
+  // x and ∇y are read twice per row: the first pass asks L2 to keep the lines
+  // for the second, which asks it to drop them (x and ∇y of the rows in flight
+  // otherwise overflow the caches and the second pass goes back to DRAM)
+  uint64_t pol_keep, pol_drop;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_drop));
   for (uint32_t row = warp; row < M; row += nwarps) {
     const uint16_t* xr = x + (size_t)row * H;
     const uint16_t* dr = dy + (size_t)row * H;
@@ -508,8 +521,8 @@ k_rmsnorm_bwd_dx(const uint16_t* __restrict__ x, const uint16_t* __restrict__ ga
         const uint32_t grp = g0 + 4 * u + g4;
         if (grp >= groups) continue;
         uint32_t rx[8], rd[8], rg[8];
-        ld32_cached(xr + grp * 128 + l8 * 16, rx);
-        ld32_cached(dr + grp * 128 + l8 * 16, rd);
+        ld32_policy(xr + grp * 128 + l8 * 16, rx, pol_keep);
+        ld32_policy(dr + grp * 128 + l8 * 16, rd, pol_keep);
         ld32_cached(gamma + grp * 128 + l8 * 16, rg);
         float cs = 0.0f;
 #pragma unroll
@@ -533,8 +546,8 @@ k_rmsnorm_bwd_dx(const uint16_t* __restrict__ x, const uint16_t* __restrict__ ga
       const uint32_t grp = g0 + g4;
       if (grp >= groups) continue;
       uint32_t rx[8], rd[8], rg[8], out[8];
-      ld32_cached(xr + grp * 128 + l8 * 16, rx);
-      ld32_cached(dr + grp * 128 + l8 * 16, rd);
+      ld32_policy(xr + grp * 128 + l8 * 16, rx, pol_drop);
+      ld32_policy(dr + grp * 128 + l8 * 16, rd, pol_drop);
       ld32_cached(gamma + grp * 128 + l8 * 16, rg);
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
