@@ -162,9 +162,9 @@ jetfp8_status jetfp8_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const ui
 
 /* F3 for up to JETFP8_MAX_GROUP linear layers at once (the operation is F3's,
  * [digest] 核心方法; 方法步骤详情, step 4; grouping them is a scheduling choice
- * the pages do not discuss): the WGrads of the linears of one layer (they share the token count M and do not depend on one
- * another) in one persistent launch, so the tiles of one fill the last wave of
- * another.  Problem i is the jetfp8_gemm_wgrad call
+ * the pages do not discuss): the WGrads of the linears of one layer (they share
+ * the token count M and do not depend on one another) in one persistent launch,
+ * so the tiles of one fill the last wave of another.  Problem i is the jetfp8_gemm_wgrad call
  *   (dyqT[i], sdyT[i], xqT[i], sxT[i], M, N[i], K[i], dw[i], out_dtype)
  * and its output equals that call's bit for bit (the same 128-token blocks in
  * the same order for every element).  dyqT, sdyT, xqT, sxT, N, K and dw are
@@ -249,7 +249,9 @@ jetfp8_status jetfp8_rmsnorm_bwd_noalloc(const void* x_bf16, const void* gamma_b
 
 /* X1 — SwiGLU fused with the 1×128 quantiser, for the decoder MLP between the
  * gate/up and down projections (not described by the pages):
- *   h = bf16(silu(g)·u), silu(g) = g/(1+exp(-g)), in FP32; then Q1 on h.
+ *   h = bf16(silu(g)·u), silu(g) = g/(1+exp(-g)), in FP32 with the fast
+ *   exponential and division (errors of a few FP32 ulps, below the bf16
+ *   rounding of h); then Q1 on h, exactly as jetfp8_quant_act_1x128 on h.
  *   gu     bf16 [M, 2I]  (gate in columns [0,I), up in [I,2I))
  *   q      E4M3 [M, I],  s fp32 [I/128][roundup(M,4)]
  *   h_bf16 bf16 [M, I] or NULL
