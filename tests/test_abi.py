@@ -134,3 +134,26 @@ def test_launch_logging(tmp_path):
     loud = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
     assert loud.returncode == 0, loud.stderr
     assert "jetfp8: jetfp8_quant_act_1x128 4 100" in loud.stderr
+
+
+def test_no_cpu_fallback(lib, tmp_path):
+    """The binding refuses host tensors (there is no CPU path), and without the
+    built library the first call raises instead of computing anything."""
+    import subprocess
+    import sys
+    import torch
+    from fp8_mixed_granularity_gb300 import jetfp8 as J
+    x = torch.zeros(4, 128, dtype=torch.bfloat16)
+    q = torch.zeros(4, 128, dtype=torch.uint8)
+    s = torch.zeros(1, 4, dtype=torch.float32)
+    with pytest.raises(J.JetFP8Error, match="CUDA tensor"):
+        J.jetfp8_quant_act_1x128(x, q, s)
+    code = ("from fp8_mixed_granularity_gb300 import jetfp8 as J\n"
+            f"J.LIB_PATH = {str(tmp_path / 'missing.so')!r}\n"
+            "try:\n"
+            "    J.load_library(J.LIB_PATH)\n"
+            "except J.JetFP8Error as e:\n"
+            "    print('raised:', e)\n")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=dict(os.environ, PYTHONPATH=ROOT),
+                         capture_output=True, text=True)
+    assert out.returncode == 0 and "raised:" in out.stdout and "not found" in out.stdout
