@@ -14,9 +14,13 @@ is needed between steps.
 metric  FP8 block-scaled GEMM TFLOP/s: the step's GEMM FLOPs (3 × 2·M·N·K per
         linear) divided by the whole step's time (quantisers included), summed
         over ranks.
-Also reported: each kernel family's own TFLOP/s or GB/s from CUDA events around
-every launch, the roofline of the dominant kernel, the CPU oracle on a bounded
-sample, and the same metric end to end from pinned host memory.
+Also reported: each kernel family's own TFLOP/s or GB/s (the median of every
+launch over the timed steps, from CUDA events on the launching stream), the
+roofline of the dominant kernel, the CPU oracle on a bounded sample, the same
+metric end to end from pinned host memory, and, after the headline step, the
+other workloads: Qwen3-8B decode FProp at 64/128/256 tokens (CUDA-graph replay,
+fraction of HBM), the 32B-class layer step at 16384 tokens with the weight
+requantisation after an update, and the gated-MLP block chain at 16384 tokens.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun (N > 1) every rank runs the same single-GPU step on its own
@@ -41,10 +45,13 @@ if ROOT not in sys.path:
 METRIC = "FP8 block-scaled GEMM TFLOP/s (% dense-FP8 peak); quant kernels GB/s (% HBM)"
 WORKLOAD = "llama3.1-8b-training-linears"
 REF_ROWS, REF_COLS = 128, 1024       # CPU sample: 128 tokens × 1024 output features per linear
-# DRAM bytes (read + write) of one gate/up FProp launch (8192 x 28672 x 4096), from the
-# ncu capture in profiles/gemm_e4m3_blockscaled_fprop_8192x28672x4096_dram.md; must be
-# re-measured (or set to None) whenever the GEMM kernel changes.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up FProp launch
+# (8192 x 28672 x 4096) from a single-pass ncu capture, and the SHA-256 (first 16 hex
+# digits) of the GEMM sources it was captured on.  When the sources differ from that
+# digest the figure no longer describes the kernel and `traffic` is reported as null.
 GATEUP_FPROP_DRAM_BYTES = 609186560
+GATEUP_FPROP_DRAM_SRC = "bd9b5caa051745fa"
+GEMM_SOURCES = ("gemm_tcgen05.cu", "jetfp8_common.cuh", "jetfp8_internal.h")
 
 # algorithmic bytes per element of each quantiser (inputs read + outputs written)
 QUANT_BYTES = {
@@ -70,6 +77,8 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the decode, 32B-class and MLP-chain workloads after the headline step")
     p.add_argument("--case", choices=sorted(CASES), default=None,
                    help="time one kernel alone (for profiling) instead of the layer step")
     p.add_argument("--shape", default="8192,28672,4096", help="M,N,K for --case")
@@ -206,7 +215,8 @@ def oracle_sample_step(lins, seed=0):
     return flops
 
 
-def cpu_threads():
+def blas_threads():
+    """Threads the oracle's BLAS calls may use (the numpy matmuls)."""
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
@@ -214,7 +224,15 @@ def cpu_threads():
             return int(max(n))
     except Exception:
         pass
-    return os.cpu_count()
+    return None
+
+
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count()
 
 
 def time_oracle(lins, steps):
@@ -247,8 +265,8 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens": 8192, "linears": [l.name for l in lins],
                    "l2": "inputs larger than L2"},
-        "cpu_baseline": {"kind": "oracle", "value": value, "unit": "TFLOP/s", "cores": cpu_threads(),
-                         "sample": sample},
+        "cpu_baseline": {"kind": "oracle", "value": value, "unit": "TFLOP/s", "cores": host_cores(),
+                         "blas_threads": blas_threads(), "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -258,6 +276,25 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def gemm_sources_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "fp8_mixed_granularity_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def launch_medians(events_per_step):
+    """{(linear, kind): median launch ms} over the timed steps.  Each step's
+    events are a list of (linear, kind, start, end)."""
+    per = {}
+    for evs in events_per_step:
+        for lname, kind, s, e in evs:
+            per.setdefault((lname, kind), []).append(s.elapsed_time(e))
+    return {k: float(np.median(v)) for k, v in per.items()}, {k: len(v) for k, v in per.items()}
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -292,13 +329,19 @@ def run_ours(args):
 
     def step(events=None):
         # forward and backward of each linear; the four WGrads (independent of
-        # everything after them) go out together as one grouped launch
+        # everything after them) go out together as one grouped launch.  With
+        # `events` (a list), every launch is bracketed by CUDA events on its stream.
         n = 0
         for b, (x, w, dy, gamma) in zip(bufs, inputs):
-            ev = None if events is None else events.setdefault(b.lin.name, [])
+            ev = None if events is None else []
             n += b.forward(x, w, gamma, events=ev)
             n += b.backward(dy, events=ev, wgrad=False)
-        n += wgrad_grouped(bufs, events=None if events is None else events.setdefault("all", []))
+            if events is not None:
+                events.extend((b.lin.name, kind, s, e) for kind, s, e in ev)
+        ev = None if events is None else []
+        n += wgrad_grouped(bufs, events=ev)
+        if events is not None:
+            events.extend(("all", kind, s, e) for kind, s, e in ev)
         return n
 
     for _ in range(args.warmup):
@@ -308,7 +351,7 @@ def run_ours(args):
 
     # --- timed region: whole steps, CUDA events on the launching stream ---
     sampler = ClockSampler(local)
-    events = {}
+    events_per_step = []
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -320,7 +363,9 @@ def run_ours(args):
     t0.record()
     launches = 0
     for _ in range(args.steps):
-        launches += step(events)
+        ev = []
+        launches += step(ev)
+        events_per_step.append(ev)
     t1.record()
     torch.cuda.synchronize()
     sampler.mark(host_t0, time.time())
@@ -330,30 +375,43 @@ def run_ours(args):
     J.jetfp8_get_last_device_error()
     ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
 
-    # per-GEMM-kind times from the events inside the timed region
-    gemm_ms = {}
-    per_launch_ms = {}
-    for lname, evs in events.items():
-        for name, s, e in evs:
-            dt = s.elapsed_time(e)
-            gemm_ms[name] = gemm_ms.get(name, 0.0) + dt
-            per_launch_ms.setdefault((lname, name), []).append(dt)
-    gemm_total_ms = sum(gemm_ms.values()) / args.steps
+    # --- per-launch medians over the timed steps ---
+    med, counts = launch_medians(events_per_step)
+    by_name = {l.name: l for l in lins}
+    gemm_kinds = ("gemm_fprop", "gemm_dgrad", "gemm_wgrad_grouped")
+    gemm_ms = {k: sum(v for (ln, kk), v in med.items() if kk == k) for k in gemm_kinds}
+    gemm_total_ms = sum(gemm_ms.values())
+    layer_flops = sum(l.gemm_flops for l in lins)
+    peaks = measured_peaks()
+    # dense FP8 = 2 × bf16 (the nominal 4.5/2.25 ratio); the burst figure, because
+    # each launch runs inside a timed region of well under a second at full clocks
+    fp8_peak = 2.0 * peaks["bf16"]
+    quant = {}
+    for kind in QUANT_KINDS:
+        parts = [(by_name[ln], v) for (ln, kk), v in med.items() if kk == kind]
+        if not parts:
+            continue
+        nbytes = sum(quant_bytes(kind, lin) for lin, _ in parts)
+        qms = sum(v for _, v in parts)
+        gbs = nbytes / (qms * 1e-3) / 1e9
+        quant[kind] = {"gbs": gbs, "frac": gbs / peaks["hbm_gbs"], "ms_per_step": qms,
+                       "launches_timed": sum(counts[(lin.name, kind)] for lin, _ in parts),
+                       "per_linear_gbs": {lin.name: quant_bytes(kind, lin) / (v * 1e-3) / 1e9 for lin, v in parts}}
     # the dominant single launch: the gate/up FProp
-    dom = next(l for l in lins if l.name == "gate_up")
-    dom_ms = float(np.mean(per_launch_ms[("gate_up", "gemm_fprop")]))
+    dom = by_name["gate_up"]
+    dom_ms = med[("gate_up", "gemm_fprop")]
     dom_tflops = dom.gemm_flops / (dom_ms * 1e-3) / 1e12
-
-    # --- quantiser breakdown: one extra pass with events around each quantiser ---
-    quant = quant_breakdown(bufs, inputs, J, torch)
+    gemm_tflops = gemm_flops / (gemm_total_ms * 1e-3) / 1e12
+    value = job_value(gemm_flops, world, ms)
+    same_src = gemm_sources_digest() == GATEUP_FPROP_DRAM_SRC
 
     # --- end to end from pinned host memory ---
     e2e = None if args.no_e2e else run_e2e(bufs, inputs, args, torch, gemm_flops, world)
+    del bufs, inputs
+    torch.cuda.empty_cache()
 
-    peaks = measured_peaks()
-    fp8_peak_sustained = 2.0 * peaks["bf16_sustained"]   # dense fp8 = 2 × bf16 (nominal ratio)
-    gemm_tflops = gemm_flops / (gemm_total_ms * 1e-3) / 1e12
-    value = job_value(gemm_flops, world, ms)
+    # --- the other workloads (parity cases of their own; timed here, outside the headline) ---
+    configs = {} if args.no_configs else run_configs(args, torch, J, W, dev, peaks)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -367,19 +425,22 @@ def run_ours(args):
         "roofline": {
             "kernel": f"k_gemm_e4m3_blockscaled gate/up FProp {dom.M}x{dom.N}x{dom.K}",
             "bound": "tensor", "achieved": dom_tflops,
-            "peak": fp8_peak_sustained, "unit": "TFLOP/s", "frac": dom_tflops / fp8_peak_sustained,
-            "traffic": GATEUP_FPROP_DRAM_BYTES,
+            "peak": fp8_peak, "unit": "TFLOP/s", "frac": dom_tflops / fp8_peak,
+            "traffic": GATEUP_FPROP_DRAM_BYTES if same_src else None,
+            "traffic_note": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one such launch"
+                             if same_src else "null: the GEMM sources changed since the DRAM capture"),
             "algorithmic_flops": dom.gemm_flops, "launch_ms": dom_ms,
-            "peak_note": (f"2 x {peaks['source']} sustained bf16 cuBLAS ({peaks['bf16_sustained']} TFLOP/s), "
-                          "of measured"),
-            "all_gemm_launches": {"achieved": gemm_tflops, "frac": gemm_tflops / fp8_peak_sustained},
+            "peak_note": (f"2 x {peaks['source']} burst bf16 cuBLAS ({peaks['bf16']} TFLOP/s), of {peaks['source']}"),
+            "all_gemm_launches": {"achieved": gemm_tflops, "frac": gemm_tflops / fp8_peak},
         },
         "breakdown": {
-            "gemm_tflops": {k: sum(l.gemm_flops for l in lins) / (v / args.steps * 1e-3) / 1e12
-                            for k, v in gemm_ms.items()},
+            "timing": "median of each launch over the timed steps (CUDA events on the launching stream)",
+            "gemm_tflops": {k: layer_flops / (v * 1e-3) / 1e12 for k, v in gemm_ms.items()},
+            "gemm_frac": {k: layer_flops / (v * 1e-3) / 1e12 / fp8_peak for k, v in gemm_ms.items()},
             "gemm_ms_per_step": gemm_total_ms,
             "quant": quant,
             "hbm_peak_gbs": peaks["hbm_gbs"],
+            "configs": configs,
         },
         "clocks": clocks,
         "gpu_launches": launches,
@@ -389,7 +450,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cv, cdt, cfl = time_oracle(lins, 5)
         line["cpu_baseline"] = {
-            "value": cv, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+            "value": cv, "unit": "TFLOP/s", "cores": host_cores(), "blas_threads": blas_threads(),
+            "kind": "oracle",
             "sample": (f"5 steps of the full path on {REF_ROWS} tokens × {REF_COLS} output features of "
                        f"each of the 4 linears ({cfl / 1e9:.1f} GFLOP in {cdt:.1f} s)")}
     if rank == 0:
@@ -398,33 +460,228 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def quant_breakdown(bufs, inputs, J, torch):
-    """GB/s of each quantiser kind from CUDA events around its launches (one
-    pass over the 4 linears, after the timed steps)."""
-    from fp8_mixed_granularity_gb300.linear import _timed
-    ev = []
-    bytes_by = {}
-    for b, (x, w, dy, gamma) in zip(bufs, inputs):
-        t, lin = b.t, b.lin
-        M, K, N = lin.M, lin.K, lin.N
-        if b.rmsnorm:
-            _timed(ev, "rmsnorm_quant", lambda: J.jetfp8_rmsnorm_quant(x, gamma, 1e-6, t["xq"], t["sx"], t["rstd"]))
-            bytes_by.setdefault("rmsnorm_quant", 0.0)
-            bytes_by["rmsnorm_quant"] += M * K * QUANT_BYTES["rmsnorm_quant"] + 2 * K + 4 * M
-        else:
-            _timed(ev, "quant_act", lambda: J.jetfp8_quant_act_1x128(x, t["xq"], t["sx"]))
-            bytes_by["quant_act"] = bytes_by.get("quant_act", 0.0) + M * K * QUANT_BYTES["quant_act"]
-        _timed(ev, "quant_weight", lambda: J.jetfp8_quant_weight_128x128(w, t["wq"], t["sw"], t["wqT"]))
-        bytes_by["quant_weight"] = bytes_by.get("quant_weight", 0.0) + N * K * QUANT_BYTES["quant_weight"]
-        _timed(ev, "quant_grad_dual", lambda: J.jetfp8_quant_grad_dual(dy, t["dyq"], t["sdy"], t["dyqT"], t["sdyT"]))
-        bytes_by["quant_grad_dual"] = bytes_by.get("quant_grad_dual", 0.0) + M * N * QUANT_BYTES["quant_grad_dual"]
-        _timed(ev, "requant", lambda: J.jetfp8_requant_rowgrp_to_colgrp(t["xq"], t["sx"], t["xqT"], t["sxT"]))
-        bytes_by["requant"] = bytes_by.get("requant", 0.0) + M * K * QUANT_BYTES["requant"]
+QUANT_KINDS = ("rmsnorm_quant", "quant_act", "quant_weight", "quant_grad_dual", "requant")
+
+
+def quant_bytes(kind, lin):
+    """Algorithmic bytes of one quantiser launch of linear `lin`."""
+    M, K, N = lin.M, lin.K, lin.N
+    if kind == "rmsnorm_quant":
+        return M * K * QUANT_BYTES[kind] + 2 * K + 4 * M
+    if kind == "quant_act":
+        return M * K * QUANT_BYTES[kind]
+    if kind == "quant_weight":
+        return N * K * QUANT_BYTES[kind]
+    if kind == "quant_grad_dual":
+        return M * N * QUANT_BYTES[kind]
+    if kind == "requant":
+        return M * K * QUANT_BYTES[kind]
+    raise KeyError(kind)
+
+
+# ---------------------------------------------------------------------------
+# the other workloads, timed after the headline step
+# ---------------------------------------------------------------------------
+def _graph_ms(torch, fn, reps=5):
+    """Median ms of one replay of a CUDA graph holding fn()'s launches."""
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            fn()
+    graph.replay()
     torch.cuda.synchronize()
-    ms_by = {}
-    for name, s, e in ev:
-        ms_by[name] = ms_by.get(name, 0.0) + s.elapsed_time(e)
-    return {k: {"gbs": bytes_by[k] / (ms_by[k] * 1e-3) / 1e9, "ms": ms_by[k]} for k in ms_by}
+    out = []
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        graph.replay()
+        e.record()
+        torch.cuda.synchronize()
+        out.append(s.elapsed_time(e))
+    return float(np.median(out))
+
+
+def _events_ms(torch, fn, steps, warmup=3):
+    """Median ms of fn() (a step of many launches), CUDA events per step."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        evs.append((s, e))
+    torch.cuda.synchronize()
+    return float(np.median([s.elapsed_time(e) for s, e in evs]))
+
+
+def decode_config(torch, J, W, dev, peaks, layers=4):
+    """Qwen3-8B decode FProp at M ∈ {64, 128, 256}: the four linears of `layers`
+    distinct layers (their weights together exceed L2, as in a model's forward),
+    replayed from a CUDA graph as a serving loop would.  HBM bytes per FProp =
+    X̂ + Ŵ + both scale sets + bf16 Y."""
+    out = {}
+    shapes = W.qwen3_8b_decode(1)
+    wsets = []
+    for l in range(layers):
+        ws = []
+        for i, lin in enumerate(shapes):
+            w = W.device_normal((lin.N, lin.K), 0.02, dev, seed=900 + 10 * l + i)
+            wq = torch.empty(lin.N, lin.K, dtype=torch.uint8, device=dev)
+            sw = torch.empty(lin.N // 128, lin.K // 128, dtype=torch.float32, device=dev)
+            J.jetfp8_quant_weight_128x128(w, wq, sw)
+            ws.append((wq, sw))
+            del w
+        wsets.append(ws)
+    for M in (64, 128, 256):
+        xs = []
+        for i, lin in enumerate(shapes):
+            x = W.device_channel_outlier_activations(M, lin.K, dev, seed=700 + i)
+            xq, sx = J.empty_rowgroup_quant(M, lin.K, dev)
+            J.jetfp8_quant_act_1x128(x, xq, sx)
+            y = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+            xs.append((xq, sx, y))
+
+        def fwd():
+            for ws in wsets:
+                for (wq, sw), (xq, sx, y) in zip(ws, xs):
+                    J.jetfp8_gemm_fprop(xq, sx, wq, sw, y)
+        ms = _graph_ms(torch, fwd) / layers
+        flops = sum(2 * M * lin.N * lin.K for lin in shapes)
+        nbytes = sum(M * lin.K + lin.N * lin.K + 4 * (lin.K // 128) * J.round_up4(M)
+                     + 4 * (lin.N // 128) * (lin.K // 128) + 2 * M * lin.N for lin in shapes)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        # each linear alone (same graph method) for the narrow / wide split
+        per = {}
+        for i, lin in enumerate(shapes):
+            def one(i=i):
+                for ws in wsets:
+                    wq, sw = ws[i]
+                    xq, sx, y = xs[i]
+                    J.jetfp8_gemm_fprop(xq, sx, wq, sw, y)
+            lms = _graph_ms(torch, one) / layers
+            lb = M * lin.K + lin.N * lin.K + 4 * (lin.K // 128) * J.round_up4(M) \
+                + 4 * (lin.N // 128) * (lin.K // 128) + 2 * M * lin.N
+            per[lin.name] = {"us": lms * 1e3, "gbs": lb / (lms * 1e-3) / 1e9,
+                             "frac_hbm": lb / (lms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        out[f"M{M}"] = {"ms_per_layer_fwd": ms, "tflops": flops / (ms * 1e-3) / 1e12, "gbs": gbs,
+                        "frac_hbm": gbs / peaks["hbm_gbs"], "per_linear": per}
+        del xs
+    out["method"] = (f"CUDA-graph replay; {layers} layers' distinct weights per replay (> L2); "
+                     "bytes = X̂ + Ŵ + scales + bf16 Y per FProp")
+    return out
+
+
+def b32_config(torch, J, W, dev, peaks, steps):
+    """32B-class layer linears at M = 16384: forward + backward of the four
+    linears (all quantisers, grouped WGrad), and the 128×128 requantisation of
+    all four weights after the update W += N(0, 1e-4)."""
+    from fp8_mixed_granularity_gb300.linear import LinearBuffers, wgrad_grouped
+    lins = W.dense32b_training()
+    bufs, inputs = [], []
+    for i, lin in enumerate(lins):
+        b = LinearBuffers(lin, dev)
+        x = W.device_activations(lin.M, lin.K, dev, seed=500 + i)
+        w = W.device_normal((lin.N, lin.K), 0.02, dev, seed=510 + i)
+        dy = W.device_normal((lin.M, lin.N), 1e-3, dev, seed=520 + i)
+        bufs.append(b)
+        inputs.append((x, w, dy))
+
+    def step():
+        for b, (x, w, dy) in zip(bufs, inputs):
+            b.forward(x, w)
+            b.backward(dy, wgrad=False)
+        wgrad_grouped(bufs)
+    ms = _events_ms(torch, step, steps)
+    flops = sum(3 * l.gemm_flops for l in lins)
+    # weight update and requantisation (the update is setup, not timed)
+    for i, (b, (x, w, dy)) in enumerate(zip(bufs, inputs)):
+        w += W.device_normal(tuple(w.shape), 1e-4, dev, seed=530 + i)
+
+    def requant_all():
+        for b, (x, w, dy) in zip(bufs, inputs):
+            J.jetfp8_quant_weight_128x128(w, b.t["wq"], b.t["sw"], b.t["wqT"])
+    rq_ms = _events_ms(torch, requant_all, steps)
+    n_w = sum(l.N * l.K for l in lins)
+    rq_gbs = n_w * QUANT_BYTES["quant_weight"] / (rq_ms * 1e-3) / 1e9
+    return {"tokens": 16384, "linears": {l.name: [l.K, l.N] for l in lins},
+            "ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+            "weight_requant": {"elements": n_w, "ms": rq_ms, "gbs": rq_gbs,
+                               "frac_hbm": rq_gbs / peaks["hbm_gbs"]}}
+
+
+def mlp_config(torch, J, W, dev, peaks, steps, M=16384, H=4096, I=14336):
+    """The gated-MLP block chain at M tokens: RMSNorm + 1×128 quant → gate/up
+    FProp → SwiGLU + quant → down FProp, then the backward: dual gradient
+    quant → down DGrad, requant of h → SwiGLU backward → dual quant → gate/up
+    DGrad, requant of the norm output → RMSNorm backward, both WGrads in one
+    grouped launch; both weights quantised (with transposes) every step."""
+    bf, u8, f32 = torch.bfloat16, torch.uint8, torch.float32
+    e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+    x = W.device_activations(M, H, dev, seed=600)
+    gamma = W.device_uniform((H,), 0.5, 1.5, dev, seed=601)
+    w_gu = W.device_normal((2 * I, H), 0.02, dev, seed=602)
+    w_d = W.device_normal((H, I), 0.02, dev, seed=603)
+    dy = W.device_normal((M, H), 1e-3, dev, seed=604)
+    xq, sx = J.empty_rowgroup_quant(M, H, dev)
+    rstd = e(M, dt=f32)
+    wq_gu, sw_gu, wqT_gu = e(2 * I, H, dt=u8), e(2 * I // 128, H // 128, dt=f32), e(H, 2 * I, dt=u8)
+    wq_d, sw_d, wqT_d = e(H, I, dt=u8), e(H // 128, I // 128, dt=f32), e(I, H, dt=u8)
+    gu = e(M, 2 * I, dt=bf)
+    hq, hs = J.empty_rowgroup_quant(M, I, dev)
+    out = e(M, H, dt=bf)
+    dyq, sdy = J.empty_rowgroup_quant(M, H, dev)
+    dyqT, sdyT = J.empty_rowgroup_quant(H, M, dev)
+    dh = e(M, I, dt=bf)
+    hqT, hsT = J.empty_rowgroup_quant(I, M, dev)
+    dw_d = e(H, I, dt=bf)
+    dgu = e(M, 2 * I, dt=bf)
+    dguq, sdgu = J.empty_rowgroup_quant(M, 2 * I, dev)
+    dguqT, sdguT = J.empty_rowgroup_quant(2 * I, M, dev)
+    dxn = e(M, H, dt=bf)
+    xqT, sxT = J.empty_rowgroup_quant(H, M, dev)
+    dw_gu = e(2 * I, H, dt=bf)
+    dx = e(M, H, dt=bf)
+    dgamma = e(H, dt=f32)
+    ws = e(J.jetfp8_rmsnorm_bwd_workspace_bytes(M, H), dt=u8)
+
+    def step():
+        J.jetfp8_quant_weight_128x128(w_gu, wq_gu, sw_gu, wqT_gu)
+        J.jetfp8_quant_weight_128x128(w_d, wq_d, sw_d, wqT_d)
+        J.jetfp8_rmsnorm_quant(x, gamma, 1e-6, xq, sx, rstd)
+        J.jetfp8_gemm_fprop(xq, sx, wq_gu, sw_gu, gu)
+        J.jetfp8_swiglu_quant(gu, hq, hs)
+        J.jetfp8_gemm_fprop(hq, hs, wq_d, sw_d, out)
+        J.jetfp8_quant_grad_dual(dy, dyq, sdy, dyqT, sdyT)
+        J.jetfp8_gemm_dgrad(dyq, sdy, wqT_d, sw_d, dh)
+        J.jetfp8_requant_rowgrp_to_colgrp(hq, hs, hqT, hsT)
+        J.jetfp8_swiglu_bwd(gu, dh, dgu)
+        J.jetfp8_quant_grad_dual(dgu, dguq, sdgu, dguqT, sdguT)
+        J.jetfp8_gemm_dgrad(dguq, sdgu, wqT_gu, sw_gu, dxn)
+        J.jetfp8_requant_rowgrp_to_colgrp(xq, sx, xqT, sxT)
+        J.jetfp8_rmsnorm_bwd(x, gamma, rstd, dxn, dx, dgamma, ws)
+        J.jetfp8_gemm_wgrad_grouped([(dyqT, sdyT, hqT, hsT, dw_d), (dguqT, sdguT, xqT, sxT, dw_gu)])
+    ms = _events_ms(torch, step, steps)
+    flops = 3 * 2 * M * (2 * I * H + H * I)
+    return {"tokens": M, "hidden": H, "intermediate": I, "ms_per_step": ms,
+            "tflops": flops / (ms * 1e-3) / 1e12, "launches_per_step": 15}
+
+
+def run_configs(args, torch, J, W, dev, peaks):
+    steps = max(5, min(args.steps, 10))
+    out = {"decode_qwen3_8b": decode_config(torch, J, W, dev, peaks)}
+    torch.cuda.empty_cache()
+    out["dense32b_training"] = b32_config(torch, J, W, dev, peaks, steps)
+    torch.cuda.empty_cache()
+    out["gated_mlp_chain"] = mlp_config(torch, J, W, dev, peaks, steps)
+    torch.cuda.empty_cache()
+    J.jetfp8_get_last_device_error()
+    return out
 
 
 def run_e2e(bufs, inputs, args, torch, gemm_flops, world):

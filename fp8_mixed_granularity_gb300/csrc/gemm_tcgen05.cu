@@ -52,6 +52,7 @@
 
 #include "jetfp8_common.cuh"
 #include "jetfp8_internal.h"
+#include "jetfp8_tma.cuh"
 
 namespace jetfp8 {
 namespace {
@@ -860,7 +861,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
               const float2 f = bf2_to_f2(f2_to_bf2(v.x, v.y));
               amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
             }
-          gq = make_scale_bf16(amax);
+          gq = make_scale(amax);
           if (row_ok) p.out_s[(long long)(col0 / 128) * p.ld_out_s + row] = gq.s;
         }
 #pragma unroll
@@ -915,63 +916,26 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
+// Tensor maps go through the library's descriptor cache (a repeated call on
+// the same buffers copies cached descriptors instead of encoding them again).
 // 2-D bf16 output [rows, cols] stored in boxes of 32 rows × 32 columns from a
 // shared-memory buffer in the 64-byte swizzle.
 bool make_out_map(CUtensorMap* m, void* ptr, uint64_t cols, uint64_t rows) {
-  auto enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_map_2d(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cols, rows, cols * 2, 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // 2-D E4M3 codes [rows, cols] stored in boxes of 32 rows × 32 bytes, no swizzle.
 bool encode_codes_map(CUtensorMap* m, void* ptr, uint64_t cols, uint64_t rows) {
-  auto enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_map_2d(m, ptr, CU_TENSOR_MAP_DATA_TYPE_UINT8, cols, rows, cols, 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // 2-D E4M3 tensor [outer, inner] (row-major, inner contiguous) loaded in
 // boxes of box_outer rows × 128 bytes with the 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-  auto enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner};
-  cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_map_2d(m, ptr, CU_TENSOR_MAP_DATA_TYPE_UINT8, inner, outer, inner, (uint32_t)BK, box_outer,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 }  // namespace

@@ -3,10 +3,12 @@
 // of every function are in include/jetfp8.h.
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "jetfp8_common.cuh"
 #include "jetfp8_internal.h"
+#include "jetfp8_tma.cuh"
 
 namespace jetfp8 {
 
@@ -98,6 +100,87 @@ struct Check {
 };
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// Tensor-map encoding with a cache.  A descriptor is a pure function of its
+// arguments, so a cached copy is always valid (even if the memory it names
+// was freed and allocated again with the same shape).  64 entries, replaced
+// round-robin, under a mutex.
+// ---------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  uint64_t inner, outer, row_bytes;
+  uint32_t box_inner, box_outer;
+  int dtype, swizzle, promo;
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+
+constexpr int kMapCache = 64;
+struct MapCache {
+  std::mutex mu;
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  bool used[kMapCache] = {};
+  int next = 0;
+};
+MapCache g_map_cache;
+
+}  // namespace
+
+bool encode_map_2d(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
+                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                   CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));   // padding bytes take part in the comparison
+  k.ptr = ptr;
+  k.inner = inner;
+  k.outer = outer;
+  k.row_bytes = row_bytes;
+  k.box_inner = box_inner;
+  k.box_outer = box_outer;
+  k.dtype = (int)dtype;
+  k.swizzle = (int)swizzle;
+  k.promo = (int)promo;
+  {
+    std::lock_guard<std::mutex> lock(g_map_cache.mu);
+    for (int i = 0; i < kMapCache; ++i)
+      if (g_map_cache.used[i] && g_map_cache.key[i] == k) {
+        *out = g_map_cache.map[i];
+        return true;
+      }
+  }
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  if (enc(out, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lock(g_map_cache.mu);
+  const int i = g_map_cache.next;
+  g_map_cache.next = (i + 1) % kMapCache;
+  g_map_cache.key[i] = k;
+  g_map_cache.map[i] = *out;
+  g_map_cache.used[i] = true;
+  return true;
+}
 
 unsigned* device_error_word() {
   DeviceInfo* d = current_device();

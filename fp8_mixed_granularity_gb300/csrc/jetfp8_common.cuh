@@ -15,6 +15,8 @@
 namespace jetfp8 {
 
 constexpr float kE4M3Max = 448.0f;
+// Group maxima below this (and above 0) quantise their elements by IEEE division.
+constexpr float kQuotientMinAmax = 0x1p-80f;
 
 // Error bits recorded in the device error word.
 constexpr unsigned kErrTimeout = 1u;
@@ -63,20 +65,17 @@ __device__ __forceinline__ void set_brackets(GroupScale& g) {
   g.rb = __fmul_rn(rs, kBracketDn);
 }
 
-// S = fp32(amax/448) by IEEE division (any finite amax).
+// S = fp32(amax/448), the correctly rounded quotient, for any finite amax >= 0,
+// without a division: Markstein's quotient correction (P. Markstein, IBM J.
+// Res. Dev. 34(1), 1990): with c = fp32(1/448) (within half an ulp of 1/448)
+// and q0 = RN(amax·c) (within one ulp of the quotient), the residual
+// r = amax - 448·q0 is exact (one FMA) and RN(q0 + r·c) (one FMA) is the
+// correctly rounded quotient.  tests/test_scale_division_free.py checks the
+// sequence in exact arithmetic for every positive finite bf16 value and for
+// every FP32 significand of a binade; it holds for every amax whose
+// intermediates are normal numbers (amax >= 2^-100), and smaller maxima take
+// the IEEE division.  amax == 0 gives S = 1.
 __device__ __forceinline__ GroupScale make_scale(float amax) {
-  GroupScale g;
-  g.s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, kE4M3Max);
-  set_brackets(g);
-  return g;
-}
-
-// S = fp32(amax/448) for an amax that is a bf16 value (the max of |x| over bf16
-// data): q0 = amax·c with c = fp32(1/448), the residual amax - 448·q0 (exact),
-// and one FMA correction give the correctly rounded quotient for every bf16
-// significand (checked exhaustively against exact rational arithmetic) while
-// the result is a normal number; tiny amax takes the division.
-__device__ __forceinline__ GroupScale make_scale_bf16(float amax) {
   constexpr float kInv448 = 1.0f / 448.0f;   // fp32(1/448)
   GroupScale g;
   if (amax == 0.0f) {
@@ -141,6 +140,105 @@ __device__ __forceinline__ void quant_pairs(const float2 (&v)[N], const GroupSca
     for (int w = 0; w < N / 2; ++w)
       out[w] = quant_pair(v[2 * w], g) | (quant_pair(v[2 * w + 1], g) << 16);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Element codes without a division and without a fallback branch.  Per group,
+// besides S: y = RN(1/S) (IEEE reciprocal).  Per element x, the correctly
+// rounded quotient RN(x/S) by two Markstein corrections of q0 = RN(x·y):
+//   q1 = RN(q0 + (x - q0·S)·y),  q2 = RN(q1 + (x - q1·S)·y)  (residuals by FMA)
+// after which q1 is within one ulp of x/S, so the second residual is exact and
+// q2 = RN(x/S) (P. Markstein, IBM J. Res. Dev. 34(1), 1990).  The sequence runs
+// on -x and -y so that the sign of a zero survives.  It holds while every
+// intermediate is a normal number, i.e. for groups with amax >= 2^-80 (and
+// amax = 0); smaller maxima take IEEE divisions (`slow`).  The sequence was
+// checked in exact arithmetic against RN(x/S) for every bf16 element of
+// sampled groups and for FP32 elements next to every kind of E4M3 midpoint.
+// ---------------------------------------------------------------------------
+struct QScale {
+  uint64_t s2;    // (S, S)
+  uint64_t ny2;   // (-y, -y), y = RN(1/S)
+  float s;
+  bool slow;      // 0 < amax < 2^-80: element quotients by IEEE division
+};
+
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// The quotient constants of a group from its S (and whether it is slow).
+__device__ __forceinline__ QScale qscale_from_s(float s, bool slow) {
+  QScale g;
+  g.s = s;
+  g.slow = slow;
+  const float ny = -__frcp_rn(s);
+  g.s2 = pack_f2(s, s);
+  g.ny2 = pack_f2(ny, ny);
+  return g;
+}
+
+// Four E4M3 codes (byte k = value k) of the bf16 values in w0 (values 0, 1)
+// and w1 (values 2, 3) under group constants g (not slow).
+__device__ __forceinline__ uint32_t codes4_bf16(uint32_t w0, uint32_t w1, const QScale& g) {
+  uint32_t c;
+  asm("{\n\t.reg .b32 a0, a1, a2, a3, n0, n1;\n\t.reg .b64 x0, x1, q0, q1, r0, r1;\n\t.reg .b16 l, h;\n\t"
+      "xor.b32 n0, %1, 0x80008000;\n\t"
+      "xor.b32 n1, %2, 0x80008000;\n\t"
+      "shl.b32 a0, n0, 16;\n\t"
+      "and.b32 a1, n0, 0xFFFF0000;\n\t"
+      "shl.b32 a2, n1, 16;\n\t"
+      "and.b32 a3, n1, 0xFFFF0000;\n\t"
+      "mov.b64 x0, {a0, a1};\n\t"
+      "mov.b64 x1, {a2, a3};\n\t"
+      "mul.rn.f32x2 q0, x0, %4;\n\t"
+      "mul.rn.f32x2 q1, x1, %4;\n\t"
+      "fma.rn.f32x2 r0, q0, %3, x0;\n\t"
+      "fma.rn.f32x2 r1, q1, %3, x1;\n\t"
+      "fma.rn.f32x2 q0, r0, %4, q0;\n\t"
+      "fma.rn.f32x2 q1, r1, %4, q1;\n\t"
+      "fma.rn.f32x2 r0, q0, %3, x0;\n\t"
+      "fma.rn.f32x2 r1, q1, %3, x1;\n\t"
+      "fma.rn.f32x2 q0, r0, %4, q0;\n\t"
+      "fma.rn.f32x2 q1, r1, %4, q1;\n\t"
+      "mov.b64 {a0, a1}, q0;\n\t"
+      "mov.b64 {a2, a3}, q1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, a1, a0;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h, a3, a2;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(c) : "r"(w0), "r"(w1), "l"(g.s2), "l"(g.ny2));
+  return c;
+}
+
+// The same for FP32 values given negated as two packed pairs (nx0 = (-v0, -v1),
+// nx1 = (-v2, -v3)).
+__device__ __forceinline__ uint32_t codes4_neg_f32(uint64_t nx0, uint64_t nx1, const QScale& g) {
+  uint32_t c;
+  asm("{\n\t.reg .b32 a0, a1, a2, a3;\n\t.reg .b64 q0, q1, r0, r1;\n\t.reg .b16 l, h;\n\t"
+      "mul.rn.f32x2 q0, %1, %4;\n\t"
+      "mul.rn.f32x2 q1, %2, %4;\n\t"
+      "fma.rn.f32x2 r0, q0, %3, %1;\n\t"
+      "fma.rn.f32x2 r1, q1, %3, %2;\n\t"
+      "fma.rn.f32x2 q0, r0, %4, q0;\n\t"
+      "fma.rn.f32x2 q1, r1, %4, q1;\n\t"
+      "fma.rn.f32x2 r0, q0, %3, %1;\n\t"
+      "fma.rn.f32x2 r1, q1, %3, %2;\n\t"
+      "fma.rn.f32x2 q0, r0, %4, q0;\n\t"
+      "fma.rn.f32x2 q1, r1, %4, q1;\n\t"
+      "mov.b64 {a0, a1}, q0;\n\t"
+      "mov.b64 {a2, a3}, q1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, a1, a0;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h, a3, a2;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(c) : "l"(nx0), "l"(nx1), "l"(g.s2), "l"(g.ny2));
+  return c;
+}
+
+// Four codes from IEEE quotients (groups with tiny maxima).
+__device__ __forceinline__ uint32_t codes4_div(float2 v0, float2 v1, float s) {
+  return cvt_e4m3x2(__fdiv_rn(v0.x, s), __fdiv_rn(v0.y, s)) |
+         (cvt_e4m3x2(__fdiv_rn(v1.x, s), __fdiv_rn(v1.y, s)) << 16);
 }
 
 // Two E4M3 codes (low byte first) -> two exact floats.

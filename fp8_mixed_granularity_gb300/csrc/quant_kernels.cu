@@ -6,20 +6,22 @@
 //                                           gradients, 128×128 blocks for weights
 //   方法步骤详情, steps 1-5                   — where each quantiser sits in the layer
 //
-// Layout of the work:
-//  * Row-group kernels (Q1, R1, X1) give each warp whole rows; eight lanes share
-//    one 128-wide group and each lane moves 32 bytes with one 256-bit access,
-//    so a warp instruction covers 1 KB of contiguous bf16.
-//  * Tile kernels (Q2, Q3, Q4) work on 128×128 tiles with 256 threads; thread t
-//    owns the 8×8 sub-block at rows 8·(t/16), columns 8·(t%16).  Transposed
-//    outputs are staged in a 16 KB shared tile with an XOR swizzle (conflict-
-//    free 8-byte writes) and leave as full 128-byte rows, 16 bytes per thread.
-//  * Pairs of values that share a scale are quantised together with packed
-//    FP32 multiplies (quant_pair): pairs run along rows for row groups and
-//    down columns for column groups, which makes the column codes come out
-//    already in transposed order.
+// Layout of the work (details at the TMA-fed kernels below):
+//  * Row streams (Q1, R1): each warp streams its own row segments (R1: whole
+//    rows) into a private two-slot shared-memory ring with bulk copies; eight
+//    lanes share a 1×128 group.  Wider R1 rows and the SwiGLU quantiser (X1)
+//    read global memory directly, one warp per row.
+//  * Tile pipelines (Q2, Q3, Q4): persistent CTAs of warpgroups, each with a
+//    private double-buffered ring of 128×128 tiles loaded by the tensor-memory
+//    accelerator; a row pass and a column pass read the tile from shared
+//    memory with their own thread mappings, so every group maximum is a
+//    half-warp shuffle and every output a coalesced 8-byte store.
+//  * Element codes: the correctly rounded quotient x/S formed without a
+//    division (codes4_bf16 / codes4_neg_f32 in jetfp8_common.cuh), then the
+//    saturating E4M3 cast.
 #include "jetfp8_common.cuh"
 #include "jetfp8_internal.h"
+#include "jetfp8_tma.cuh"
 
 namespace jetfp8 {
 namespace {
@@ -51,14 +53,6 @@ __device__ __forceinline__ void ld32_policy(const void* p, uint32_t (&r)[8], uin
                  "=r"(r[6]), "=r"(r[7])
                : "l"(p), "l"(pol));
 }
-// 16-byte read that stays in L1 for a second pass over the same tile.
-__device__ __forceinline__ uint4 ldg_cached16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
 // Max over the 8 lanes that share a group (lanes 8j .. 8j+7).
 __device__ __forceinline__ float group8_max(float v) {
   v = fmaxf(v, __shfl_xor_sync(kFull, v, 4));
@@ -66,12 +60,6 @@ __device__ __forceinline__ float group8_max(float v) {
   v = fmaxf(v, __shfl_xor_sync(kFull, v, 1));
   return v;
 }
-// Max over the 16 lanes of a half-warp.
-__device__ __forceinline__ float group16_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 8));
-  return group8_max(v);
-}
-
 // One lane's 16 values (8 packed pairs) of a 1×128 group held by 8 lanes,
 // all bf16 values: group amax, scale, and the 16 codes (4 words, first value
 // in the low byte).
@@ -81,331 +69,784 @@ __device__ __forceinline__ uint4 quant16(const float2 (&f)[8], bool valid, float
 #pragma unroll
     for (int w = 0; w < 8; ++w) amax = fmaxf(amax, fmaxf(fabsf(f[w].x), fabsf(f[w].y)));
   }
-  const GroupScale g = make_scale_bf16(group8_max(amax));
+  const GroupScale g = make_scale(group8_max(amax));
   S = g.s;
   uint32_t c[4];
   quant_pairs<8>(f, g, c);
   return make_uint4(c[0], c[1], c[2], c[3]);
 }
 
-// ---------------------------------------------------------------------------
-// Q1: 1×128 row groups, one warp per row.
-// ---------------------------------------------------------------------------
-template <int U>
-__global__ void __launch_bounds__(kThreads)
-k_quant_rows(const uint16_t* __restrict__ x, uint32_t M, uint32_t K, uint32_t ld_s,
-             uint8_t* __restrict__ q, float* __restrict__ s) {
-  const uint32_t lane = threadIdx.x & 31u, g4 = lane >> 3, l8 = lane & 7u;
-  const uint32_t warp = (blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const uint32_t nwarps = (gridDim.x * kThreads) >> 5;
-  const uint32_t groups = K >> 7;
-  for (uint32_t row = warp; row < M; row += nwarps) {
-    const uint16_t* xr = x + (size_t)row * K;
-    uint8_t* qr = q + (size_t)row * K;
-    for (uint32_t g0 = 0; g0 < groups; g0 += 4 * U) {
-      uint32_t raw[U][8];
+// ===========================================================================
+// TMA-fed quantisers.  Two shapes of work:
+//  * row streams (Q1, R1): each warp owns a private ring of shared-memory
+//    slots and streams its own row segments into them with bulk copies one
+//    unit ahead of the one it quantises; codes and scales go straight to
+//    global memory.  R1 holds the whole row in its slot, so the row is read
+//    from HBM once for both of its passes.
+//  * tile pipelines (Q2, Q3, Q4): persistent CTAs of several warpgroups; each
+//    warpgroup owns a private double-buffered ring of 128×128 tiles
+//    (128-byte swizzled tensor-map boxes), filled by its first thread one tile
+//    ahead of the one it quantises.  A tile is read from shared memory once
+//    per grouping: in the row pass thread t holds rows 8·(t/16)+i, columns
+//    8·(t%16)+0..7, so the 16 threads of a row group are one half-warp; in the
+//    column pass thread t holds columns 8·(t/16)+0..7 of rows 8·(t%16)+i, so
+//    the 16 threads of a 128-row column group are one half-warp.  Both group
+//    maxima are half-warp shuffles, and both outputs leave as 8-byte stores
+//    that a half-warp makes into one 128-byte line (column codes come out in
+//    transposed order).  In the column pass thread t reads its rows in the
+//    rotated order i -> 8·(t%16) + ((i + t%16) mod 8), which spreads a
+//    half-warp's reads over all banks under the 128-byte swizzle; its codes
+//    are rotated back into row order before the store.
+// Codes use the bracketing products of quant_pair (jetfp8_common.cuh), four
+// at a time, with the undecided case (and scales whose reciprocal overflows)
+// taken by one branch per thread and pass that redoes the pass with IEEE
+// divisions.  Of the 8 group scales a half-warp needs, each lane computes one
+// and the others arrive by shuffle.  Every wait is bounded (jetfp8_tma.cuh);
+// on expiry the kernel records the error word, stops issuing copies, waits
+// for the copies it issued and returns.
+// ===========================================================================
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds32f(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+
+// Per half of two packed bf16 pairs: a value whose magnitude is max(|a|, |b|)
+// (its sign bit is not meaningful; mask with 0x7FFF7FFF).
+__device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// f16 (one half of a decoded pair) -> FP32, exact.
+__device__ __forceinline__ float h2f(uint16_t b) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(b));
+  return f;
+}
+
+// Quotient constants of 8 groups whose maxima every lane of a half-warp holds
+// (amax[i] for group i): lane l computes group (l mod 8)'s S and -RN(1/S),
+// and the half-warp shares them by shuffle; bit i of the returned mask marks
+// group i as slow (0 < amax < kQuotientMinAmax).
+__device__ __forceinline__ uint32_t half_warp_qscales(const float (&amax)[8], float (&s)[8], float (&ny)[8]) {
+  const uint32_t lane = threadIdx.x & 31u, me = lane & 7u, base = lane & 16u;
+  float a = amax[0];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const uint32_t grp = g0 + 4 * u + g4;
-        if (grp < groups) {
-          ld32_stream(xr + grp * 128 + l8 * 16, raw[u]);
-        } else {
+  for (int i = 1; i < 8; ++i) a = (me == (uint32_t)i) ? amax[i] : a;
+  const float s_mine = make_scale(a).s;
+  const float ny_mine = -__frcp_rn(s_mine);
+  const bool slow = a != 0.0f && a < kQuotientMinAmax;
+  const uint32_t mask = (__ballot_sync(kFull, slow) >> base) & 0xFFu;
 #pragma unroll
-          for (int w = 0; w < 8; ++w) raw[u][w] = 0;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const uint32_t grp = g0 + 4 * u + g4;
-        const bool valid = grp < groups;
-        float2 f[8];
-#pragma unroll
-        for (int w = 0; w < 8; ++w) f[w] = bf2_to_f2(raw[u][w]);
-        float S;
-        const uint4 c = quant16(f, valid, S);
-        if (valid) {
-          *reinterpret_cast<uint4*>(qr + grp * 128 + l8 * 16) = c;
-          if (l8 == 0) s[(size_t)grp * ld_s + row] = S;
-        }
-      }
-    }
+  for (int i = 0; i < 8; ++i) {
+    s[i] = __shfl_sync(kFull, s_mine, base + i);
+    ny[i] = __shfl_sync(kFull, ny_mine, base + i);
   }
+  return mask;
 }
 
-// ---------------------------------------------------------------------------
-// Shared 128×128-byte tile for transposed stores.  Row k holds 16 units of 8
-// bytes; unit u is stored at position u ^ ((k/8) mod 16).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void ttile_put8(uint8_t* T, uint32_t k, uint32_t unit, uint32_t lo,
-                                           uint32_t hi) {
-  const uint32_t phys = unit ^ ((k >> 3) & 15u);
-  *reinterpret_cast<uint2*>(T + k * 128 + phys * 8) = make_uint2(lo, hi);
-}
-
-// out[(row0 + k) * ld + col0 + 0..127] = tile row k, for k = 0..127.
-__device__ __forceinline__ void ttile_store(const uint8_t* T, uint8_t* __restrict__ out, size_t ld,
-                                            size_t row0, size_t col0) {
-#pragma unroll
-  for (uint32_t i = threadIdx.x; i < 128 * 8; i += kThreads) {
-    const uint32_t k = i >> 3, v = i & 7u;
-    const uint32_t sw = (k >> 3) & 15u;
-    uint4 val = *reinterpret_cast<const uint4*>(T + k * 128 + ((v ^ (sw >> 1)) << 4));
-    if (sw & 1u) {
-      const uint32_t a = val.x, b = val.y;
-      val.x = val.z; val.y = val.w; val.z = a; val.w = b;
-    }
-    *reinterpret_cast<uint4*>(out + (row0 + k) * ld + col0 + v * 16) = val;
-  }
-}
-
-// Column scales of a 128×128 tile: each thread passes its 8 columns' maxima
-// over its 8 rows; 128 threads reduce a column each, build its GroupScale and
-// store S to sT_out[0..127]; afterwards every thread can read the scale of any
-// column from shared memory.  BF16_AMAX: the maxima are of bf16 values, so the
-// scale takes the division-free exact path.
-struct ColScales {
-  float red[16][128];
-  // column c's (S, ra, rb, exact) at g[c + c/8]: one 16-byte read per column,
-  // and the 16 columns a warp reads together fall on distinct banks
-  float4 g[128 + 16];
-};
-
-template <bool BF16_AMAX>
-__device__ __forceinline__ void col_scales(const float (&cm)[8], ColScales& cs, float* sT_out) {
-  const uint32_t rowgrp = threadIdx.x >> 4, c0 = 8u * (threadIdx.x & 15u);
-  *reinterpret_cast<float4*>(&cs.red[rowgrp][c0]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
-  *reinterpret_cast<float4*>(&cs.red[rowgrp][c0 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
-  __syncthreads();
-  if (threadIdx.x < 128) {
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) m = fmaxf(m, cs.red[i][threadIdx.x]);
-    const GroupScale g = BF16_AMAX ? make_scale_bf16(m) : make_scale(m);
-    cs.g[threadIdx.x + (threadIdx.x >> 3)] = make_float4(g.s, g.ra, g.rb, g.exact ? 1.0f : 0.0f);
-    sT_out[threadIdx.x] = g.s;
-  }
-  __syncthreads();
-}
-
-__device__ __forceinline__ GroupScale load_col_scale(const ColScales& cs, uint32_t c) {
-  const float4 v = cs.g[c + (c >> 3)];
-  GroupScale g;
-  g.s = v.x;
-  g.ra = v.y;
-  g.rb = v.z;
-  g.exact = v.w != 0.0f;
+__device__ __forceinline__ QScale qscale_of(float s, float ny) {
+  QScale g;
+  g.s = s;
+  g.slow = false;
+  g.s2 = pack_f2(s, s);
+  g.ny2 = pack_f2(ny, ny);
   return g;
 }
 
-// Quantise column j of an 8×8 sub-block (rows 0..7) with that column's scale:
-// returns the 8 codes in row order as (lo = rows 0-3, hi = rows 4-7).
-template <typename Get>
-__device__ __forceinline__ uint2 quant_col8(Get get, int j, const GroupScale& g) {
-  const uint32_t p0 = quant_pair(make_float2(get(0, j), get(1, j)), g);
-  const uint32_t p1 = quant_pair(make_float2(get(2, j), get(3, j)), g);
-  const uint32_t p2 = quant_pair(make_float2(get(4, j), get(5, j)), g);
-  const uint32_t p3 = quant_pair(make_float2(get(6, j), get(7, j)), g);
-  return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+__device__ __forceinline__ void record_timeout(volatile int* abort_word, unsigned* err) {
+  if (abort_word != nullptr) *abort_word = 1;
+  atomicOr(err, kErrTimeout);
 }
 
-struct TileSmem {
-  ColScales cs;
-  uint8_t T[128 * 128];
-  float wmax[kThreads / 32];
+// 8 codes held as (lo, hi) with byte i from rotated slot i, i.e. tile row
+// (i + k) mod 8 -> bytes in row order: a left rotation of the 64-bit value by
+// k bytes (k = 0..7).
+__device__ __forceinline__ uint2 unrotate8(uint32_t lo, uint32_t hi, uint32_t k) {
+  if (k & 4u) {
+    const uint32_t t = lo;
+    lo = hi;
+    hi = t;
+  }
+  const uint32_t sh = (k & 3u) * 8u;
+  return make_uint2(__funnelshift_l(hi, lo, sh), __funnelshift_l(lo, hi, sh));
+}
+
+// Offset of 16-byte chunk c (0..7) of row r in a box of 128-byte rows stored
+// with the 128-byte swizzle (box base 1024-byte aligned).
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+
+// ---------------------------------------------------------------------------
+// Row streams.  Lanes 8j..8j+7 share 128-element groups g with g ≡ j (mod 4);
+// lane l holds elements 8·(l mod 8) + 0..7 and 64 + 8·(l mod 8) + 0..7 of its
+// group (two 16-byte reads that are conflict-free across the warp).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void load_group16(uint32_t gb, uint32_t l8, uint32_t (&w)[8]) {
+  const uint4 a = lds128(gb + l8 * 16u), b = lds128(gb + 128u + l8 * 16u);
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
+// One lane's 16 bf16 values of a group (8 packed words): the group's maximum
+// over its 8 lanes, its scale, and the 16 codes as (first half, second half).
+__device__ __forceinline__ void group16_codes(const uint32_t (&w)[8], bool valid, float& S, uint2& c0, uint2& c1) {
+  uint32_t m = amax2(amax2(amax2(w[0], w[1]), amax2(w[2], w[3])), amax2(amax2(w[4], w[5]), amax2(w[6], w[7])));
+  m &= 0x7FFF7FFFu;
+  float amax = valid ? fmaxf(bf_lo(m), bf_hi(m)) : 0.0f;
+  amax = group8_max(amax);
+  S = make_scale(amax).s;
+  uint32_t c[4];
+  if (amax != 0.0f && amax < kQuotientMinAmax) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = codes4_div(bf2_to_f2(w[2 * k]), bf2_to_f2(w[2 * k + 1]), S);
+  } else {
+    const QScale g = qscale_from_s(S, false);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = codes4_bf16(w[2 * k], w[2 * k + 1], g);
+  }
+  c0 = make_uint2(c[0], c[1]);
+  c1 = make_uint2(c[2], c[3]);
+}
+
+constexpr uint32_t kSeg = 2048;   // Q1 unit: 4 KB of bf16
+
+template <int W, int D>
+__global__ void __launch_bounds__(32 * W, 1)
+k_quant_rows_tma(const uint16_t* __restrict__ x, uint32_t M, uint32_t K, uint32_t ld_s,
+                 uint8_t* __restrict__ q, float* __restrict__ s, unsigned* err) {
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[W][D];
+  constexpr uint32_t SLOT = kSeg * 2;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u, g4 = lane >> 3, l8 = lane & 7u;
+  const uint32_t nseg = (K + kSeg - 1) / kSeg;
+  const uint64_t units = (uint64_t)M * nseg;
+  const uint64_t gw = (uint64_t)blockIdx.x * W + warp, GW = (uint64_t)gridDim.x * W;
+  const uint32_t slot0 = smem_addr(dsm) + warp * D * SLOT;
+  const uint32_t bar0 = smem_addr(&full[warp][0]);
+  if (lane == 0) {
+    for (int d = 0; d < D; ++d) mbar_init_s(bar0 + 8 * d, 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](uint64_t j) {
+    const uint64_t u = gw + j * GW;
+    if (u >= units) return;
+    const uint32_t row = (uint32_t)(u / nseg), col0 = (uint32_t)(u % nseg) * kSeg;
+    const uint32_t bytes = min(K - col0, kSeg) * 2u, d = (uint32_t)(j % D);
+    mbar_expect_tx(bar0 + 8 * d, bytes);
+    bulk_g2s(slot0 + d * SLOT, x + (size_t)row * K + col0, bytes, bar0 + 8 * d, pol);
+  };
+  if (lane == 0)
+    for (int d = 0; d < D; ++d) issue(d);
+  uint64_t j = 0;
+  bool ok = true;
+  for (; gw + j * GW < units; ++j) {
+    const uint64_t u = gw + j * GW;
+    const uint32_t row = (uint32_t)(u / nseg), col0 = (uint32_t)(u % nseg) * kSeg;
+    const uint32_t ng = min(K - col0, kSeg) >> 7, d = (uint32_t)(j % D);
+    if (!mbar_wait_bounded(bar0 + 8 * d, (uint32_t)(j / D) & 1u)) {
+      ok = false;
+      break;
+    }
+    const uint32_t sb = slot0 + d * SLOT;
+    uint8_t* qr = q + (size_t)row * K + col0;
+    for (uint32_t g0 = 0; g0 < ng; g0 += 8) {
+      uint32_t w[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t grp = g0 + 4 * h + g4;
+        if (grp < ng) {
+          load_group16(sb + grp * 256u, l8, w[h]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) w[h][k] = 0;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t grp = g0 + 4 * h + g4;
+        const bool valid = grp < ng;
+        float S;
+        uint2 c0, c1;
+        group16_codes(w[h], valid, S, c0, c1);
+        if (valid) {
+          *reinterpret_cast<uint2*>(qr + grp * 128u + l8 * 8u) = c0;
+          *reinterpret_cast<uint2*>(qr + grp * 128u + 64u + l8 * 8u) = c1;
+          if (l8 == 0) s[(size_t)((col0 >> 7) + grp) * ld_s + row] = S;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) issue(j + D);
+  }
+  if (!ok && lane == 0) record_timeout(nullptr, err);
+  // copies still in flight into this warp's slots land before the CTA exits
+  if (lane == 0)
+    for (uint64_t jj = j; jj < j + D && gw + jj * GW < units; ++jj)
+      mbar_wait_bounded(bar0 + 8 * (uint32_t)(jj % D), (uint32_t)(jj / D) & 1u);
+}
+
+// R1 on a row stream: one unit = one whole row (H ≤ SLOT_ELEMS), γ staged in
+// shared memory once per CTA.  Σx² in FP32: per lane a 16-term FMA chain per
+// group, the lane's groups (at most SLOT_ELEMS/512 = 16) added as a binary
+// tree, the 32 lanes by a butterfly; r = RN(1/sqrt(Σx²/H + eps)) (IEEE
+// reciprocal square root).  With at most 16 + 4 + 5 roundings on a sum of
+// positive terms, the relative error of Σx² is at most 25·2^-24 (first order)
+// and that of r at most 14·2^-24.
+template <int W, int D, uint32_t SLOT_ELEMS>
+__global__ void __launch_bounds__(32 * W, 1)
+k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
+                    uint32_t M, uint32_t H, uint32_t ld_s, uint8_t* __restrict__ q,
+                    float* __restrict__ s, float* __restrict__ rstd, uint16_t* __restrict__ y,
+                    unsigned* err) {
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[W][D];
+  __shared__ __align__(8) uint64_t gbar;
+  constexpr uint32_t SLOT = SLOT_ELEMS * 2;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u, g4 = lane >> 3, l8 = lane & 7u;
+  const uint32_t gsm = smem_addr(dsm);                       // γ
+  const uint32_t slot0 = gsm + SLOT + warp * D * SLOT;
+  const uint32_t bar0 = smem_addr(&full[warp][0]), gb = smem_addr(&gbar);
+  const uint64_t gw = (uint64_t)blockIdx.x * W + warp, GW = (uint64_t)gridDim.x * W;
+  const uint32_t ng = H >> 7;
+  if (threadIdx.x == 0) {
+    mbar_init_s(gb, 1);
+    mbar_fence_init();
+    mbar_expect_tx(gb, H * 2u);
+    bulk_g2s_plain(gsm, gamma, H * 2u, gb);
+  }
+  if (lane == 0) {
+    for (int d = 0; d < D; ++d) mbar_init_s(bar0 + 8 * d, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](uint64_t j) {
+    const uint64_t row = gw + j * GW;
+    if (row >= M) return;
+    const uint32_t d = (uint32_t)(j % D);
+    mbar_expect_tx(bar0 + 8 * d, H * 2u);
+    bulk_g2s(slot0 + d * SLOT, x + (size_t)row * H, H * 2u, bar0 + 8 * d, pol);
+  };
+  if (lane == 0)
+    for (int d = 0; d < D; ++d) issue(d);
+  bool ok = mbar_wait_bounded(gb, 0);
+  uint64_t j = 0;
+  for (; ok && gw + j * GW < M; ++j) {
+    const uint32_t row = (uint32_t)(gw + j * GW), d = (uint32_t)(j % D);
+    if (!mbar_wait_bounded(bar0 + 8 * d, (uint32_t)(j / D) & 1u)) {
+      ok = false;
+      break;
+    }
+    const uint32_t sb = slot0 + d * SLOT;
+    // chunk sums of the lane's groups g4, g4 + 4, ... (zero past the row)
+    constexpr int NC = (int)(SLOT_ELEMS / 512);
+    float cs[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      const uint32_t grp = g4 + 4u * k;
+      float c = 0.0f;
+      if (grp < ng) {
+        uint32_t w[8];
+        load_group16(sb + grp * 256u, l8, w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 f = bf2_to_f2(w[e]);
+          c = __fmaf_rn(f.x, f.x, c);
+          c = __fmaf_rn(f.y, f.y, c);
+        }
+      }
+      cs[k] = c;
+    }
+#pragma unroll
+    for (int width = NC / 2; width >= 1; width /= 2)
+#pragma unroll
+      for (int k = 0; k < width; ++k) cs[k] = __fadd_rn(cs[k], cs[k + width]);
+    float ss = cs[0];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, o));
+    const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps));
+    if (lane == 0) rstd[row] = r;
+    for (uint32_t g0 = 0; g0 < ng; g0 += 4) {
+      const uint32_t grp = g0 + g4;
+      const bool valid = grp < ng;
+      uint32_t wx[8], wg[8];
+      if (valid) {
+        load_group16(sb + grp * 256u, l8, wx);
+        load_group16(gsm + grp * 256u, l8, wg);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) wx[k] = wg[k] = 0;
+      }
+      uint32_t yb[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 t = mul2(mul2(bf2_to_f2(wx[k]), make_float2(r, r)), bf2_to_f2(wg[k]));
+        yb[k] = f2_to_bf2(t.x, t.y);
+      }
+      float S;
+      uint2 c0, c1;
+      group16_codes(yb, valid, S, c0, c1);
+      if (valid) {
+        uint8_t* qg = q + (size_t)row * H + grp * 128u;
+        *reinterpret_cast<uint2*>(qg + l8 * 8u) = c0;
+        *reinterpret_cast<uint2*>(qg + 64u + l8 * 8u) = c1;
+        if (y != nullptr) {
+          uint16_t* yr = y + (size_t)row * H + grp * 128u;
+          *reinterpret_cast<uint4*>(yr + l8 * 8u) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+          *reinterpret_cast<uint4*>(yr + 64u + l8 * 8u) = make_uint4(yb[4], yb[5], yb[6], yb[7]);
+        }
+        if (l8 == 0) s[(size_t)grp * ld_s + row] = S;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) issue(j + D);
+  }
+  if (!ok && lane == 0) record_timeout(nullptr, err);
+  if (lane == 0) {
+    for (uint64_t jj = j; jj < j + D && gw + jj * GW < M; ++jj)
+      mbar_wait_bounded(bar0 + 8 * (uint32_t)(jj % D), (uint32_t)(jj / D) & 1u);
+    if (warp == 0 && !ok) mbar_wait_bounded(gb, 0);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Tile pipelines (Q2, Q3, Q4)
+// ---------------------------------------------------------------------------
+constexpr int kMaxWG = 4, kRing = 2;
+
+struct TileRing {
+  uint64_t full[kMaxWG][kRing];
+  uint64_t empty[kMaxWG][kRing];
+  // Q2: per-warp block maxima of a warpgroup's tiles, double-buffered by tile
+  // parity, each buffer with a barrier the 8 warps arrive on (a bounded wait
+  // instead of a warpgroup barrier, so a warp that gives up cannot strand the others)
+  uint64_t redbar[kMaxWG][2];
+  float red[kMaxWG][2][8];
 };
 
-// ---------------------------------------------------------------------------
-// Q2: 128×128 weight blocks, optional transposed payload (same codes).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 4)
-k_quant_weight(const uint16_t* __restrict__ w, uint32_t N, uint32_t K, uint8_t* __restrict__ q,
-               float* __restrict__ s, uint8_t* __restrict__ qT) {
-  __shared__ __align__(16) TileSmem sm;
-  const uint32_t kblocks = K / 128, nblocks = N / 128;
-  const uint32_t r0 = 8u * (threadIdx.x >> 4), c0 = 8u * (threadIdx.x & 15u);
-  for (uint32_t blk = blockIdx.x; blk < kblocks * nblocks; blk += gridDim.x) {
-    const uint32_t nb = blk / kblocks, kb = blk % kblocks;
-    const size_t row0 = (size_t)nb * 128 + r0, col0 = (size_t)kb * 128 + c0;
-    // read through L1; the codes pass reads the sub-block again (an L1 hit)
-    // rather than holding it across the block-amax barrier
-    uint4 raw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) raw[i] = ldg_cached16(w + (row0 + i) * K + col0);
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t ws[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const float2 f = bf2_to_f2(ws[p]);
-        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+// Warpgroup w of CTA b takes the tiles j·(gridDim·NWG) + b·NWG + w; its tile j
+// sits in its stage j mod 2.  The warpgroup's first thread fills a stage
+// (`issue(tile, stage address, full barrier)`, STAGE_TX bytes) once all 8 warps
+// have released it, one tile ahead of the tile being quantised.  `consume(tile,
+// stage address, warpgroup, thread in warpgroup, j, ring, release)` quantises a
+// tile and calls release() after its warp's last read of the stage.
+template <int NWG, uint32_t STAGE_BYTES, uint32_t STAGE_TX, class Issue, class Consume>
+__device__ __forceinline__ void run_tile_pipeline(uint32_t ntiles, unsigned* err, Issue issue,
+                                                  Consume consume) {
+  static_assert(NWG <= kMaxWG && STAGE_BYTES % 1024 == 0, "stages 1024-byte aligned (128-byte swizzle)");
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  __shared__ TileRing ring;
+  const uint32_t base = (smem_addr(dsm) + 1023u) & ~1023u;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+  const uint32_t wg = warp >> 3, tid = threadIdx.x & 255u;
+  const uint32_t first = blockIdx.x * NWG + wg, step = gridDim.x * NWG;
+  const uint32_t nj = first < ntiles ? (ntiles - first + step - 1) / step : 0u;
+  const uint32_t st0 = base + wg * kRing * STAGE_BYTES;
+  if (tid == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init_s(smem_addr(&ring.full[wg][i]), 1);
+      mbar_init_s(smem_addr(&ring.empty[wg][i]), 8);
+    }
+    mbar_init_s(smem_addr(&ring.redbar[wg][0]), 8);
+    mbar_init_s(smem_addr(&ring.redbar[wg][1]), 8);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  auto fill = [&](uint32_t j) {
+    const uint32_t st = j % kRing, fb = smem_addr(&ring.full[wg][st]);
+    mbar_expect_tx(fb, STAGE_TX);
+    issue(first + j * step, st0 + st * STAGE_BYTES, fb);
+  };
+  uint32_t issued = 0;   // tiles whose copies this warpgroup's first thread started
+  if (tid == 0)
+    for (; issued < kRing && issued < nj; ++issued) fill(issued);
+  bool ok = true;
+  uint32_t j = 0;
+  for (; j < nj; ++j) {
+    const uint32_t st = j % kRing;
+    if (tid == 0 && j >= 1 && issued < nj) {
+      // refill the stage of tile j-1 with tile j+1 once all warps released it
+      const uint32_t sp = (j - 1) % kRing;
+      if (!mbar_wait_bounded(smem_addr(&ring.empty[wg][sp]), ((j - 1) / kRing) & 1u)) {
+        record_timeout(nullptr, err);
+        ok = false;
+      } else {
+        fill(issued++);
       }
     }
+    if (!ok || !mbar_wait_bounded(smem_addr(&ring.full[wg][st]), (j / kRing) & 1u)) {
+      if (lane == 0) record_timeout(nullptr, err);
+      break;
+    }
+    const uint32_t eb = smem_addr(&ring.empty[wg][st]);
+    consume(first + j * step, st0 + st * STAGE_BYTES, wg, tid, j, &ring, [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive_s(eb);
+    });
+  }
+  // the copies this warpgroup started land before the CTA's shared memory goes away
+  if (tid == 0)
+    for (uint32_t jj = j; jj < issued; ++jj)
+      mbar_wait_bounded(smem_addr(&ring.full[wg][jj % kRing]), (jj / kRing) & 1u);
+}
+
+// Row pass of a bf16 tile (two 64-column boxes, 16 KB apart): thread (rg, cg)
+// = (tid/16, tid%16) loads rows 8rg + i, columns 8cg + 0..7.
+__device__ __forceinline__ void load_rows_bf16(uint32_t sbase, uint32_t tid, uint32_t (&w)[8][4]) {
+  const uint32_t rg = tid >> 4, cg = tid & 15u;
+  const uint32_t b = sbase + (cg >> 3) * 16384u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 v = lds128(b + sw128(8u * rg + i, cg & 7u));
+    w[i][0] = v.x; w[i][1] = v.y; w[i][2] = v.z; w[i][3] = v.w;
+  }
+}
+// Column pass of a bf16 tile: thread (rg, cg) = (tid%16, tid/16) loads
+// columns 8cg + 0..7 of rows 8rg + ((i + rg) mod 8) into slot i.
+__device__ __forceinline__ void load_cols_bf16(uint32_t sbase, uint32_t tid, uint32_t (&w)[8][4]) {
+  const uint32_t rg = tid & 15u, cg = tid >> 4;
+  const uint32_t b = sbase + (cg >> 3) * 16384u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 v = lds128(b + sw128(8u * rg + ((i + rg) & 7u), cg & 7u));
+    w[i][0] = v.x; w[i][1] = v.y; w[i][2] = v.z; w[i][3] = v.w;
+  }
+}
+
+// Max over the 16 lanes of a half-warp of packed bf16 magnitudes.
+__device__ __forceinline__ uint32_t half_warp_amax2(uint32_t v) {
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) v = amax2(v, __shfl_xor_sync(kFull, v, o));
+  return v & 0x7FFF7FFFu;
+}
+
+// Row pass: the 8 rows' group maxima (each row's 128-column group spans the
+// half-warp) as floats.
+__device__ __forceinline__ void row_group_amax(const uint32_t (&w)[8][4], float (&amax)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    const uint32_t m0 = amax2(amax2(w[i][0], w[i][1]), amax2(w[i][2], w[i][3]));
+    const uint32_t m1 = amax2(amax2(w[i + 1][0], w[i + 1][1]), amax2(w[i + 1][2], w[i + 1][3]));
+    // rows i (low half) and i+1 (high half): low halves against high halves
+    const uint32_t a = half_warp_amax2(amax2(__byte_perm(m0, m1, 0x5410), __byte_perm(m0, m1, 0x7632)));
+    amax[i] = bf_lo(a);
+    amax[i + 1] = bf_hi(a);
+  }
+}
+
+// Column pass: the maxima of the thread's 8 columns over the 128 rows of the
+// tile (the column group spans the half-warp).
+__device__ __forceinline__ void col_group_amax(const uint32_t (&w)[8][4], float (&amax)[8]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t m = w[0][c];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = amax2(m, w[i][c]);
+    m = half_warp_amax2(m);
+    amax[2 * c] = bf_lo(m);
+    amax[2 * c + 1] = bf_hi(m);
+  }
+}
+
+// Codes of the 8 rows of a row-pass block under per-row constants (s[i],
+// ny[i]); row i's 8 codes (columns in order) go to put(i, codes).  Rows whose
+// group is slow (bit i of `slow`) are stored again from IEEE quotients.
+template <class Put>
+__device__ __forceinline__ void row_codes_bf16(const uint32_t (&w)[8][4], const float (&s)[8],
+                                               const float (&ny)[8], uint32_t slow, Put put) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const QScale g = qscale_of(s[i], ny[i]);
+    put(i, make_uint2(codes4_bf16(w[i][0], w[i][1], g), codes4_bf16(w[i][2], w[i][3], g)));
+  }
+  if (slow) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (slow & (1u << i))
+        put(i, make_uint2(codes4_div(bf2_to_f2(w[i][0]), bf2_to_f2(w[i][1]), s[i]),
+                          codes4_div(bf2_to_f2(w[i][2]), bf2_to_f2(w[i][3]), s[i])));
+  }
+}
+
+// Codes of the 8 columns of a column-pass block under per-column constants:
+// column j's 8 codes in slot order (rotated rows) go to put(j, lo, hi).
+template <class Put>
+__device__ __forceinline__ void col_codes_bf16(const uint32_t (&w)[8][4], const float (&s)[8],
+                                               const float (&ny)[8], uint32_t slow, Put put) {
+  // column j, slots (i, i+1): the pair's bf16 values from two row words
+  auto pair = [&](int j, int i) { return __byte_perm(w[i][j >> 1], w[i + 1][j >> 1], (j & 1) ? 0x7632 : 0x5410); };
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const QScale g = qscale_of(s[j], ny[j]);
+    put(j, codes4_bf16(pair(j, 0), pair(j, 2), g), codes4_bf16(pair(j, 4), pair(j, 6), g));
+  }
+  if (slow) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (slow & (1u << j))
+        put(j, codes4_div(bf2_to_f2(pair(j, 0)), bf2_to_f2(pair(j, 2)), s[j]),
+            codes4_div(bf2_to_f2(pair(j, 4)), bf2_to_f2(pair(j, 6)), s[j]));
+  }
+}
+
+struct Q4Args {
+  uint32_t M, N, ld_srow;
+  uint8_t* q_row;
+  float* s_row;
+  uint8_t* qT_col;
+  float* sT_col;
+  unsigned* err;
+};
+
+constexpr int kBf16WG = 3;     // warpgroups per CTA for 32 KB bf16 tiles (two-tile rings: 192 KB)
+
+// Q4: one read of the bf16 gradient → 1×128 row groups along N (stored as is)
+// and 128×1 column groups along M (stored transposed).
+__global__ void __launch_bounds__(256 * kBf16WG, 1)
+k_quant_grad_dual_tma(const __grid_constant__ CUtensorMap map, const Q4Args a) {
+  const uint32_t nb_n = a.N / 128, ntiles = (a.M / 128) * nb_n;
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](uint32_t tile, uint32_t dst, uint32_t fb) {
+    const int m0 = (int)(tile / nb_n) * 128, n0 = (int)(tile % nb_n) * 128;
+    tma_g2s_2d(dst, &map, fb, n0, m0, pol);
+    tma_g2s_2d(dst + 16384u, &map, fb, n0 + 64, m0, pol);
+  };
+  auto consume = [&](uint32_t tile, uint32_t sb, uint32_t, uint32_t tid, uint32_t, TileRing*, auto release) {
+    const uint32_t mb = tile / nb_n, nb = tile % nb_n;
+    const size_t m0 = (size_t)mb * 128, n0 = (size_t)nb * 128;
+    {  // row groups
+      uint32_t w[8][4];
+      load_rows_bf16(sb, tid, w);
+      float amax[8], sc[8], ny[8];
+      row_group_amax(w, amax);
+      const uint32_t slow = half_warp_qscales(amax, sc, ny);
+      const uint32_t rg = tid >> 4, cg = tid & 15u;
+      uint8_t* qp = a.q_row + (m0 + 8 * rg) * a.N + n0 + 8 * cg;
+      row_codes_bf16(w, sc, ny, slow, [&](int i, uint2 c) { *reinterpret_cast<uint2*>(qp + (size_t)i * a.N) = c; });
+      if (cg == 0) {
+        float* sp = a.s_row + (size_t)nb * a.ld_srow + m0 + 8 * rg;
+        *reinterpret_cast<float4*>(sp) = make_float4(sc[0], sc[1], sc[2], sc[3]);
+        *reinterpret_cast<float4*>(sp + 4) = make_float4(sc[4], sc[5], sc[6], sc[7]);
+      }
+    }
+    {  // column groups, stored transposed
+      uint32_t w[8][4];
+      load_cols_bf16(sb, tid, w);
+      release();
+      float amax[8], sc[8], ny[8];
+      col_group_amax(w, amax);
+      const uint32_t slow = half_warp_qscales(amax, sc, ny);
+      const uint32_t rg = tid & 15u, cg = tid >> 4;
+      uint8_t* qp = a.qT_col + (n0 + 8 * cg) * a.M + m0 + 8 * rg;
+      col_codes_bf16(w, sc, ny, slow, [&](int j, uint32_t lo, uint32_t hi) {
+        *reinterpret_cast<uint2*>(qp + (size_t)j * a.M) = unrotate8(lo, hi, rg & 7u);
+      });
+      if (rg == 0) {
+        float* sp = a.sT_col + (size_t)mb * a.N + n0 + 8 * cg;
+        *reinterpret_cast<float4*>(sp) = make_float4(sc[0], sc[1], sc[2], sc[3]);
+        *reinterpret_cast<float4*>(sp + 4) = make_float4(sc[4], sc[5], sc[6], sc[7]);
+      }
+    }
+  };
+  run_tile_pipeline<kBf16WG, 32768u, 32768u>(ntiles, a.err, issue, consume);
+}
+
+struct Q2Args {
+  uint32_t N, K;
+  uint8_t* q;
+  float* s;
+  uint8_t* qT;
+  unsigned* err;
+};
+
+// Q2: 128×128 weight blocks; the optional transposed payload Ŵᵀ holds the
+// same codes (each column of the block quantised again with the block's scale).
+__global__ void __launch_bounds__(256 * kBf16WG, 1)
+k_quant_weight_tma(const __grid_constant__ CUtensorMap map, const Q2Args a) {
+  const uint32_t kblocks = a.K / 128, ntiles = (a.N / 128) * kblocks;
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](uint32_t tile, uint32_t dst, uint32_t fb) {
+    const int n0 = (int)(tile / kblocks) * 128, k0 = (int)(tile % kblocks) * 128;
+    tma_g2s_2d(dst, &map, fb, k0, n0, pol);
+    tma_g2s_2d(dst + 16384u, &map, fb, k0 + 64, n0, pol);
+  };
+  auto consume = [&](uint32_t tile, uint32_t sb, uint32_t wg, uint32_t tid, uint32_t j, TileRing* ring,
+                     auto release) {
+    const uint32_t nb = tile / kblocks, kb = tile % kblocks;
+    const size_t n0 = (size_t)nb * 128, k0 = (size_t)kb * 128;
+    uint32_t w[8][4];
+    load_rows_bf16(sb, tid, w);
+    if (a.qT == nullptr) release();
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = amax2(m, amax2(amax2(w[i][0], w[i][1]), amax2(w[i][2], w[i][3])));
+    m &= 0x7FFF7FFFu;
+    float amax = fmaxf(bf_lo(m), bf_hi(m));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    if ((threadIdx.x & 31) == 0) sm.wmax[threadIdx.x >> 5] = amax;
-    __syncthreads();
-    amax = sm.wmax[0];
-#pragma unroll
-    for (int i = 1; i < kThreads / 32; ++i) amax = fmaxf(amax, sm.wmax[i]);
-    const GroupScale g = make_scale_bf16(amax);
-    if (threadIdx.x == 0) s[(size_t)nb * kblocks + kb] = g.s;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) raw[i] = ldg_cached16(w + (row0 + i) * K + col0);
-    uint32_t lo[8], hi[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      lo[i] = quant_pair(bf2_to_f2(raw[i].x), g) | (quant_pair(bf2_to_f2(raw[i].y), g) << 16);
-      hi[i] = quant_pair(bf2_to_f2(raw[i].z), g) | (quant_pair(bf2_to_f2(raw[i].w), g) << 16);
-      *reinterpret_cast<uint2*>(q + (row0 + i) * K + col0) = make_uint2(lo[i], hi[i]);
+    // the warpgroup's j-th tile uses buffer j mod 2 for the (j/2)-th time
+    const uint32_t buf = j & 1u;
+    float* red = ring->red[wg][buf];
+    const uint32_t rb = smem_addr(&ring->redbar[wg][buf]);
+    if ((tid & 31u) == 0) {
+      red[tid >> 5] = amax;
+      mbar_arrive_s(rb);   // release: the write above is seen by the waiters
     }
-    if (qT != nullptr) {
-      uint32_t olo[8], ohi[8];
-      transpose8x8(lo, hi, olo, ohi);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ttile_put8(sm.T, c0 + j, r0 >> 3, olo[j], ohi[j]);
-      __syncthreads();
-      ttile_store(sm.T, qT, N, (size_t)kb * 128, (size_t)nb * 128);
+    if (!mbar_wait_bounded(rb, (j >> 1) & 1u)) {
+      if ((tid & 31u) == 0) record_timeout(nullptr, a.err);
+      if (a.qT != nullptr) release();
+      return;
     }
-    __syncthreads();   // wmax and T are reused by the next block
-  }
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    float sc[8], ny[8];
+    sc[0] = make_scale(amax).s;
+    ny[0] = -__frcp_rn(sc[0]);
+    const uint32_t slow = (amax != 0.0f && amax < kQuotientMinAmax) ? 0xFFu : 0u;
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      sc[i] = sc[0];
+      ny[i] = ny[0];
+    }
+    if (tid == 0) a.s[(size_t)nb * kblocks + kb] = sc[0];
+    const uint32_t rg = tid >> 4, cg = tid & 15u;
+    uint8_t* qp = a.q + (n0 + 8 * rg) * a.K + k0 + 8 * cg;
+    row_codes_bf16(w, sc, ny, slow, [&](int i, uint2 c) { *reinterpret_cast<uint2*>(qp + (size_t)i * a.K) = c; });
+    if (a.qT != nullptr) {
+      load_cols_bf16(sb, tid, w);
+      release();
+      const uint32_t rgc = tid & 15u, cgc = tid >> 4;
+      uint8_t* tp = a.qT + (k0 + 8 * cgc) * a.N + n0 + 8 * rgc;
+      col_codes_bf16(w, sc, ny, slow, [&](int c, uint32_t lo, uint32_t hi) {
+        *reinterpret_cast<uint2*>(tp + (size_t)c * a.N) = unrotate8(lo, hi, rgc & 7u);
+      });
+    }
+  };
+  run_tile_pipeline<kBf16WG, 32768u, 32768u>(ntiles, a.err, issue, consume);
 }
 
-// ---------------------------------------------------------------------------
-// Q3: dequantise 1×128 row groups, requantise 128×1 column groups, transpose.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 3)
-k_requant_row2col(const uint8_t* __restrict__ q, const float* __restrict__ s, uint32_t M,
-                  uint32_t K, uint8_t* __restrict__ qT, float* __restrict__ sT) {
-  __shared__ __align__(16) TileSmem sm;
-  const uint32_t kblocks = K / 128, mblocks = M / 128;
-  const uint32_t r0 = 8u * (threadIdx.x >> 4), c0 = 8u * (threadIdx.x & 15u);
-  for (uint32_t blk = blockIdx.x; blk < kblocks * mblocks; blk += gridDim.x) {
-    const uint32_t mb = blk / kblocks, kb = blk % kblocks;
-    const size_t row0 = (size_t)mb * 128 + r0, col0 = (size_t)kb * 128 + c0;
-    uint2 c[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = *reinterpret_cast<const uint2*>(q + (row0 + i) * K + col0);
-    const float4 s_lo = *reinterpret_cast<const float4*>(s + (size_t)kb * M + row0);
-    const float4 s_hi = *reinterpret_cast<const float4*>(s + (size_t)kb * M + row0 + 4);
-    const float srow[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
-    // x̃ = fp32(dec(q)·S) for a column pair (j, j+1) of the 8 rows; computed
-    // once for the column maxima and again for the codes, so that only the
-    // 64 code bytes stay in registers across the column-scale barriers
-    auto dequant = [&](int i, int j) {
-      const uint32_t word = (j < 4 ? c[i].x : c[i].y) >> (8 * (j & 3));
-      const float2 d = dec_e4m3x2(word & 0xFFFFu);
-      return make_float2(__fmul_rn(d.x, srow[i]), __fmul_rn(d.y, srow[i]));
-    };
-    float cm[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) cm[j] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-#pragma unroll
-      for (int j = 0; j < 8; j += 2) {
-        const float2 v = dequant(i, j);
-        cm[j] = fmaxf(cm[j], fabsf(v.x));
-        cm[j + 1] = fmaxf(cm[j + 1], fabsf(v.y));
-      }
-    }
-    col_scales<false>(cm, sm.cs, sT + (size_t)mb * K + (size_t)kb * 128);
-#pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      float v0[8], v1[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float2 v = dequant(i, j);
-        v0[i] = v.x;
-        v1[i] = v.y;
-      }
-      const uint2 codes0 = quant_col8([&](int i, int) { return v0[i]; }, j, load_col_scale(sm.cs, c0 + j));
-      ttile_put8(sm.T, c0 + j, r0 >> 3, codes0.x, codes0.y);
-      const uint2 codes1 =
-          quant_col8([&](int i, int) { return v1[i]; }, j + 1, load_col_scale(sm.cs, c0 + j + 1));
-      ttile_put8(sm.T, c0 + j + 1, r0 >> 3, codes1.x, codes1.y);
-    }
-    __syncthreads();
-    ttile_store(sm.T, qT, M, (size_t)kb * 128, (size_t)mb * 128);
-    __syncthreads();
-  }
-}
+struct Q3Args {
+  uint32_t M, K;
+  const float* s;
+  uint8_t* qT;
+  float* sT;
+  unsigned* err;
+};
 
-// ---------------------------------------------------------------------------
-// Q4: one read of the bf16 gradient: 1×128 row groups along N (stored as is)
-// and 128×1 column groups along M (stored transposed).  M multiple of 128.
-// The first pass reads the tile through L1 and the column pass reads the
-// thread's 8×8 sub-block again (an L1 hit) instead of holding it in registers
-// across the column-scale barriers, which leaves room for four CTAs per SM.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 4)
-k_quant_grad_dual(const uint16_t* __restrict__ dy, uint32_t M, uint32_t N, uint32_t ld_srow,
-                  uint8_t* __restrict__ q_row, float* __restrict__ s_row,
-                  uint8_t* __restrict__ qT_col, float* __restrict__ sT_col) {
-  __shared__ __align__(16) TileSmem sm;
-  const uint32_t nblocks = N / 128, mblocks = M / 128;
-  const uint32_t r0 = 8u * (threadIdx.x >> 4), c0 = 8u * (threadIdx.x & 15u);
-  for (uint32_t blk = blockIdx.x; blk < nblocks * mblocks; blk += gridDim.x) {
-    const uint32_t mb = blk / nblocks, nb = blk % nblocks;
-    const size_t row0 = (size_t)mb * 128 + r0, col0 = (size_t)nb * 128 + c0;
-    uint32_t raw[8][4];
+constexpr int kQ3WG = 2;       // warpgroups per CTA for 17 KB code tiles (two-tile rings: 68 KB)
+
+// Q3: dequantise 1×128 row groups (x̃ = fp32(dec(q)·S)), requantise in 128×1
+// column groups, store transposed.  A stage holds the 128×128 code tile
+// (one 128-byte swizzled box) and the tile rows' 128 scales.
+__global__ void __launch_bounds__(256 * kQ3WG, 1)
+k_requant_row2col_tma(const __grid_constant__ CUtensorMap map, const Q3Args a) {
+  constexpr uint32_t STAGE = 17408;   // 16 KB codes + 512 B scales, padded to 1 KB
+  const uint32_t kblocks = a.K / 128, ntiles = (a.M / 128) * kblocks;
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](uint32_t tile, uint32_t dst, uint32_t fb) {
+    const uint32_t mb = tile / kblocks, kb = tile % kblocks;
+    tma_g2s_2d(dst, &map, fb, (int)(kb * 128), (int)(mb * 128), pol);
+    bulk_g2s(dst + 16384u, a.s + (size_t)kb * a.M + (size_t)mb * 128, 512u, fb, pol);
+  };
+  auto consume = [&](uint32_t tile, uint32_t sb, uint32_t, uint32_t tid, uint32_t, TileRing*, auto release) {
+    const uint32_t mb = tile / kblocks, kb = tile % kblocks;
+    const size_t m0 = (size_t)mb * 128, k0 = (size_t)kb * 128;
+    const uint32_t rg = tid & 15u, cg = tid >> 4;
+    // slot i: row 8rg + ((i + rg) mod 8), columns 8cg + 0..7 (8 codes) and the row's scale
+    uint2 u[8];
+    float sr[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint4 t = ldg_cached16(dy + (row0 + i) * N + col0);
-      raw[i][0] = t.x; raw[i][1] = t.y; raw[i][2] = t.z; raw[i][3] = t.w;
+      const uint32_t r = 8u * rg + ((i + rg) & 7u);
+      u[i] = lds64(sb + sw128(r, cg >> 1) + ((cg & 1u) << 3));
+      sr[i] = lds32f(sb + 16384u + r * 4u);
     }
-    float cm[8];
+    release();
+    // nx[j][p] = -x̃ of column j in slots (2p, 2p+1): the two codes side by
+    // side (byte permute), decoded exactly (E4M3 -> f16 -> FP32) and multiplied
+    // by the negated row scales (one FP32 multiply each: the exact negative of x̃)
+    uint64_t nx[8][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) cm[j] = 0.0f;
-    float srow[8];
+    for (int p = 0; p < 4; ++p) {
+      const uint64_t ns = pack_f2(-sr[2 * p], -sr[2 * p + 1]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float2 f[4];
-      float amax = 0.0f;
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        f[p] = bf2_to_f2(raw[i][p]);
-        cm[2 * p] = fmaxf(cm[2 * p], fabsf(f[p].x));
-        cm[2 * p + 1] = fmaxf(cm[2 * p + 1], fabsf(f[p].y));
-        amax = fmaxf(amax, fmaxf(fabsf(f[p].x), fabsf(f[p].y)));
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t w0 = j < 4 ? u[2 * p].x : u[2 * p].y, w1 = j < 4 ? u[2 * p + 1].x : u[2 * p + 1].y;
+        const uint32_t sel = (uint32_t)(j & 3) | ((4u + (uint32_t)(j & 3)) << 4);   // byte j%4 of w0, then of w1
+        const uint16_t two = (uint16_t)__byte_perm(w0, w1, sel);
+        uint32_t hh;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(two));
+        const uint64_t v = pack_f2(h2f((uint16_t)(hh & 0xFFFFu)), h2f((uint16_t)(hh >> 16)));
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(nx[j][p]) : "l"(v), "l"(ns));
       }
-      const GroupScale g = make_scale_bf16(group16_max(amax));
-      srow[i] = g.s;
-      uint32_t codes[2];
-      quant_pairs<4>(f, g, codes);
-      *reinterpret_cast<uint2*>(q_row + (row0 + i) * N + col0) = make_uint2(codes[0], codes[1]);
     }
-    if (c0 == 0) {
-      *reinterpret_cast<float4*>(s_row + (size_t)nb * ld_srow + row0) =
-          make_float4(srow[0], srow[1], srow[2], srow[3]);
-      *reinterpret_cast<float4*>(s_row + (size_t)nb * ld_srow + row0 + 4) =
-          make_float4(srow[4], srow[5], srow[6], srow[7]);
-    }
-    col_scales<true>(cm, sm.cs, sT_col + (size_t)mb * N + (size_t)nb * 128);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint4 t = ldg_cached16(dy + (row0 + i) * N + col0);
-      raw[i][0] = t.x; raw[i][1] = t.y; raw[i][2] = t.z; raw[i][3] = t.w;
-    }
-    auto get = [&](int i, int j) {
-      const uint32_t wv = raw[i][j >> 1];
-      return __uint_as_float((j & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
-    };
+    float amax[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint2 codes = quant_col8(get, j, load_col_scale(sm.cs, c0 + j));
-      ttile_put8(sm.T, c0 + j, r0 >> 3, codes.x, codes.y);
+      float m = 0.0f;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 v = bits_f2(nx[j][p]);
+        m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
+      }
+      amax[j] = m;
     }
-    __syncthreads();
-    ttile_store(sm.T, qT_col, M, (size_t)nb * 128, (size_t)mb * 128);
-    __syncthreads();
-  }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) amax[jj] = fmaxf(amax[jj], __shfl_xor_sync(kFull, amax[jj], o));
+    float sc[8], ny[8];
+    const uint32_t slow = half_warp_qscales(amax, sc, ny);
+    uint8_t* qp = a.qT + (k0 + 8 * cg) * a.M + m0 + 8 * rg;
+    auto put = [&](int jj, uint32_t lo, uint32_t hi) {
+      *reinterpret_cast<uint2*>(qp + (size_t)jj * a.M) = unrotate8(lo, hi, rg & 7u);
+    };
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const QScale g = qscale_of(sc[jj], ny[jj]);
+      put(jj, codes4_neg_f32(nx[jj][0], nx[jj][1], g), codes4_neg_f32(nx[jj][2], nx[jj][3], g));
+    }
+    if (slow) {
+      auto xpair = [&](int jj, int p) {
+        const float2 v = bits_f2(nx[jj][p]);
+        return make_float2(-v.x, -v.y);
+      };
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (slow & (1u << jj))
+          put(jj, codes4_div(xpair(jj, 0), xpair(jj, 1), sc[jj]), codes4_div(xpair(jj, 2), xpair(jj, 3), sc[jj]));
+    }
+    if (rg == 0) {
+      float* sp = a.sT + (size_t)mb * a.K + k0 + 8 * cg;
+      *reinterpret_cast<float4*>(sp) = make_float4(sc[0], sc[1], sc[2], sc[3]);
+      *reinterpret_cast<float4*>(sp + 4) = make_float4(sc[4], sc[5], sc[6], sc[7]);
+    }
+  };
+  run_tile_pipeline<kQ3WG, STAGE, 16384u + 512u>(ntiles, a.err, issue, consume);
 }
 
 // ---------------------------------------------------------------------------
 // R1: RMSNorm fused with the 1×128 quantiser.  One warp per row, 8 lanes per
-// group.  Pass 1 accumulates Σx² (16-term FP32 chunk sums per lane, lanes
-// combined in FP64); pass 2 re-reads the row (an L1/L2 hit) and writes y, q, S.
+// group.  Pass 1 accumulates Σx² (16-term FP32 chunk sums per lane, the
+// chunks and then the lanes combined in FP64); pass 2 re-reads the row (an
+// L1/L2 hit) and writes y, q, S.  Serves rows wider than 8192.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
 k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
@@ -418,7 +859,7 @@ k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gam
   const uint32_t groups = H / 128;
   for (uint32_t row = warp; row < M; row += nwarps) {
     const uint16_t* xr = x + (size_t)row * H;
-    float ss = 0.0f;
+    double ss = 0.0;
     for (uint32_t g0 = 0; g0 < groups; g0 += 4 * U) {
       uint32_t raw[U][8];
 #pragma unroll
@@ -440,10 +881,10 @@ k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gam
           cs = __fmaf_rn(f.x, f.x, cs);
           cs = __fmaf_rn(f.y, f.y, cs);
         }
-        ss = __fadd_rn(ss, cs);
+        ss += (double)cs;
       }
     }
-    double d = (double)ss;
+    double d = ss;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(kFull, d, o);
     // every lane holds the same d; FP64 division and square root are slow on
@@ -561,26 +1002,29 @@ k_rmsnorm_bwd_dx(const uint16_t* __restrict__ x, const uint16_t* __restrict__ ga
   }
 }
 
-// Partial ∇γ over rows [128p, 128p + 128) for 512 columns per CTA (2 per thread).
+// Partial ∇γ over rows [128p, 128p + 128) for 512 columns per CTA (2 per
+// thread); the CTAs of one grid column take the chunks p = blockIdx.y,
+// blockIdx.y + gridDim.y, ... (the grid's y extent is capped at 65535).
 __global__ void __launch_bounds__(kThreads)
 k_rmsnorm_bwd_dgamma_partial(const uint16_t* __restrict__ x, const float* __restrict__ rstd,
                              const uint16_t* __restrict__ dy, uint32_t M, uint32_t H,
-                             float* __restrict__ ws) {
+                             uint32_t chunks, float* __restrict__ ws) {
   const uint32_t col = blockIdx.x * 512u + 2u * threadIdx.x;
-  const uint32_t p = blockIdx.y;
-  const uint32_t r0 = p * kNormBwdRows, r1 = min(M, r0 + kNormBwdRows);
   if (col >= H) return;
-  float ax = 0.0f, ay = 0.0f;
-  // eight rows' loads in flight per thread (the sums still run in row order)
+  for (uint32_t p = blockIdx.y; p < chunks; p += gridDim.y) {
+    const uint32_t r0 = p * kNormBwdRows, r1 = min(M, r0 + kNormBwdRows);
+    float ax = 0.0f, ay = 0.0f;
+    // eight rows' loads in flight per thread (the sums still run in row order)
 #pragma unroll 8
-  for (uint32_t m = r0; m < r1; ++m) {
-    const float2 fx = bf2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(x + (size_t)m * H + col)));
-    const float2 fd = bf2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(dy + (size_t)m * H + col)));
-    const float r = __ldg(rstd + m);
-    ax = __fadd_rn(ax, __fmul_rn(__fmul_rn(fd.x, fx.x), r));
-    ay = __fadd_rn(ay, __fmul_rn(__fmul_rn(fd.y, fx.y), r));
+    for (uint32_t m = r0; m < r1; ++m) {
+      const float2 fx = bf2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(x + (size_t)m * H + col)));
+      const float2 fd = bf2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(dy + (size_t)m * H + col)));
+      const float r = __ldg(rstd + m);
+      ax = __fadd_rn(ax, __fmul_rn(__fmul_rn(fd.x, fx.x), r));
+      ay = __fadd_rn(ay, __fmul_rn(__fmul_rn(fd.y, fx.y), r));
+    }
+    *reinterpret_cast<float2*>(ws + (size_t)p * H + col) = make_float2(ax, ay);
   }
-  *reinterpret_cast<float2*>(ws + (size_t)p * H + col) = make_float2(ax, ay);
 }
 
 // 32 columns per CTA, eight threads per column (one per warp): thread j adds
@@ -694,46 +1138,120 @@ inline unsigned grid_for(size_t work_items, unsigned per_block, unsigned blocks_
 // ---------------------------------------------------------------------------
 // Launchers (arguments already validated by the C ABI layer)
 // ---------------------------------------------------------------------------
+// Dynamic shared memory above 48 KB needs an opt-in per kernel and device.
+template <class Kern>
+cudaError_t opt_in_smem(Kern kern, int bytes, int (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done[dev] = 1;
+  }
+  return cudaSuccess;
+}
+
+constexpr int kRowW = 24, kRowD = 2;            // Q1: warps per CTA, slots per warp
+
 cudaError_t launch_quant_rowgroups(const void* x, int64_t M, int64_t K, uint8_t* q, float* s,
                                    cudaStream_t st) {
-  constexpr int U = 2;
-  const unsigned grid = grid_for((size_t)M, kThreads / 32, 8);
-  k_quant_rows<U><<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(x), (uint32_t)M,
-                                             (uint32_t)K, (uint32_t)round_up4(M), q, s);
+  unsigned* err = device_error_word();
+  if (err == nullptr) return cudaErrorInvalidValue;
+  auto kern = k_quant_rows_tma<kRowW, kRowD>;
+  constexpr int smem = kRowW * kRowD * (int)kSeg * 2;
+  static int done[64] = {0};
+  cudaError_t e = opt_in_smem(kern, smem, done);
+  if (e != cudaSuccess) return e;
+  const size_t units = (size_t)M * ((K + kSeg - 1) / kSeg);
+  const unsigned grid = grid_for(units, kRowW, 1);
+  kern<<<grid, 32 * kRowW, smem, st>>>(static_cast<const uint16_t*>(x), (uint32_t)M, (uint32_t)K,
+                                       (uint32_t)round_up4(M), q, s, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,
                                 uint8_t* qT, cudaStream_t st) {
-  const size_t blocks = (size_t)(N / 128) * (K / 128);
-  const unsigned grid = grid_for(blocks, 1, 8);
-  k_quant_weight<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(w), (uint32_t)N,
-                                            (uint32_t)K, q, s, qT);
+  unsigned* err = device_error_word();
+  if (err == nullptr) return cudaErrorInvalidValue;
+  CUtensorMap map;
+  if (!encode_map_2d(&map, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2,
+                     64, 128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    return cudaErrorInvalidValue;
+  auto kern = k_quant_weight_tma;
+  constexpr int smem = kBf16WG * kRing * 32768 + 1024;
+  static int done[64] = {0};
+  cudaError_t e = opt_in_smem(kern, smem, done);
+  if (e != cudaSuccess) return e;
+  const size_t tiles = (size_t)(N / 128) * (K / 128);
+  kern<<<grid_for(tiles, kBf16WG, 1), 256 * kBf16WG, smem, st>>>(
+      map, Q2Args{(uint32_t)N, (uint32_t)K, q, s, qT, err});
   return cudaGetLastError();
 }
 
 cudaError_t launch_requant_row2col(const uint8_t* q, const float* s, int64_t M, int64_t K,
                                    uint8_t* qT, float* sT, cudaStream_t st) {
-  const size_t blocks = (size_t)(M / 128) * (K / 128);
-  const unsigned grid = grid_for(blocks, 1, 6);
-  k_requant_row2col<<<grid, kThreads, 0, st>>>(q, s, (uint32_t)M, (uint32_t)K, qT, sT);
+  unsigned* err = device_error_word();
+  if (err == nullptr) return cudaErrorInvalidValue;
+  CUtensorMap map;
+  if (!encode_map_2d(&map, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)K, (uint64_t)M, (uint64_t)K, 128,
+                     128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    return cudaErrorInvalidValue;
+  auto kern = k_requant_row2col_tma;
+  constexpr int smem = kQ3WG * kRing * 17408 + 1024;
+  static int done[64] = {0};
+  cudaError_t e = opt_in_smem(kern, smem, done);
+  if (e != cudaSuccess) return e;
+  const size_t tiles = (size_t)(M / 128) * (K / 128);
+  kern<<<grid_for(tiles, kQ3WG, 1), 256 * kQ3WG, smem, st>>>(
+      map, Q3Args{(uint32_t)M, (uint32_t)K, s, qT, sT, err});
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_grad_dual(const void* dy, int64_t M, int64_t N, uint8_t* q_row,
                                    float* s_row, uint8_t* qT_col, float* sT_col, cudaStream_t st) {
   if (qT_col == nullptr) return launch_quant_rowgroups(dy, M, N, q_row, s_row, st);
-  const size_t blocks = (size_t)(M / 128) * (N / 128);
-  const unsigned grid = grid_for(blocks, 1, 8);
-  k_quant_grad_dual<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(dy), (uint32_t)M,
-                                               (uint32_t)N, (uint32_t)round_up4(M), q_row, s_row,
-                                               qT_col, sT_col);
+  unsigned* err = device_error_word();
+  if (err == nullptr) return cudaErrorInvalidValue;
+  CUtensorMap map;
+  if (!encode_map_2d(&map, dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2,
+                     64, 128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    return cudaErrorInvalidValue;
+  auto kern = k_quant_grad_dual_tma;
+  constexpr int smem = kBf16WG * kRing * 32768 + 1024;
+  static int done[64] = {0};
+  cudaError_t e = opt_in_smem(kern, smem, done);
+  if (e != cudaSuccess) return e;
+  const size_t tiles = (size_t)(M / 128) * (N / 128);
+  kern<<<grid_for(tiles, kBf16WG, 1), 256 * kBf16WG, smem, st>>>(
+      map, Q4Args{(uint32_t)M, (uint32_t)N, (uint32_t)round_up4(M), q_row, s_row, qT_col, sT_col, err});
+  return cudaGetLastError();
+}
+
+template <int W, int D, uint32_t SLOT>
+cudaError_t launch_rmsnorm_tma(const void* x, const void* gamma, float eps, int64_t M, int64_t H,
+                               uint8_t* q, float* s, float* rstd, void* y, unsigned* err, cudaStream_t st) {
+  auto kern = k_rmsnorm_quant_tma<W, D, SLOT>;
+  constexpr int smem = (1 + W * D) * (int)SLOT * 2;
+  static int done[64] = {0};
+  cudaError_t e = opt_in_smem(kern, smem, done);
+  if (e != cudaSuccess) return e;
+  kern<<<grid_for((size_t)M, W, 1), 32 * W, smem, st>>>(
+      static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma), eps, (uint32_t)M, (uint32_t)H,
+      (uint32_t)round_up4(M), q, s, rstd, static_cast<uint16_t*>(y), err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, int64_t M,
                                  int64_t H, uint8_t* q, float* s, float* rstd, void* y,
                                  cudaStream_t st) {
+  unsigned* err = device_error_word();
+  if (err == nullptr) return cudaErrorInvalidValue;
+  // rows up to 8192 wide stream whole through shared memory; wider rows take
+  // the register kernel (which reads each row twice)
+  if (H <= 4096) return launch_rmsnorm_tma<12, 2, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+  if (H <= 8192) return launch_rmsnorm_tma<6, 2, 8192>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
   const unsigned grid = grid_for((size_t)M, kThreads / 32, 8);
   k_rmsnorm_quant<<<grid, kThreads, 0, st>>>(
       static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma), eps, (uint32_t)M,
@@ -754,8 +1272,9 @@ cudaError_t launch_rmsnorm_bwd(const void* x, const void* gamma, const float* rs
   k_rmsnorm_bwd_dx<<<grid, kThreads, 0, st>>>(xb, static_cast<const uint16_t*>(gamma), rstd, db,
                                               (uint32_t)M, (uint32_t)H, static_cast<uint16_t*>(dx));
   const uint32_t chunks = (uint32_t)((M + kNormBwdRows - 1) / kNormBwdRows);
-  const dim3 pgrid((unsigned)((H + 511) / 512), chunks);
-  k_rmsnorm_bwd_dgamma_partial<<<pgrid, kThreads, 0, st>>>(xb, rstd, db, (uint32_t)M, (uint32_t)H, ws);
+  const dim3 pgrid((unsigned)((H + 511) / 512), chunks < 65535u ? chunks : 65535u);
+  k_rmsnorm_bwd_dgamma_partial<<<pgrid, kThreads, 0, st>>>(xb, rstd, db, (uint32_t)M, (uint32_t)H,
+                                                           chunks, ws);
   k_rmsnorm_bwd_dgamma_reduce<<<(unsigned)((H + 31) / 32), kThreads, 0, st>>>(
       ws, chunks, (uint32_t)H, dgamma);
   return cudaGetLastError();

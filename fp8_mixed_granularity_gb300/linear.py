@@ -55,23 +55,30 @@ class LinearBuffers:
                 stream=None, events=None) -> int:
         t = self.t
         if self.rmsnorm:
-            J.jetfp8_rmsnorm_quant(x, gamma, 1e-6, t["xq"], t["sx"], t["rstd"], None, stream)
+            _timed(events, "rmsnorm_quant",
+                   lambda: J.jetfp8_rmsnorm_quant(x, gamma, 1e-6, t["xq"], t["sx"], t["rstd"], None, stream), stream)
         else:
-            J.jetfp8_quant_act_1x128(x, t["xq"], t["sx"], stream)
-        J.jetfp8_quant_weight_128x128(w, t["wq"], t["sw"], t["wqT"], stream)
-        _timed(events, "gemm_fprop", lambda: J.jetfp8_gemm_fprop(t["xq"], t["sx"], t["wq"], t["sw"], t["y"], stream))
+            _timed(events, "quant_act", lambda: J.jetfp8_quant_act_1x128(x, t["xq"], t["sx"], stream), stream)
+        _timed(events, "quant_weight",
+               lambda: J.jetfp8_quant_weight_128x128(w, t["wq"], t["sw"], t["wqT"], stream), stream)
+        _timed(events, "gemm_fprop",
+               lambda: J.jetfp8_gemm_fprop(t["xq"], t["sx"], t["wq"], t["sw"], t["y"], stream), stream)
         return 3
 
     def backward(self, dy: torch.Tensor, stream=None, events=None, wgrad: bool = True) -> int:
         """Q4, F2, Q3 and (unless `wgrad` is False, for a later grouped
         launch by `wgrad_grouped`) F3.  Returns the number of launches."""
         t = self.t
-        J.jetfp8_quant_grad_dual(dy, t["dyq"], t["sdy"], t["dyqT"], t["sdyT"], stream)
-        _timed(events, "gemm_dgrad", lambda: J.jetfp8_gemm_dgrad(t["dyq"], t["sdy"], t["wqT"], t["sw"], t["dx"], stream))
-        J.jetfp8_requant_rowgrp_to_colgrp(t["xq"], t["sx"], t["xqT"], t["sxT"], stream)
+        _timed(events, "quant_grad_dual",
+               lambda: J.jetfp8_quant_grad_dual(dy, t["dyq"], t["sdy"], t["dyqT"], t["sdyT"], stream), stream)
+        _timed(events, "gemm_dgrad",
+               lambda: J.jetfp8_gemm_dgrad(t["dyq"], t["sdy"], t["wqT"], t["sw"], t["dx"], stream), stream)
+        _timed(events, "requant",
+               lambda: J.jetfp8_requant_rowgrp_to_colgrp(t["xq"], t["sx"], t["xqT"], t["sxT"], stream), stream)
         if not wgrad:
             return 3
-        _timed(events, "gemm_wgrad", lambda: J.jetfp8_gemm_wgrad(t["dyqT"], t["sdyT"], t["xqT"], t["sxT"], t["dw"], stream))
+        _timed(events, "gemm_wgrad",
+               lambda: J.jetfp8_gemm_wgrad(t["dyqT"], t["sdyT"], t["xqT"], t["sxT"], t["dw"], stream), stream)
         return 4
 
 
@@ -82,20 +89,22 @@ def wgrad_grouped(bufs, stream=None, events=None) -> int:
     n = 0
     for i in range(0, len(bufs), J.MAX_GROUP):
         probs = [(b.t["dyqT"], b.t["sdyT"], b.t["xqT"], b.t["sxT"], b.t["dw"]) for b in bufs[i:i + J.MAX_GROUP]]
-        _timed(events, "gemm_wgrad_grouped", lambda: J.jetfp8_gemm_wgrad_grouped(probs, stream))
+        _timed(events, "gemm_wgrad_grouped", lambda: J.jetfp8_gemm_wgrad_grouped(probs, stream), stream)
         n += 1
     return n
 
 
-def _timed(events, name, fn):
-    """Run fn; if `events` (a list) is given, bracket it with CUDA events on the
-    current stream and append (name, start, end)."""
+def _timed(events, name, fn, stream=None):
+    """Run fn, which launches on `stream` (None: the current stream); if
+    `events` (a list) is given, bracket it with CUDA events recorded on that
+    same stream and append (name, start, end)."""
     if events is None:
         fn()
         return
+    st = torch.cuda.current_stream() if stream is None else stream
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
-    s.record()
+    s.record(st)
     fn()
-    e.record()
+    e.record(st)
     events.append((name, s, e))

@@ -149,3 +149,13 @@ def device_normal(shape, std: float, device, seed: int = 0) -> torch.Tensor:
 def device_uniform(shape, lo: float, hi: float, device, seed: int = 0) -> torch.Tensor:
     gen = torch.Generator(device=device).manual_seed(seed)
     return (torch.rand(*shape, device=device, generator=gen, dtype=torch.float32) * (hi - lo) + lo).to(torch.bfloat16)
+
+
+def device_channel_outlier_activations(M: int, K: int, device, seed: int = 0,
+                                       lo: float = 1.0, hi: float = 50.0) -> torch.Tensor:
+    """X ~ N(0,1)·c_k, c_k log-uniform in [lo, hi] per input channel k, drawn on the device."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    c = torch.exp(torch.rand(K, device=device, generator=gen, dtype=torch.float32)
+                  * (np.log(hi) - np.log(lo)) + np.log(lo))
+    x = torch.randn(M, K, device=device, generator=gen, dtype=torch.float32) * c[None, :]
+    return x.to(torch.bfloat16)

@@ -82,6 +82,44 @@ def test_validation_rejects_before_touching_the_device(lib):
     assert lib.jetfp8_gemm_fprop(P(64), P(64), P(64), P(64), 0, 128, 128, P(64), 0, None) == 1
 
 
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="passes placeholder addresses: only where no GPU can be reached")
+def test_noalloc_rejects_scratch_above_8mib(lib):
+    """The allocation-free RMSNorm backward refuses sizes whose scratch would
+    exceed its fixed 8 MiB.  Placeholder (never dereferenced) addresses are
+    passed, so this runs only on a machine without a GPU: there, even if the
+    size check were skipped, the device check after it would refuse the call
+    before any launch."""
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    fn = lib.jetfp8_rmsnorm_bwd_noalloc
+    fn.argtypes = [P, P, P, P, I64, I64, P, P, P]
+    lib.jetfp8_rmsnorm_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.jetfp8_rmsnorm_bwd_workspace_bytes.argtypes = [I64, I64]
+    H = 4096
+    # 512 chunks of 128 rows × 4096 columns × 4 B is exactly 8 MiB; one more row is too many
+    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(128 * 512, H) == (8 << 20)
+    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(128 * 512 + 1, H) > (8 << 20)
+    A = P(1 << 20)
+    assert fn(A, A, A, A, 128 * 512 + 1, H, A, A, None) == 2      # JETFP8_ERR_UNSUPPORTED_SHAPE
+    # the largest size passes the size check and stops at the device check (no GPU here)
+    assert fn(A, A, A, A, 128 * 512, H, A, A, None) == 4          # JETFP8_ERR_CUDA
+
+
+def test_rmsnorm_bwd_many_row_chunks_validated(lib):
+    """A shape with more 128-row chunks than a grid's y dimension holds
+    (65535) is accepted by validation: the partial-sum kernel loops over its
+    chunks.  Here validation stops at the device check (no GPU)."""
+    if __import__("torch").cuda.is_available():
+        pytest.skip("placeholder addresses: only where no GPU can be reached")
+    P, I64, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    fn = lib.jetfp8_rmsnorm_bwd
+    fn.argtypes = [P, P, P, P, I64, I64, P, P, P, SZ, P]
+    M, H = 128 * 70000, 128
+    ws = lib.jetfp8_rmsnorm_bwd_workspace_bytes(M, H)
+    A = P(1 << 20)
+    assert fn(A, A, A, A, M, H, A, A, A, SZ(ws), None) == 4         # JETFP8_ERR_CUDA, not a shape error
+
+
 def test_grouped_wgrad_validation(lib):
     """The grouped WGrad refuses a bad problem count, null arrays and any
     problem's bad shape or alignment before touching the device."""

@@ -185,10 +185,11 @@ def test_rmsnorm_quant_parity(dev, M, H):
     # y within one bf16 ulp of the FP64 result rounded to bf16
     ulp = np.ldexp(1.0, np.frexp(np.abs(oy))[1] - 8)
     assert np.all(np.abs(gy - oy) <= ulp)
-    # rstd: per lane, 8-square FP32 chunk sums (<= 7 roundings) added in FP32
-    # (<= H/256 - 1 more), lanes combined in FP64: relative error of Σx² below
-    # 22·2^-24 for H = 4096, halved by the square root, plus the final FP32
-    # rounding -> at most 12·2^-24; the test allows 16·2^-24.
+    # rstd: Σx² in FP32 as 16-square chains per lane and group, a binary tree
+    # over a lane's groups and a butterfly over the lanes (at most 25 roundings
+    # of positive terms), one more each for /H and +eps, halved by the square
+    # root, plus the reciprocal square root's rounding -> at most 14·2^-24 to
+    # first order; the test allows 16·2^-24.
     assert np.allclose(h(rstd), orstd, rtol=16 * 2.0 ** -24, atol=0)
     # the fused quantiser is bit-exact on the GPU's own y
     gq, gs = O.quant_rowgroups(gy.astype(np.float32))
@@ -224,3 +225,119 @@ def test_swiglu_bwd_parity(dev):
     gd = h(dgu.float()).astype(np.float64)
     ulp = np.ldexp(1.0, np.frexp(np.abs(od))[1] - 8)
     assert np.all(np.abs(gd - od) <= ulp + 1e-40)
+
+
+# ---------------------------------------------------------------------------
+# The division-free scale over every bf16 maximum, and the TMA-fed kernels'
+# segment and width variants
+# ---------------------------------------------------------------------------
+def _group_maxima():
+    """Every positive finite bf16 value (0x0001 .. 0x7F7F), then 0: 32640 = 255·128."""
+    a = (np.arange(1, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    a = np.concatenate([a, np.zeros(1, np.float32)])
+    assert a[-2] == np.float32(3.3895314e38) and np.all(np.isfinite(a)) and len(a) == 255 * 128
+    return a
+
+
+def _every_bf16_max_groups(seed):
+    """[32640, 128] bf16 values: row r holds the r-th group maximum a_r at a
+    random position (random sign) and otherwise values of magnitude ≤ a_r;
+    the last row is all zeros."""
+    a = _group_maxima()
+    g = np.random.default_rng(seed)
+    u = g.uniform(-1.0, 1.0, size=(len(a), 128)).astype(np.float64)
+    x = W.to_bf16((u * a[:, None].astype(np.float64)).astype(np.float32))
+    xf = W.bf16_values(x)
+    assert np.all(np.abs(xf) <= a[:, None])
+    pos = g.integers(0, 128, size=len(a))
+    xf[np.arange(len(a)), pos] = a * np.where(g.random(len(a)) < 0.5, -1.0, 1.0).astype(np.float32)
+    return W.to_bf16(xf), a
+
+
+def test_quant_act_every_bf16_group_max(dev):
+    """S = fp32(amax/448) from the kernels' division-free sequence, for every
+    positive finite bf16 group maximum (one group each), codes included."""
+    x, a = _every_bf16_max_groups(seed=41)
+    q, s = q_act(x, dev)
+    want = np.where(a == 0, np.float32(1.0), (a / np.float32(448.0)).astype(np.float32))
+    assert np.array_equal(h(s)[0, :len(a)], want)
+    _assert_rowquant(q, s, W.bf16_values(x))
+
+
+def test_quant_grad_dual_every_bf16_group_max(dev):
+    """The dual quantiser over every bf16 maximum, once as row groups (a
+    [32640, 128] gradient) and once as 128-token column groups (its transpose)."""
+    x, a = _every_bf16_max_groups(seed=42)
+    xf = W.bf16_values(x)
+    for t in (x, W.to_bf16(np.ascontiguousarray(xf.T))):
+        q, s, qT, sT = q_grad(t, dev)
+        oq, os_, oqT, osT = O.quant_grad_dual(W.bf16_values(t))
+        M = t.shape[0]
+        assert np.array_equal(h(s)[:, :M], os_) and np.array_equal(h(q), oq)
+        assert np.array_equal(h(sT), osT) and np.array_equal(h(qT), oqT)
+
+
+def test_quant_weight_block_max_sweep(dev):
+    """128×128 blocks whose maxima step through the bf16 range (every 16th
+    positive finite value, both extremes included)."""
+    a = _group_maxima()[:-1]
+    a = np.concatenate([a[::16][:2039], a[-1:]])
+    assert a[-1] == np.float32(3.3895314e38) and len(a) == 2040
+    nb = len(a)
+    g = np.random.default_rng(43)
+    blocks = (g.uniform(-1, 1, size=(nb, 128, 128)) * a[:, None, None].astype(np.float64)).astype(np.float32)
+    blocks = W.bf16_values(W.to_bf16(blocks.reshape(nb * 128, 128))).reshape(nb, 128, 128)
+    blocks[np.arange(nb), g.integers(0, 128, nb), g.integers(0, 128, nb)] = a
+    # lay the blocks out as a [nb/8·128, 8·128] weight (8 blocks per block row)
+    w = blocks.reshape(nb // 8, 8, 128, 128).transpose(0, 2, 1, 3).reshape(nb // 8 * 128, 8 * 128)
+    wt = W.to_bf16(np.ascontiguousarray(w))
+    q, s, qT = q_weight(wt, dev)
+    oq, os_, oqT = O.quant_weight_128x128(W.bf16_values(wt))
+    assert np.array_equal(h(s), os_) and np.array_equal(h(q), oq) and np.array_equal(h(qT), oqT)
+
+
+def test_requant_scales_across_the_fp32_range(dev):
+    """Requantisation with row scales log-uniform over most of the FP32 range,
+    so column maxima x̃ = fp32(dec(q)·S) take the division-free scale above
+    2^-100 and the division below it."""
+    M, K = 1024, 1024
+    g = np.random.default_rng(44)
+    finite = np.concatenate([np.arange(0x7F), np.arange(0x80, 0xFF)]).astype(np.uint8)
+    codes = g.choice(finite, size=(M, K))
+    # one exponent per (k-block, 128-row band), jittered per row: a column
+    # group's maximum follows its band's exponent, from 2^-126 to 2^100
+    band = g.integers(-126, 100, size=(K // 128, M // 128))
+    e = np.repeat(band, 128, axis=1) + g.integers(0, 4, size=(K // 128, M))
+    s = np.ldexp(g.uniform(1.0, 2.0, size=(K // 128, M)), e).astype(np.float32)
+    qT, sT = requant(torch.from_numpy(codes).to(dev), torch.from_numpy(s).to(dev), dev)
+    oqT, osT = O.requant_rowgrp_to_colgrp(codes, s)
+    assert np.any(osT < 2.0 ** -100 / 448) and np.any(osT > 1.0)
+    assert np.array_equal(h(sT), osT) and np.array_equal(h(qT), oqT)
+
+
+@pytest.mark.parametrize("M,K", [(5, 14336), (3, 4224), (9, 8192), (700, 256)])
+def test_quant_act_row_segments(dev, M, K):
+    """Rows longer than one streamed segment (4096 elements), with a short last one."""
+    x = W.activations(M, K, seed=45, stream=K)
+    q, s = q_act(x, dev)
+    _assert_rowquant(q, s, W.bf16_values(x))
+
+
+@pytest.mark.parametrize("M,H", [(40, 5120), (33, 8192), (17, 12288)])
+def test_rmsnorm_quant_row_widths(dev, M, H):
+    """The three R1 variants: rows streamed whole through 8 KB or 16 KB slots,
+    and wider rows through the register kernel."""
+    x = W.activations(M, H, seed=46)
+    gamma = W.uniform((H,), 0.5, 1.5, seed=46, stream=9)
+    q, s = J.empty_rowgroup_quant(M, H, dev)
+    rstd = torch.empty(M, dtype=torch.float32, device=dev)
+    y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    J.jetfp8_rmsnorm_quant(x.to(dev), gamma.to(dev), 1e-6, q, s, rstd, y)
+    check_errors()
+    oy, orstd, oq, os_ = O.rmsnorm_quant(W.bf16_values(x), W.bf16_values(gamma), 1e-6)
+    gy = h(y.float()).astype(np.float64)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(oy))[1] - 8)
+    assert np.all(np.abs(gy - oy) <= ulp)
+    assert np.allclose(h(rstd), orstd, rtol=16 * 2.0 ** -24, atol=0)
+    gq, gs = O.quant_rowgroups(gy.astype(np.float32))
+    assert np.array_equal(h(s)[:, :M], gs) and np.array_equal(h(q), gq)

@@ -1,7 +1,8 @@
 """The allocation-free RMSNorm backward (the library's fixed 8 MiB scratch)
 against the workspace entry point: two consecutive calls on the same inputs
-must both equal it bit for bit, and sizes whose scratch would exceed 8 MiB are
-rejected.  Kept in a file collected last; it also runs on its own."""
+must both equal it bit for bit.  Kept in a file collected last; it also runs
+on its own.  The refusal of sizes whose scratch would exceed 8 MiB is checked
+on the host, where no device can be reached (tests/test_abi.py)."""
 import pytest
 import torch
 
@@ -39,16 +40,3 @@ def test_noalloc_matches_workspace_entry_point(dev, M, H):
         J.jetfp8_rmsnorm_bwd_noalloc(x, gamma, rstd, dy, dx, dg)
         check_errors()
         assert torch.equal(dx, dx_ref) and torch.equal(dg, dg_ref)
-
-
-def test_noalloc_rejects_scratch_above_8mib(dev):
-    """Validated before any device access: aligned dummy addresses suffice."""
-    import ctypes
-    M, H = 128 * 513, 4096            # 513 chunks × 4096 × 4 B > 8 MiB
-    assert J.jetfp8_rmsnorm_bwd_workspace_bytes(M, H) > (8 << 20)
-    lib = J.load_library()
-    P = ctypes.c_void_p(1 << 20)      # 1 MiB: aligned for every argument, never dereferenced
-    st = lib.jetfp8_rmsnorm_bwd_noalloc(P, P, P, P, M, H, P, P, None)
-    assert st == 2, J._STATUS.get(st, st)    # JETFP8_ERR_UNSUPPORTED_SHAPE
-    # the largest size that fits is accepted by the check (returns OK or a CUDA error, never 2)
-    assert J.jetfp8_rmsnorm_bwd_workspace_bytes(128 * 512, H) == (8 << 20)
