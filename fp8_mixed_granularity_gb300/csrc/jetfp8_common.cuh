@@ -15,7 +15,7 @@
 namespace jetfp8 {
 
 constexpr float kE4M3Max = 448.0f;
-// Group maxima below this (and above 0) quantise their elements by IEEE division.
+// Group maxima below this (and above 0) form their element quotients on operands scaled by 2^96.
 constexpr float kQuotientMinAmax = 0x1p-80f;
 
 // Error bits recorded in the device error word.
@@ -151,7 +151,7 @@ __device__ __forceinline__ void quant_pairs(const float2 (&v)[N], const GroupSca
 // q2 = RN(x/S) (P. Markstein, IBM J. Res. Dev. 34(1), 1990).  The sequence runs
 // on -x and -y so that the sign of a zero survives.  It holds while every
 // intermediate is a normal number, i.e. for groups with amax >= 2^-80 (and
-// amax = 0); smaller maxima take IEEE divisions (`slow`).  The sequence was
+// amax = 0); groups with smaller maxima (`slow`) run it on x·2^96 and S·2^96.  The sequence was
 // checked in exact arithmetic against RN(x/S) for every bf16 element of
 // sampled groups and for FP32 elements next to every kind of E4M3 midpoint.
 // ---------------------------------------------------------------------------
@@ -159,7 +159,7 @@ struct QScale {
   uint64_t s2;    // (S, S)
   uint64_t ny2;   // (-y, -y), y = RN(1/S)
   float s;
-  bool slow;      // 0 < amax < 2^-80: element quotients by IEEE division
+  bool slow;      // 0 < amax < 2^-80: quotients formed on scaled operands (codes4_tiny)
 };
 
 __device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
@@ -235,10 +235,13 @@ __device__ __forceinline__ uint32_t codes4_neg_f32(uint64_t nx0, uint64_t nx1, c
   return c;
 }
 
-// Four codes from IEEE quotients (groups with tiny maxima).
-__device__ __forceinline__ uint32_t codes4_div(float2 v0, float2 v1, float s) {
-  return cvt_e4m3x2(__fdiv_rn(v0.x, s), __fdiv_rn(v0.y, s)) |
-         (cvt_e4m3x2(__fdiv_rn(v1.x, s), __fdiv_rn(v1.y, s)) << 16);
+// Four codes of a group with a tiny maximum (0 < amax < kQuotientMinAmax):
+// the elements and S scaled by 2^96 (exact, the quotients unchanged) put every
+// intermediate of the sequence above in the normal range.
+__device__ __forceinline__ uint32_t codes4_tiny(float2 v0, float2 v1, float s) {
+  constexpr float k = 0x1p96f;
+  const QScale g = qscale_from_s(s * k, false);
+  return codes4_neg_f32(pack_f2(v0.x * -k, v0.y * -k), pack_f2(v1.x * -k, v1.y * -k), g);
 }
 
 // Two E4M3 codes (low byte first) -> two exact floats.

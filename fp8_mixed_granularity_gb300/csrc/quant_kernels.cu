@@ -212,7 +212,7 @@ __device__ __forceinline__ void group16_codes(const uint32_t (&w)[8], bool valid
   uint32_t c[4];
   if (amax != 0.0f && amax < kQuotientMinAmax) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) c[k] = codes4_div(bf2_to_f2(w[2 * k]), bf2_to_f2(w[2 * k + 1]), S);
+    for (int k = 0; k < 4; ++k) c[k] = codes4_tiny(bf2_to_f2(w[2 * k]), bf2_to_f2(w[2 * k + 1]), S);
   } else {
     const QScale g = qscale_from_s(S, false);
 #pragma unroll
@@ -304,14 +304,14 @@ k_quant_rows_tma(const uint16_t* __restrict__ x, uint32_t M, uint32_t K, uint32_
 // R1 on a row stream: one unit = one whole row (H ≤ SLOT_ELEMS), γ staged in
 // shared memory once per CTA.  Σx² in FP32: per lane a 16-term FMA chain per
 // group, the lane's groups (at most SLOT_ELEMS/512 = 16) added as a binary
-// tree, the 32 lanes by a butterfly; r = RN(1/sqrt(Σx²/H + eps)) (IEEE
-// reciprocal square root).  With at most 16 + 4 + 5 roundings on a sum of
-// positive terms, the relative error of Σx² is at most 25·2^-24 (first order)
-// and that of r at most 14·2^-24.
+// tree, the 32 lanes by a butterfly; r = RN(1/sqrt(RN(Σx²·RN(1/H)) + eps))
+// (IEEE reciprocal square root).  With at most 16 + 4 + 5 roundings on a sum
+// of positive terms, the relative error of Σx² is at most 25·2^-24 (first
+// order), and that of r at most 14.25·2^-24.
 template <int W, int D, uint32_t SLOT_ELEMS>
 __global__ void __launch_bounds__(32 * W, 1)
 k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
-                    uint32_t M, uint32_t H, uint32_t ld_s, uint8_t* __restrict__ q,
+                    float inv_h, uint32_t M, uint32_t H, uint32_t ld_s, uint8_t* __restrict__ q,
                     float* __restrict__ s, float* __restrict__ rstd, uint16_t* __restrict__ y,
                     unsigned* err) {
   extern __shared__ __align__(1024) uint8_t dsm[];
@@ -380,7 +380,7 @@ k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__
     float ss = cs[0];
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, o));
-    const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps));
+    const float r = __frsqrt_rn(__fadd_rn(__fmul_rn(ss, inv_h), eps));
     if (lane == 0) rstd[row] = r;
     for (uint32_t g0 = 0; g0 < ng; g0 += 4) {
       const uint32_t grp = g0 + g4;
@@ -566,7 +566,7 @@ __device__ __forceinline__ void col_group_amax(const uint32_t (&w)[8][4], float 
 
 // Codes of the 8 rows of a row-pass block under per-row constants (s[i],
 // ny[i]); row i's 8 codes (columns in order) go to put(i, codes).  Rows whose
-// group is slow (bit i of `slow`) are stored again from IEEE quotients.
+// group is slow (bit i of `slow`) are stored again from scaled operands.
 template <class Put>
 __device__ __forceinline__ void row_codes_bf16(const uint32_t (&w)[8][4], const float (&s)[8],
                                                const float (&ny)[8], uint32_t slow, Put put) {
@@ -579,8 +579,8 @@ __device__ __forceinline__ void row_codes_bf16(const uint32_t (&w)[8][4], const 
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       if (slow & (1u << i))
-        put(i, make_uint2(codes4_div(bf2_to_f2(w[i][0]), bf2_to_f2(w[i][1]), s[i]),
-                          codes4_div(bf2_to_f2(w[i][2]), bf2_to_f2(w[i][3]), s[i])));
+        put(i, make_uint2(codes4_tiny(bf2_to_f2(w[i][0]), bf2_to_f2(w[i][1]), s[i]),
+                          codes4_tiny(bf2_to_f2(w[i][2]), bf2_to_f2(w[i][3]), s[i])));
   }
 }
 
@@ -600,8 +600,8 @@ __device__ __forceinline__ void col_codes_bf16(const uint32_t (&w)[8][4], const 
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (slow & (1u << j))
-        put(j, codes4_div(bf2_to_f2(pair(j, 0)), bf2_to_f2(pair(j, 2)), s[j]),
-            codes4_div(bf2_to_f2(pair(j, 4)), bf2_to_f2(pair(j, 6)), s[j]));
+        put(j, codes4_tiny(bf2_to_f2(pair(j, 0)), bf2_to_f2(pair(j, 2)), s[j]),
+            codes4_tiny(bf2_to_f2(pair(j, 4)), bf2_to_f2(pair(j, 6)), s[j]));
   }
 }
 
@@ -831,7 +831,7 @@ k_requant_row2col_tma(const __grid_constant__ CUtensorMap map, const Q3Args a) {
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj)
         if (slow & (1u << jj))
-          put(jj, codes4_div(xpair(jj, 0), xpair(jj, 1), sc[jj]), codes4_div(xpair(jj, 2), xpair(jj, 3), sc[jj]));
+          put(jj, codes4_tiny(xpair(jj, 0), xpair(jj, 1), sc[jj]), codes4_tiny(xpair(jj, 2), xpair(jj, 3), sc[jj]));
     }
     if (rg == 0) {
       float* sp = a.sT + (size_t)mb * a.K + k0 + 8 * cg;
@@ -1238,8 +1238,8 @@ cudaError_t launch_rmsnorm_tma(const void* x, const void* gamma, float eps, int6
   cudaError_t e = opt_in_smem(kern, smem, done);
   if (e != cudaSuccess) return e;
   kern<<<grid_for((size_t)M, W, 1), 32 * W, smem, st>>>(
-      static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma), eps, (uint32_t)M, (uint32_t)H,
-      (uint32_t)round_up4(M), q, s, rstd, static_cast<uint16_t*>(y), err);
+      static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma), eps, 1.0f / (float)H, (uint32_t)M,
+      (uint32_t)H, (uint32_t)round_up4(M), q, s, rstd, static_cast<uint16_t*>(y), err);
   return cudaGetLastError();
 }
 
