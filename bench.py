@@ -82,6 +82,9 @@ def parse_args():
     p.add_argument("--case", choices=sorted(CASES), default=None,
                    help="time one kernel alone (for profiling) instead of the layer step")
     p.add_argument("--shape", default="8192,28672,4096", help="M,N,K for --case")
+    p.add_argument("--gemm-path", type=int, choices=[0, 1, 2], default=0,
+                   help="with --case: GEMM kernel choice (0 automatic, 1 single-CTA tiles, 2 CTA-pair "
+                        "tiles where the shape allows)")
     p.add_argument("--graph", action="store_true",
                    help="with --case: capture the timed launches in a CUDA graph and time its replay "
                         "(kernel time without the per-call host work, as a serving loop runs decode)")
@@ -770,6 +773,7 @@ def run_case(args):
     from fp8_mixed_granularity_gb300 import workloads as W
     from fp8_mixed_granularity_gb300.linear import LinearBuffers
     M, N, K = (int(v) for v in args.shape.split(","))
+    J.jetfp8_test_set_gemm_path(args.gemm_path)
     if args.case == "decoder_layer":
         # a Llama-3.1-8B-shaped decoder layer (BF16 attention core), forward +
         # backward, on M tokens = M/1024 sequences of 1024; the rate counts the
@@ -931,7 +935,8 @@ def _time_case(args, fn, work, unit, shape):
         med = ms[len(ms) // 2]
     scale = 1e12 if unit == "TFLOP/s" else 1e9
     print(json.dumps({"case": args.case, "shape": shape, "median_ms": med, "min_ms": ms[0],
-                      "value": work / (med * 1e-3) / scale, "unit": unit, "graph": bool(args.graph)}),
+                      "value": work / (med * 1e-3) / scale, "unit": unit, "graph": bool(args.graph),
+                      "gemm_path": args.gemm_path}),
           flush=True)
 
 

@@ -427,6 +427,13 @@ jetfp8_status jetfp8_test_gemm_fprop_drop_block(const uint8_t* xq, const float* 
   return from_cuda(launch_gemm(g, stream));
 }
 
+jetfp8_status jetfp8_test_set_gemm_path(int mode) {
+  log_call("jetfp8_test_set_gemm_path", mode);
+  if (mode < 0 || mode > 2) return JETFP8_ERR_INVALID_ARG;
+  set_gemm_path(mode);
+  return JETFP8_OK;
+}
+
 size_t jetfp8_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H) {
   if (M <= 0 || H <= 0) return 0;
   return rmsnorm_bwd_workspace_bytes(M, H);

@@ -57,6 +57,9 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
+// Kernel choice for later GEMM launches: 0 automatic, 1 single-CTA tiles
+// wherever possible, 2 CTA-pair tiles wherever possible.
+void set_gemm_path(int mode);
 // `count` (1..4) column-scale (WGrad) problems in one persistent launch; each
 // problem's output equals that of its own launch_gemm, bit for bit.
 cudaError_t launch_gemm_grouped(const GemmArgs* a, int count, cudaStream_t st);

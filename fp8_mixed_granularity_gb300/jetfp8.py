@@ -48,6 +48,7 @@ SIGNATURES = {
     "jetfp8_swiglu_quant": [_P, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_swiglu_bwd": [_P, _P, _I64, _I64, _P, _P],
     "jetfp8_get_last_device_error": [_P],
+    "jetfp8_test_set_gemm_path": [_INT],
 }
 
 
@@ -290,6 +291,12 @@ def jetfp8_swiglu_bwd(gu, dh, dgu, stream=None):
     _check(load_library().jetfp8_swiglu_bwd(
         _ptr(gu, _BF, None, "gu"), _ptr(dh, _BF, (M, I), "dh"), M, I, _ptr(dgu, _BF, (M, I2), "dgu"),
         _stream(stream)), "jetfp8_swiglu_bwd")
+
+
+def jetfp8_test_set_gemm_path(mode: int):
+    """Kernel choice of later GEMM launches: 0 automatic, 1 single-CTA tiles,
+    2 CTA-pair tiles wherever allowed (results are identical either way)."""
+    _check(load_library().jetfp8_test_set_gemm_path(int(mode)), "jetfp8_test_set_gemm_path")
 
 
 def jetfp8_get_last_device_error(stream=None):

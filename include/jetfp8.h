@@ -211,6 +211,18 @@ jetfp8_status jetfp8_test_gemm_fprop_drop_block(const uint8_t* xq, const float* 
                                                int64_t N, int64_t K, void* y, int drop_kb,
                                                cudaStream_t stream);
 
+/* Test and diagnosis knob (no counterpart on the pages).  Chooses the kernel
+ * of later GEMM launches of this process: 0 (the default) and 1 run every
+ * GEMM on single-CTA tiles, 2 runs every GEMM that allows it (at least 256
+ * rows of output, output width a multiple of 128, no fused output quantiser)
+ * on CTA-pair tiles (tcgen05 cta_group::2, 256 x 128 per pair), which are
+ * slower on GB300 and therefore not chosen by default.  Every output
+ * element's arithmetic is the same on either kernel, so the results are
+ * identical bit for bit; the knob lets tests check that.  Not synchronised with launches
+ * in flight on other host threads.  Returns JETFP8_ERR_INVALID_ARG for any
+ * other mode. */
+jetfp8_status jetfp8_test_set_gemm_path(int mode);
+
 /* Set the environment variable JETFP8_LOG (to anything but "" or "0") and every
  * entry point prints its name and sizes to stderr when called. */
 
