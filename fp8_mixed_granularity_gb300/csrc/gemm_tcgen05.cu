@@ -41,6 +41,12 @@
 // A launch may carry up to four problems of one configuration (the WGrads of a
 // layer's linears, which share the token count): their tiles form one
 // persistent sequence, each tile computed exactly as in a launch of its own.
+// The same kernel body also runs on CTA pairs (tcgen05 cta_group::2, a
+// cluster of two CTAs on two SMs per 256 × 256 tile): each CTA loads its 128
+// rows of A and half of B, the leader issues M = 256 MMAs, and both CTAs
+// promote their own 128 rows exactly as above, so the two kernels' results
+// are identical bit for bit.  The pair kernel is for tests and diagnosis; the
+// single-CTA kernel is faster on GB300 and is the default.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records an
 // error word, lets copies and MMAs in flight land, frees TMEM and returns.
 #include <cuda.h>
@@ -68,12 +74,13 @@ constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 384
 // the launch total, or setmaxnreg.inc would wait forever.  The host refuses to
 // launch unless the compiled kernel uses exactly LAUNCH_REGS.
 constexpr int LAUNCH_REGS = 168;
-// Grouped launches (several problems per launch) give the control warps 32:
-// the TMA producer then also tracks which problem a tile belongs to.
-template <int G> constexpr int CTRL_REGS = G > 1 ? 32 : 24;
-template <int G> constexpr int EPI_REGS = G > 1 ? 232 : 240;
-static_assert(128 * CTRL_REGS<1> + 256 * EPI_REGS<1> <= THREADS * LAUNCH_REGS, "register split");
-static_assert(128 * CTRL_REGS<2> + 256 * EPI_REGS<2> <= THREADS * LAUNCH_REGS, "register split");
+// Grouped launches (several problems per launch) and CTA pairs give the
+// control warps 32: the TMA producer then also tracks which problem a tile
+// belongs to, or the pair's barriers.
+template <int G, bool PAIR> constexpr int CTRL_REGS = G > 1 ? 32 : 24;
+template <int G, bool PAIR> constexpr int EPI_REGS = G > 1 ? 232 : 240;
+static_assert(128 * CTRL_REGS<1, false> + 256 * EPI_REGS<1, false> <= THREADS * LAUNCH_REGS, "register split");
+static_assert(128 * CTRL_REGS<2, true> + 256 * EPI_REGS<2, true> <= THREADS * LAUNCH_REGS, "register split");
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int MAX_STAGES = 8, MAX_BUFS = 4;
 // bf16 output leaves through shared memory in 32-row × 32-column chunks, one
@@ -83,22 +90,25 @@ constexpr int MAX_STAGES = 8, MAX_BUFS = 4;
 // different banks.
 constexpr int OUT_CHUNK_BYTES = 32 * 32 * 2;
 
-template <int BN_>
+// Tile configuration.  PAIR: a CTA pair computes a 256 × BN tile (BN = 256);
+// each CTA holds its 128 rows of A and half (BN/2 rows) of the B tile.
+template <int BN_, bool PAIR = false>
 struct Cfg {
   static constexpr int BN = BN_;
-  // deeper rings for narrower tiles (same shared-memory budget)
-  static constexpr int STAGES = BN_ == 256 ? 4 : (BN_ == 128 ? 6 : 8);
+  static_assert(!PAIR || BN_ == 256, "CTA pairs use 256-wide tiles");
+  // deeper rings for smaller stages (same shared-memory budget)
+  static constexpr int STAGES = PAIR ? 6 : (BN_ == 256 ? 4 : (BN_ == 128 ? 6 : 8));
   static constexpr int A_BYTES = BM * BK;
-  static constexpr int B_BYTES = BN * BK;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int ACC_BUFS = TMEM_COLS / BN < MAX_BUFS ? TMEM_COLS / BN : MAX_BUFS;
   static constexpr int TMEM_ALLOC = ACC_BUFS * BN;   // a power of two >= 32
   static constexpr int EPI_COLS = BN / 2;        // columns per promotion warp
   static constexpr int CHUNKS = EPI_COLS / 32;   // 32-column TMEM loads per block
   // UMMA instruction descriptor: D = F32 (bits 4-5 = 1), A = B = E4M3 (format 0),
-  // both K-major, N/8 at bits 17-22, M/16 at bits 24-28.
+  // both K-major, N/8 at bits 17-22, M/16 at bits 24-28 (M = 256 for a pair).
   static constexpr uint32_t IDESC =
-      (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+      (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((PAIR ? 2 * BM : BM) >> 4) << 24);
   // Column-mode scale staging, per promotion warp and ring slot: the warp's
   // 32 row scales, then its column scales ordered [g][GS] where group
   // g = (c mod 8)/2 holds the columns c = 8j + 2g + {0,1} at 2j + {0,1} (GS
@@ -468,6 +478,62 @@ __device__ __forceinline__ void promote_cols_frag(uint64_t* acc, const uint32_t 
         "l"(sb[1]), "l"(sb[2]), "l"(sb[3]), "l"(sa_lo), "l"(sa_hi));
 }
 
+// ---- CTA pairs (tcgen05 cta_group::2) ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Relaxed arrives hand an accumulator back: the TMEM loads they follow have
+// completed (tcgen05.wait::ld) and nothing else needs ordering, so the arrive
+// does not wait for the thread's other memory operations in flight.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on a
+// barrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+// Issued by the leader CTA of a pair: M = 256 rows, 128 from each CTA's
+// shared memory (same offsets), B halves from both; each CTA's TMEM receives
+// its own 128 rows.
+__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+// Arrives once on the barrier at this shared-memory offset in both CTAs when
+// the MMAs issued so far have completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+
 template <int EPI_COLS>
 struct ColScaleVec;
 template <>
@@ -483,10 +549,9 @@ struct ColScaleVec<128> {
   using T = float4;
 };
 
-template <int BN_, bool COLS, int G>
-__global__ void __launch_bounds__(THREADS, 1)
-k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
-  using C = Cfg<BN_>;
+template <int BN_, bool COLS, int G, bool PAIR>
+__device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
+  using C = Cfg<BN_, PAIR>;
   constexpr int BN = C::BN, STAGES = C::STAGES, ACC_BUFS = C::ACC_BUFS;
   constexpr int EPI_COLS = C::EPI_COLS, CHUNKS = C::CHUNKS;
   using CsVec = typename ColScaleVec<EPI_COLS>::T;
@@ -505,6 +570,17 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_tiles = kp.tile_end[G - 1];
+  // A CTA pair is a cluster of two sharing one 256-row tile (rank 0, the
+  // leader, issues the MMAs); a single CTA is a "cluster" of one.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int cl = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ncl = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  constexpr int TILE_M = PAIR ? 2 * BM : BM;
+  // records the error and stops every role of this CTA (and of the peer)
+  auto fail = [&]() {
+    record_abort(abort_flag, kp.p[0].err);
+    if constexpr (PAIR) st_cluster_u32(mapa_shared(smem_u32((const void*)&bars->abort_flag), rank ^ 1u), 1u);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -513,26 +589,78 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
     }
     for (int b = 0; b < ACC_BUFS; ++b) {
       mbar_init(&bars->tfull[b], 1);
-      mbar_init(&bars->tempty[b], EPI_WARPS);
+      // a pair's accumulators are handed back to the leader by both CTAs
+      mbar_init(&bars->tempty[b], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&bars->tmem_base)),
-                 "r"(C::TMEM_ALLOC));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    if constexpr (PAIR) {
+      // one warp of each CTA of the pair allocates, collectively, the same columns in both
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(&bars->tmem_base)),
+                   "r"(C::TMEM_ALLOC));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(&bars->tmem_base)),
+                   "r"(C::TMEM_ALLOC));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  // (a pair: both CTAs' barriers are initialised before either signals the other's)
+  if constexpr (PAIR) cluster_sync_all();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
   if (warp < EPI_WARP0) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS<G>));
-    if (warp == 0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS<G, PAIR>));
+    if (warp == 0 && PAIR) {
+      // ---------------- TMA producer (both CTAs of a pair) ----------------
+      // Each CTA loads its 128 rows of A and its half of B; every copy counts
+      // on the leader's full barrier, which expects both CTAs' bytes.
+      // (32-bit shared-memory addresses, as in the single-CTA producer)
+      if (lane == 0) {
+        const uint32_t full0 = smem_u32(&bars->full[0]);
+        const uint32_t full_leader0 = mapa_shared(full0, 0);
+        constexpr uint32_t STAGE0_OFF = STAGES * C::STAGE_BYTES + offsetof(Barriers, full);
+        constexpr uint32_t EMPTY_OFF = offsetof(Barriers, empty) - offsetof(Barriers, full);
+        constexpr uint32_t ABORT_OFF = offsetof(Barriers, abort_flag) - offsetof(Barriers, full);
+        const int row_off = (int)rank * BM, col_off = (int)rank * (BN / 2);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
+          int local, mt, nt;
+          const int g = problem_of(kp, tile, local);
+          tile_coords(kp.p[g], local, mt, nt);
+          const int nkb = kp.p[g].nKB;
+          const CUtensorMap* const mA = &kp.tmA[g];   // tmB[g] lies G maps after it
+          for (int kb = 0; kb < nkb; ++kb, ++it) {
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+            const uint32_t full = full0 + 8 * s;
+            if (!mbar_wait_s(full + EMPTY_OFF, ph ^ 1u, full0 + ABORT_OFF)) {
+              fail();
+              ok = false;
+              break;
+            }
+            if (rank == 0) mbar_arrive_expect_tx(full, 2 * C::STAGE_BYTES);
+            const uint32_t st = full0 - STAGE0_OFF + s * C::STAGE_BYTES;
+            tma_load_2d_pair(st, mA, full_leader0 + 8 * s, kb * BK, mt * TILE_M + row_off);
+            tma_load_2d_pair(st + C::A_BYTES, mA + G, full_leader0 + 8 * s, kb * BK, nt * BN + col_off);
+          }
+        }
+        // the leader sees every copy of both CTAs land before the pair exits
+        if (rank == 0) {
+          const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+          for (uint32_t j = first; j < it; ++j)
+            mbar_wait(&bars->full[j % STAGES], (j / STAGES) & 1u, abort_flag, false);
+        }
+      }
+    } else if (warp == 0) {
       // ---------------- TMA producer ----------------
       // (32-bit shared-memory addresses throughout: this warp has few registers)
       if (lane == 0) {
@@ -550,7 +678,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
         bool ok = true;
         static_assert(offsetof(KParams<G>, tmB) == offsetof(KParams<G>, tmA) + G * sizeof(CUtensorMap),
                       "map arrays are contiguous");
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
           int local, mt, nt;
           const int g = problem_of(kp, tile, local);
           tile_coords(kp.p[g], local, mt, nt);
@@ -563,7 +691,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             const uint32_t full = full0 + 8 * s;
             if (!mbar_wait_s(full + EMPTY_OFF, ph ^ 1u, full0 + ABORT_OFF)) {
-              record_abort(abort_flag, kp.p[0].err);
+              fail();
               ok = false;
               break;
             }
@@ -581,11 +709,11 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
           mbar_wait(&bars->full[j % STAGES], (j / STAGES) & 1u, abort_flag, false);
       }
     } else if (warp == 1) {
-      // ---------------- MMA issuer ----------------
-      if (lane == 0) {
+      // ---------------- MMA issuer (a pair's leader) ----------------
+      if (lane == 0 && rank == 0) {
         uint32_t it = 0, acc_it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
           int local;
           const int nkb = kp.p[problem_of(kp, tile, local)].nKB;
           for (int kb = 0; kb < nkb; ++kb, ++it, ++acc_it) {
@@ -593,7 +721,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
             const uint32_t b = acc_it % ACC_BUFS, bph = (acc_it / ACC_BUFS) & 1u;
             if (!mbar_wait(&bars->tempty[b], bph ^ 1u, abort_flag, true) ||
                 !mbar_wait(&bars->full[s], ph, abort_flag, true)) {
-              record_abort(abort_flag, kp.p[0].err);
+              fail();
               ok = false;
               break;
             }
@@ -601,20 +729,32 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
             const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
             const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
-            for (int k = 0; k < BK / 32; ++k)
-              umma_e4m3(tmem + b * BN, sdesc_sw128(a_addr + 32 * k), sdesc_sw128(b_addr + 32 * k),
-                        C::IDESC, k > 0 ? 1u : 0u);
-            umma_commit(&bars->empty[s]);
-            umma_commit(&bars->tfull[b]);
+            for (int k = 0; k < BK / 32; ++k) {
+              if constexpr (PAIR)
+                umma_e4m3_pair(tmem + b * BN, sdesc_sw128(a_addr + 32 * k), sdesc_sw128(b_addr + 32 * k),
+                               C::IDESC, k > 0 ? 1u : 0u);
+              else
+                umma_e4m3(tmem + b * BN, sdesc_sw128(a_addr + 32 * k), sdesc_sw128(b_addr + 32 * k),
+                          C::IDESC, k > 0 ? 1u : 0u);
+            }
+            // (a pair: the commits arrive on these barriers in both CTAs)
+            if constexpr (PAIR) {
+              umma_commit_pair(&bars->empty[s]);
+              umma_commit_pair(&bars->tfull[b]);
+            } else {
+              umma_commit(&bars->empty[s]);
+              umma_commit(&bars->tfull[b]);
+            }
           }
         }
         // all MMAs issued by this thread complete before TMEM is released
-        umma_commit(&bars->done);
-        if (!mbar_wait(&bars->done, 0, abort_flag, false)) record_abort(abort_flag, kp.p[0].err);
+        if constexpr (PAIR) umma_commit_pair(&bars->done);
+        else umma_commit(&bars->done);
       }
+      if (lane == 0 && !mbar_wait(&bars->done, 0, abort_flag, false) && !*abort_flag) fail();
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS<G>));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS<G, PAIR>));
     // ---------------- promotion + epilogue ----------------
     const int ew = warp - EPI_WARP0;
     const int wg = ew >> 2;                 // column half of the tile
@@ -623,12 +763,12 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
     float* cbuf = colbuf + ew * 2 * C::CB_F;
     uint32_t acc_it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
       int local, mt, nt;
       const int g = problem_of(kp, tile, local);
       const DevArgs& p = kp.p[g];
       tile_coords(p, local, mt, nt);
-      const int wrow0 = mt * BM + lq * 32;   // first tile row of this warp
+      const int wrow0 = mt * TILE_M + (int)rank * BM + lq * 32;   // first tile row of this warp
       const int row = wrow0 + lane;          // the row whose sA this lane fetches
       const int col0 = nt * BN + wg * EPI_COLS;
       const bool row_ok = row < p.R;
@@ -716,7 +856,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
           sb_r[SL] = load_sb(kb + 2);
         }
         bool good = mbar_wait(&bars->tfull[b], bph, abort_flag, true);
-        if (!good) record_abort(abort_flag, kp.p[0].err);
+        if (!good) fail();
         if (__any_sync(0xffffffffu, !good)) return false;
         tc_fence_after();
         const uint32_t tbase = taddr_w + b * BN;
@@ -729,7 +869,11 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
         auto release = [&]() {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->tempty[b]);
+          if (lane == 0) {
+            // (a pair: on the leader's barrier, addressed through the cluster)
+            if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->tempty[b]), 0));
+            else mbar_arrive(&bars->tempty[b]);
+          }
         };
         if (COLS) {
           // fragments i = 2·cq + h: columns 32cq.., lanes 16h..
@@ -849,7 +993,7 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
         // quantiser applied to the bf16 output.
         uint8_t* ob = outbuf + ew * OUT_CHUNK_BYTES;
         uint8_t* qb = reinterpret_cast<uint8_t*>(colbuf) + ew * 1024;
-        const bool fuse_q = EPI_COLS == 128 && p.out_q != nullptr;
+        const bool fuse_q = !PAIR && EPI_COLS == 128 && p.out_q != nullptr;
         GroupScale gq{};
         if (fuse_q) {
           float amax = 0.0f;
@@ -902,441 +1046,40 @@ k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
   }
 
   // ---------------- teardown ----------------
+  // (a pair: neither CTA leaves, or frees TMEM, while the pair's MMAs could
+  // still read its shared memory or its TMEM is still being read)
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    __syncwarp();
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(C::TMEM_ALLOC));
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_ALLOC));
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(C::TMEM_ALLOC));
   }
 }
 
-// ===========================================================================
-// CTA-pair variant (tcgen05 cta_group::2).  A cluster of two CTAs on two SMs
-// computes a 256-row × 128-column tile: each CTA loads its own 128 rows of A
-// and one half (64 rows) of the tile's B, the leader CTA (rank 0) issues
-// M = 256, N = 128 MMAs that read both CTAs' shared memory, and each CTA's
-// TMEM receives its own 128 rows.  Per SM that is the shared-memory traffic
-// per FLOP of a 128 × 256 single-CTA tile, with half the accumulator: four
-// 128-column TMEM accumulators instead of two, so the tensor core can run
-// three blocks ahead of the promotion, and a promotion warp (32 rows × 64
-// columns) takes a block's whole partial from TMEM with one wait.
-//   barriers: the leader's full[s] collects both CTAs' TMA bytes (the copies
-//   of the peer CTA signal it across the pair); the MMA commits arrive on
-//   empty[s], tfull[b] and done in both CTAs (multicast); both CTAs'
-//   promotion warps release an accumulator on the leader's tempty[b].
-// ===========================================================================
-constexpr int PBN = 128;                                  // pair-tile columns
-constexpr int P_STAGES = 8;
-constexpr int P_A_BYTES = BM * BK, P_B_BYTES = (PBN / 2) * BK;
-constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;      // per CTA
-constexpr int P_ACC_BUFS = 4;
-constexpr int P_EPI_COLS = PBN / 2, P_CHUNKS = P_EPI_COLS / 32;
-constexpr int P_GS = P_EPI_COLS / 4 + 4, P_CB_F = 32 + 4 * P_GS;
-constexpr int P_COLBUF_BYTES = EPI_WARPS * 2 * P_CB_F * 4;
-constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 1024 + P_COLBUF_BYTES + EPI_WARPS * OUT_CHUNK_BYTES;
-// D = F32, A = B = E4M3, both K-major, N = 128, M = 256
-constexpr uint32_t P_IDESC = (1u << 4) | ((uint32_t)(PBN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
-static_assert(P_SMEM_BYTES <= 232448, "shared memory");
-static_assert(P_STAGE_BYTES % 1024 == 0 && P_COLBUF_BYTES % 128 == 0, "alignment");
-static_assert(P_STAGES <= MAX_STAGES && P_ACC_BUFS <= MAX_BUFS, "barrier arrays");
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// The address of the same shared variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-// Relaxed arrives hand an accumulator back: the TMEM loads they follow have
-// completed (tcgen05.wait::ld) and nothing else needs ordering, so the arrive
-// does not wait for the thread's other memory operations in flight.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
-// TMA load into this CTA's shared memory whose completion is counted on a
-// barrier of either CTA of the pair.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
-                                                 int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(map), "r"(bar_cluster), "r"(x), "r"(y)
-      : "memory");
-}
-__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %3, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %4, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(accumulate), "r"(P_IDESC));
-}
-// Arrives once on the barrier at this shared-memory offset in both CTAs when
-// the MMAs issued so far have completed.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"((uint16_t)3)
-      : "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+template <int BN_, bool COLS, int G>
+__global__ void __launch_bounds__(THREADS, 1)
+k_gemm_e4m3_blockscaled(const __grid_constant__ KParams<G> kp) {
+  gemm_body<BN_, COLS, G, false>(kp);
 }
 
+// CTA pairs: 256 × 256 tiles over two SMs.  Per SM that is the MMA work of a
+// 128 × 256 tile with half of its B operand loaded into (and read from)
+// shared memory, the resource that bounds the single-CTA kernel.
 template <bool COLS, int G>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 k_gemm_e4m3_blockscaled_pair(const __grid_constant__ KParams<G> kp) {
-  using CsVec = typename ColScaleVec<P_EPI_COLS>::T;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + P_STAGES * P_STAGE_BYTES);
-  float* colbuf = reinterpret_cast<float*>(smem + P_STAGES * P_STAGE_BYTES + 1024);
-  uint8_t* outbuf = smem + P_STAGES * P_STAGE_BYTES + 1024 + P_COLBUF_BYTES;
-  volatile int* abort_flag = &bars->abort_flag;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-  const int num_tiles = kp.tile_end[G - 1];
-  // sets this CTA's abort flag and the peer's, and records the error word
-  auto abort_pair = [&]() {
-    *abort_flag = 1;
-    st_cluster_u32(mapa_shared(smem_u32((const void*)&bars->abort_flag), rank ^ 1u), 1u);
-    atomicOr(kp.p[0].err, kErrTimeout);
-  };
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < P_STAGES; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
-    }
-    for (int b = 0; b < P_ACC_BUFS; ++b) {
-      mbar_init(&bars->tfull[b], 1);
-      mbar_init(&bars->tempty[b], 2 * EPI_WARPS);
-    }
-    mbar_init(&bars->done, 1);
-    bars->abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 1) {
-    // one warp of each CTA of the pair allocates, collectively, the same columns in both
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&bars->tmem_base)),
-                 "r"(TMEM_COLS));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
-  }
-  tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();   // both CTAs' barriers are initialised before either CTA signals the other's
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-
-  if (warp < EPI_WARP0) {
-    // (the producer tracks the pair's barriers: the larger control share)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS<2>));
-    if (warp == 0 && lane == 0) {
-      // ---------------- TMA producer (both CTAs) ----------------
-      const uint32_t full_leader0 = mapa_shared(smem_u32(&bars->full[0]), 0);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
-        int local, mt, nt;
-        const int g = problem_of(kp, tile, local);
-        tile_coords(kp.p[g], local, mt, nt);
-        const int nkb = kp.p[g].nKB;
-        const CUtensorMap* mA = &kp.tmA[g];
-        const CUtensorMap* mB = &kp.tmB[g];
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const uint32_t s = it % P_STAGES, ph = (it / P_STAGES) & 1u;
-          if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort_flag, true)) {
-            abort_pair();
-            ok = false;
-            break;
-          }
-          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&bars->full[s]), 2 * P_STAGE_BYTES);
-          const uint32_t st = smem_u32(smem + s * P_STAGE_BYTES);
-          tma_load_2d_pair(st, mA, full_leader0 + 8 * s, kb * BK, mt * 2 * BM + (int)rank * BM);
-          tma_load_2d_pair(st + P_A_BYTES, mB, full_leader0 + 8 * s, kb * BK, nt * PBN + (int)rank * (PBN / 2));
-        }
-      }
-      // the leader sees every copy of both CTAs land on its barriers before the pair exits
-      if (rank == 0) {
-        const uint32_t first = it > (uint32_t)P_STAGES ? it - P_STAGES : 0u;
-        for (uint32_t j = first; j < it; ++j)
-          mbar_wait(&bars->full[j % P_STAGES], (j / P_STAGES) & 1u, abort_flag, false);
-      }
-    } else if (warp == 1 && lane == 0) {
-      if (rank == 0) {
-        // ---------------- MMA issuer (leader) ----------------
-        uint32_t it = 0, acc_it = 0;
-        bool ok = true;
-        for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
-          int local;
-          const int nkb = kp.p[problem_of(kp, tile, local)].nKB;
-          for (int kb = 0; kb < nkb; ++kb, ++it, ++acc_it) {
-            const uint32_t s = it % P_STAGES, ph = (it / P_STAGES) & 1u;
-            const uint32_t b = acc_it % P_ACC_BUFS, bph = (acc_it / P_ACC_BUFS) & 1u;
-            if (!mbar_wait(&bars->tempty[b], bph ^ 1u, abort_flag, true) ||
-                !mbar_wait(&bars->full[s], ph, abort_flag, true)) {
-              abort_pair();
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + s * P_STAGE_BYTES);
-            const uint32_t b_addr = a_addr + P_A_BYTES;
-#pragma unroll
-            for (int k = 0; k < BK / 32; ++k)
-              umma_e4m3_pair(tmem + b * PBN, sdesc_sw128(a_addr + 32 * k), sdesc_sw128(b_addr + 32 * k),
-                             k > 0 ? 1u : 0u);
-            umma_commit_pair(&bars->empty[s]);
-            umma_commit_pair(&bars->tfull[b]);
-          }
-        }
-        umma_commit_pair(&bars->done);
-      }
-      // both CTAs: every MMA has completed before TMEM is released
-      if (!mbar_wait(&bars->done, 0, abort_flag, false) && !*abort_flag) abort_pair();
-    }
-  } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS<2>));
-    // ---------------- promotion + epilogue (both CTAs) ----------------
-    const int ew = warp - EPI_WARP0;
-    const int wg = ew >> 2;
-    const int lq = warp & 3;
-    const uint32_t taddr_w = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(wg * P_EPI_COLS);
-    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&bars->tempty[0]), 0);
-    float* cbuf = colbuf + ew * 2 * P_CB_F;
-    uint32_t acc_it = 0;
-    bool ok = true;
-    for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
-      int local, mt, nt;
-      const int g = problem_of(kp, tile, local);
-      const DevArgs& p = kp.p[g];
-      tile_coords(p, local, mt, nt);
-      const int wrow0 = mt * 2 * BM + (int)rank * BM + lq * 32;
-      const int row = wrow0 + lane;
-      const int col0 = nt * PBN + wg * P_EPI_COLS;
-      const bool row_ok = row < p.R;
-      const int nkb = p.nKB;
-      const float* sa_ptr = p.sA + row;
-      const float* sb_ptr = p.sB + (COLS ? (long long)col0 : (long long)(col0 / 128) * p.sb_j);
-      auto load_sa = [&](int kb) { return (row_ok && kb < nkb) ? __ldg(sa_ptr + (long long)kb * p.ld_sA) : 0.0f; };
-      auto load_sb = [&](int kb) { return kb < nkb ? __ldg(sb_ptr + (long long)kb * p.sb_k) : 0.0f; };
-      auto load_cs = [&](int kb) {
-        CsVec v;
-        if (kb < nkb) v = __ldg(reinterpret_cast<const CsVec*>(sb_ptr + (long long)kb * p.sb_k) + lane);
-        else memset(&v, 0, sizeof(v));
-        return v;
-      };
-      float sa_r[2], sb_r[2];
-      CsVec cs_r[2];
-      sa_r[0] = load_sa(0);
-      sa_r[1] = load_sa(1);
-      if (COLS) {
-        cs_r[0] = load_cs(0);
-        cs_r[1] = load_cs(1);
-      } else {
-        sb_r[0] = load_sb(0);
-        sb_r[1] = load_sb(1);
-      }
-      uint64_t acc[P_CHUNKS][16];
-#pragma unroll
-      for (int c = 0; c < P_CHUNKS; ++c)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[c][j] = 0ull;
-
-      auto block = [&](int kb, auto slot) -> bool {
-        constexpr int SL = decltype(slot)::value;
-        const uint32_t b = acc_it % P_ACC_BUFS, bph = (acc_it / P_ACC_BUFS) & 1u;
-        ++acc_it;
-        uint64_t s2u = 0;
-        uint64_t sb[COLS ? P_CHUNKS : 1][4];
-        float sa_raw[4];
-        if (COLS) {
-          float* cb = cbuf + SL * P_CB_F;
-          cb[lane] = sa_r[SL];
-          // columns 2l, 2l+1 of the warp's 64: group l mod 4 at 2j = 2(l/4)
-          *reinterpret_cast<float2*>(cb + 32 + (lane & 3) * P_GS + 2 * (lane >> 2)) =
-              *reinterpret_cast<const float2*>(&cs_r[SL]);
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sa_raw[i] = cb[(lane >> 2) + 8 * i];
-          const ulonglong2* cs = reinterpret_cast<const ulonglong2*>(cb + 32 + (lane & 3) * P_GS);
-#pragma unroll
-          for (int cq = 0; cq < (COLS ? P_CHUNKS : 1); ++cq) {
-            const ulonglong2 v0 = cs[2 * cq], v1 = cs[2 * cq + 1];
-            sb[cq][0] = v0.x;
-            sb[cq][1] = v0.y;
-            sb[cq][2] = v1.x;
-            sb[cq][3] = v1.y;
-          }
-        } else {
-          const float sc = sa_r[SL] * sb_r[SL];
-          s2u = pack2(sc, sc);
-        }
-        // the scales of block kb + 2 are fetched after this block's
-        // accumulator is handed back, so the hand-off never waits for them
-        auto prefetch = [&]() {
-          sa_r[SL] = load_sa(kb + 2);
-          if (COLS) cs_r[SL] = load_cs(kb + 2);
-          else sb_r[SL] = load_sb(kb + 2);
-        };
-        bool good = mbar_wait(&bars->tfull[b], bph, abort_flag, true);
-        if (!good) abort_pair();
-        if (__any_sync(0xffffffffu, !good)) return false;
-        tc_fence_after();
-        const uint32_t tbase = taddr_w + b * PBN;
-        // the whole partial of the warp's 32 rows × 64 columns in one go, then
-        // the accumulator goes back to the leader's MMA
-        auto release = [&]() {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if (rank == 0) mbar_arrive_relaxed(&bars->tempty[b]);
-            else mbar_arrive_cluster(tempty_leader0 + 8 * b);
-          }
-        };
-        if (COLS) {
-          uint32_t r[4][16];   // fragments i = 2·cq + h: columns 32cq.., lanes 16h..
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tmem_ld16x256_x4(tbase + ((uint32_t)(16 * (i & 1)) << 16) + 32 * (i >> 1), r[i]);
-          tmem_wait_ld16(r[0]);
-          tmem_tie16(r[1]);
-          tmem_tie16(r[2]);
-          tmem_tie16(r[3]);
-          release();
-          prefetch();
-          const uint64_t sal0 = pack2(sa_raw[0], sa_raw[0]), sah0 = pack2(sa_raw[1], sa_raw[1]);
-          const uint64_t sal1 = pack2(sa_raw[2], sa_raw[2]), sah1 = pack2(sa_raw[3], sa_raw[3]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            promote_cols_frag(&acc[i >> 1][8 * (i & 1)], r[i], sb[i >> 1], (i & 1) ? sal1 : sal0,
-                              (i & 1) ? sah1 : sah0);
-        } else {
-          uint32_t cur[2][32];
-          tmem_ld32_async(tbase, cur[0]);
-          tmem_ld32_async(tbase + 32, cur[1]);
-          tmem_wait_ld(cur[0]);
-          tmem_tie32(cur[1]);
-          release();
-          prefetch();
-          fma32_uniform(acc[0], cur[0], s2u);
-          fma32_uniform(acc[1], cur[1], s2u);
-        }
-        return true;
-      };
-      for (int kb = 0; kb < nkb; kb += 2) {
-        if (!block(kb, std::integral_constant<int, 0>{}) ||
-            (kb + 1 < nkb && !block(kb + 1, std::integral_constant<int, 1>{}))) {
-          ok = false;
-          break;
-        }
-      }
-      if (!ok) break;
-      if (COLS) {
-        const int g2 = 2 * (lane & 3);
-        if (p.out_fp32) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int rs = 0; rs < 2; ++rs) {
-              const int r = wrow0 + (lane >> 2) + 8 * rs + 16 * h;
-              if (r < p.R) {
-                float* o = static_cast<float*>(p.out) + (size_t)r * p.C + col0 + g2;
-#pragma unroll
-                for (int cq = 0; cq < P_CHUNKS; ++cq)
-#pragma unroll
-                  for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<float2*>(o + 32 * cq + 8 * j) = unpack2(acc[cq][8 * h + 2 * j + rs]);
-              }
-            }
-        } else {
-          uint8_t* ob = outbuf + ew * OUT_CHUNK_BYTES;
-#pragma unroll
-          for (int cq = 0; cq < P_CHUNKS; ++cq) {
-            if (lane == 0) tma_store_wait_read();
-            __syncwarp();
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int rs = 0; rs < 2; ++rs)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const float2 v = unpack2(acc[cq][8 * h + 2 * j + rs]);
-                  *reinterpret_cast<uint32_t*>(ob + ((lane >> 2) + 8 * rs + 16 * h) * 64 +
-                                               16 * (j ^ ((lane >> 3) & 3)) + 2 * g2) = f2_to_bf2(v.x, v.y);
-                }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && wrow0 < p.R) tma_store_2d(&kp.tmOut[g], smem_u32(ob), col0 + cq * 32, wrow0);
-          }
-        }
-      } else if (p.out_fp32) {
-        if (row_ok) {
-          float* o = static_cast<float*>(p.out) + (size_t)row * p.C + col0;
-#pragma unroll
-          for (int c = 0; c < P_CHUNKS; ++c)
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-              const float2 a = unpack2(acc[c][j]), bq = unpack2(acc[c][j + 1]);
-              *reinterpret_cast<float4*>(o + c * 32 + 2 * j) = make_float4(a.x, a.y, bq.x, bq.y);
-            }
-        }
-      } else {
-        uint8_t* ob = outbuf + ew * OUT_CHUNK_BYTES;
-#pragma unroll
-        for (int c = 0; c < P_CHUNKS; ++c) {
-          if (lane == 0) tma_store_wait_read();
-          __syncwarp();
-          uint4* dst = reinterpret_cast<uint4*>(ob + lane * 64);
-          uint32_t yb[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float2 v = unpack2(acc[c][j]);
-            yb[j] = f2_to_bf2(v.x, v.y);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            dst[(j / 4) ^ ((lane >> 1) & 3)] = make_uint4(yb[j], yb[j + 1], yb[j + 2], yb[j + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && wrow0 < p.R) tma_store_2d(&kp.tmOut[g], smem_u32(ob), col0 + c * 32, wrow0);
-        }
-      }
-    }
-    if (lane == 0) tma_store_wait_all();
-  }
-
-  // ---------------- teardown ----------------
-  // neither CTA leaves (or frees TMEM) while the pair's MMAs could still read
-  // its shared memory or its TMEM is still being read
-  tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
-  }
+  gemm_body<256, COLS, G, true>(kp);
 }
-
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -1446,9 +1189,10 @@ cudaError_t launch_cfg(const GemmArgs* a, int count, int dev, cudaStream_t st) {
 }
 
 
-// CTA-pair launch: 256 × 128 tiles (see k_gemm_e4m3_blockscaled_pair).
+// CTA-pair launch: 256 × 256 tiles (see k_gemm_e4m3_blockscaled_pair).
 template <bool COLS, int G>
 cudaError_t launch_pair(const GemmArgs* a, int count, int dev, cudaStream_t st) {
+  using C = Cfg<256, true>;
   auto kern = k_gemm_e4m3_blockscaled_pair<COLS, G>;
   static int ready[64] = {0};   // 0 = unchecked, 1 = ok, -1 = unusable
   if (ready[dev] == 0) {
@@ -1458,7 +1202,7 @@ cudaError_t launch_pair(const GemmArgs* a, int count, int dev, cudaStream_t st) 
     if (fa.numRegs != LAUNCH_REGS) {
       ready[dev] = -1;
     } else {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
       if (e != cudaSuccess) return e;
       ready[dev] = 1;
     }
@@ -1480,9 +1224,9 @@ cudaError_t launch_pair(const GemmArgs* a, int count, int dev, cudaStream_t st) 
       continue;
     }
     const GemmArgs& x = a[g];
-    if (x.out_q != nullptr || x.drop_kb >= 0 || x.C % PBN != 0) return cudaErrorInvalidValue;
+    if (x.out_q != nullptr || x.drop_kb >= 0 || x.C % C::BN != 0) return cudaErrorInvalidValue;
     if (!make_map(&kp.tmA[g], x.A, (uint64_t)x.Kc, (uint64_t)x.R, BM) ||
-        !make_map(&kp.tmB[g], x.B, (uint64_t)x.Kc, (uint64_t)x.C, PBN / 2))
+        !make_map(&kp.tmB[g], x.B, (uint64_t)x.Kc, (uint64_t)x.C, C::BN / 2))
       return cudaErrorInvalidValue;
     if (x.out_fp32 || x.out == nullptr) {
       kp.tmOut[g] = kp.tmA[g];
@@ -1500,7 +1244,7 @@ cudaError_t launch_pair(const GemmArgs* a, int count, int dev, cudaStream_t st) 
     d.C = (int)x.C;
     d.nKB = (int)(x.Kc / BK);
     d.tiles_m = (int)((x.R + 2 * BM - 1) / (2 * BM));
-    d.tiles_n = (int)(x.C / PBN);
+    d.tiles_n = (int)(x.C / C::BN);
     d.m_fastest = x.R <= x.C ? 1 : 0;
     d.out_fp32 = x.out_fp32 ? 1 : 0;
     d.err = err;
@@ -1512,21 +1256,22 @@ cudaError_t launch_pair(const GemmArgs* a, int count, int dev, cudaStream_t st) 
   if (tiles == 0) return cudaSuccess;
   const int pairs = num_sms() / 2;
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  kern<<<grid, THREADS, P_SMEM_BYTES, st>>>(kp);
+  kern<<<grid, THREADS, C::SMEM_BYTES, st>>>(kp);
   return cudaGetLastError();
 }
 
-// Kernel choice.  The single-CTA kernel runs every GEMM by default: on
-// GB300 a cta_group::2 MMA of M = 256, N = 128 keeps each SM's tensor core
-// busy about as long per instruction as an M = 128, N = 256 one, so pair
-// tiles halve the work per block at nearly the same block time (measured:
-// 8192 x 28672 x 4096 FProp 1280 vs 2542 TFLOP/s, WGrad 1106 vs 1825).
+// Kernel choice.  The single-CTA kernel runs every GEMM by default.  CTA
+// pairs load half as much of B per SM, but on GB300 that does not raise the
+// rate: with the promotion removed (a timing-only variant) both kernels run
+// the 8192 x 28672 x 4096 FProp at about 2900 TFLOP/s, and with it the pair
+// is slower (1950 vs 2400 FProp, 1680 vs 1880 WGrad), because each 256-column
+// accumulator is handed back only when both CTAs have promoted it.
 // g_gemm_path = 2 runs every GEMM the pair kernel can take on CTA pairs
 // (testing and diagnosis); every output element's arithmetic (its MMA
 // blocks, promotion order and rounding) is the same on either kernel.
 int g_gemm_path = 0;
 bool pair_possible(const GemmArgs& a) {
-  return a.out_q == nullptr && a.drop_kb < 0 && a.C % PBN == 0 && a.R >= 2 * BM;
+  return a.out_q == nullptr && a.drop_kb < 0 && a.C % 256 == 0 && a.R >= 2 * BM;
 }
 bool use_pair(const GemmArgs& a) { return g_gemm_path == 2 && pair_possible(a); }
 

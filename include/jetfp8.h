@@ -214,8 +214,8 @@ jetfp8_status jetfp8_test_gemm_fprop_drop_block(const uint8_t* xq, const float* 
 /* Test and diagnosis knob (no counterpart on the pages).  Chooses the kernel
  * of later GEMM launches of this process: 0 (the default) and 1 run every
  * GEMM on single-CTA tiles, 2 runs every GEMM that allows it (at least 256
- * rows of output, output width a multiple of 128, no fused output quantiser)
- * on CTA-pair tiles (tcgen05 cta_group::2, 256 x 128 per pair), which are
+ * rows of output, output width a multiple of 256, no fused output quantiser)
+ * on CTA-pair tiles (tcgen05 cta_group::2, 256 x 256 per pair), which are
  * slower on GB300 and therefore not chosen by default.  Every output
  * element's arithmetic is the same on either kernel, so the results are
  * identical bit for bit; the knob lets tests check that.  Not synchronised with launches
