@@ -219,7 +219,9 @@ def oracle_sample_step(lins, seed=0):
 
 
 def blas_threads():
-    """Threads the oracle's BLAS calls may use (the numpy matmuls)."""
+    """Threads the oracle's BLAS calls may use (the numpy matmuls): from
+    threadpoolctl where it is installed, else from the thread-count variables
+    the BLAS libraries read, else their default of one thread per usable core."""
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
@@ -227,7 +229,11 @@ def blas_threads():
             return int(max(n))
     except Exception:
         pass
-    return None
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var, "").strip()
+        if v.isdigit() and int(v) > 0:
+            return int(v)
+    return host_cores()
 
 
 def host_cores():
