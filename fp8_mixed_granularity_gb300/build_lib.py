@@ -23,7 +23,7 @@ STAMP = os.path.join(BUILD_DIR, "libjetfp8.stamp")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-Xptxas", "-warn-spills", f"-I{INCLUDE}"]
-SOURCES = ["jetfp8_api.cu", "quant_kernels.cu", "gemm_tcgen05.cu"]
+SOURCES = ["jetfp8_api.cu", "quant_kernels.cu", "gemm_tcgen05.cu", "nvfp4.cu"]
 
 
 def _nvcc() -> str:

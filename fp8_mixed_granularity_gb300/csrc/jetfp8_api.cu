@@ -80,6 +80,10 @@ struct Check {
     if (st == JETFP8_OK && v <= 0) st = JETFP8_ERR_INVALID_ARG;
     return *this;
   }
+  Check& mult(int64_t v, int64_t m) {
+    if (st == JETFP8_OK && (v <= 0 || v % m != 0)) st = (v <= 0) ? JETFP8_ERR_INVALID_ARG : JETFP8_ERR_UNSUPPORTED_SHAPE;
+    return *this;
+  }
   Check& mult128(int64_t v) {
     if (st == JETFP8_OK && (v <= 0 || v % 128 != 0)) st = (v <= 0) ? JETFP8_ERR_INVALID_ARG : JETFP8_ERR_UNSUPPORTED_SHAPE;
     return *this;
@@ -432,6 +436,31 @@ jetfp8_status jetfp8_test_set_gemm_path(int mode) {
   if (mode < 0 || mode > 2) return JETFP8_ERR_INVALID_ARG;
   set_gemm_path(mode);
   return JETFP8_OK;
+}
+
+size_t jetfp8_nvfp4_scale_bytes(int64_t R, int64_t K) {
+  if (R <= 0 || K <= 0 || K % 64 != 0) return 0;
+  return nvfp4_scale_bytes(R, K);
+}
+
+jetfp8_status jetfp8_quant_nvfp4(const void* x_bf16, int64_t R, int64_t K, uint8_t* q, uint8_t* sf,
+                                 float* g, cudaStream_t stream) {
+  log_call("jetfp8_quant_nvfp4", R, K);
+  Check c;
+  c.bf(x_bf16).ptr(q).ptr(sf).ptr(g).positive(R).mult(K, 64).fits(R, K).device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_quant_nvfp4(x_bf16, R, K, q, sf, g, stream));
+}
+
+jetfp8_status jetfp8_gemm_fprop_nvfp4(const uint8_t* xq, const uint8_t* xsf, const float* gx,
+                                      const uint8_t* wq, const uint8_t* wsf, const float* gw, int64_t M,
+                                      int64_t N, int64_t K, void* y_bf16, cudaStream_t stream) {
+  log_call("jetfp8_gemm_fprop_nvfp4", M, N, K);
+  Check c;
+  c.ptr(xq).ptr(xsf).ptr(gx).ptr(wq).ptr(wsf).ptr(gw).ptr(y_bf16).positive(M).mult(N, 256).mult(K, 256)
+      .fits(M, K).fits(N, K).fits(M, N).device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_gemm_nvfp4(xq, xsf, gx, wq, wsf, gw, M, N, K, y_bf16, stream));
 }
 
 size_t jetfp8_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H) {

@@ -64,4 +64,13 @@ void set_gemm_path(int mode);
 // problem's output equals that of its own launch_gemm, bit for bit.
 cudaError_t launch_gemm_grouped(const GemmArgs* a, int count, cudaStream_t st);
 
+// FP4 variant (NVFP4-style E2M1 codes, E4M3 scales per 16 elements in the
+// blocked layout, FP32 row scales; nvfp4.cu).
+size_t nvfp4_scale_bytes(int64_t R, int64_t K);
+cudaError_t launch_quant_nvfp4(const void* x, int64_t R, int64_t K, uint8_t* q, uint8_t* sf, float* g,
+                               cudaStream_t st);
+cudaError_t launch_gemm_nvfp4(const uint8_t* xq, const uint8_t* xsf, const float* gx, const uint8_t* wq,
+                              const uint8_t* wsf, const float* gw, int64_t M, int64_t N, int64_t K, void* y,
+                              cudaStream_t st);
+
 }  // namespace jetfp8

@@ -49,6 +49,8 @@ SIGNATURES = {
     "jetfp8_swiglu_bwd": [_P, _P, _I64, _I64, _P, _P],
     "jetfp8_get_last_device_error": [_P],
     "jetfp8_test_set_gemm_path": [_INT],
+    "jetfp8_quant_nvfp4": [_P, _I64, _I64, _P, _P, _P, _P],
+    "jetfp8_gemm_fprop_nvfp4": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P],
 }
 
 
@@ -74,6 +76,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.jetfp8_status_string.restype = ctypes.c_char_p
         lib.jetfp8_rmsnorm_bwd_workspace_bytes.argtypes = [_I64, _I64]
         lib.jetfp8_rmsnorm_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.jetfp8_nvfp4_scale_bytes.argtypes = [_I64, _I64]
+        lib.jetfp8_nvfp4_scale_bytes.restype = ctypes.c_size_t
         _lib = lib
     return _lib
 
@@ -306,6 +310,39 @@ def jetfp8_get_last_device_error(stream=None):
 # ---------------------------------------------------------------------------
 # Allocation helpers (torch.empty on the device; no computation)
 # ---------------------------------------------------------------------------
+def jetfp8_nvfp4_scale_bytes(R: int, K: int) -> int:
+    return int(load_library().jetfp8_nvfp4_scale_bytes(R, K))
+
+
+def jetfp8_quant_nvfp4(x, q, sf, g, stream=None):
+    """FP4 variant: bf16 rows x [R, K] -> codes q uint8 [R, K/2], block scales sf
+    uint8 [jetfp8_nvfp4_scale_bytes(R, K)] (blocked layout), row scales g float32 [R]."""
+    R, K = x.shape
+    _check(load_library().jetfp8_quant_nvfp4(
+        _ptr(x, _BF, None, "x"), R, K, _ptr(q, _U8, (R, K // 2), "q"),
+        _ptr(sf, _U8, (jetfp8_nvfp4_scale_bytes(R, K),), "sf"), _ptr(g, _F, (R,), "g"), _stream(stream)),
+        "jetfp8_quant_nvfp4")
+
+
+def jetfp8_gemm_fprop_nvfp4(xq, xsf, gx, wq, wsf, gw, y, stream=None):
+    """FP4 variant FProp: y bf16 [M, N] from jetfp8_quant_nvfp4 of X [M, K] and W [N, K]."""
+    M, K2 = xq.shape
+    N = wq.shape[0]
+    K = 2 * K2
+    _check(load_library().jetfp8_gemm_fprop_nvfp4(
+        _ptr(xq, _U8, None, "xq"), _ptr(xsf, _U8, (jetfp8_nvfp4_scale_bytes(M, K),), "xsf"),
+        _ptr(gx, _F, (M,), "gx"), _ptr(wq, _U8, (N, K2), "wq"),
+        _ptr(wsf, _U8, (jetfp8_nvfp4_scale_bytes(N, K),), "wsf"), _ptr(gw, _F, (N,), "gw"), M, N, K,
+        _ptr(y, _BF, (M, N), "y"), _stream(stream)), "jetfp8_gemm_fprop_nvfp4")
+
+
+def empty_nvfp4(rows: int, cols: int, device) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(codes uint8 [rows, cols/2], block scales uint8 [scale bytes], row scales float32 [rows])"""
+    return (torch.empty(rows, cols // 2, dtype=torch.uint8, device=device),
+            torch.empty(jetfp8_nvfp4_scale_bytes(rows, cols), dtype=torch.uint8, device=device),
+            torch.empty(rows, dtype=torch.float32, device=device))
+
+
 def empty_rowgroup_quant(rows: int, cols: int, device) -> tuple[torch.Tensor, torch.Tensor]:
     """(q uint8 [rows, cols], S float32 [cols/128, roundup(rows,4)])"""
     return (torch.empty(rows, cols, dtype=_U8, device=device),

@@ -223,6 +223,54 @@ jetfp8_status jetfp8_test_gemm_fprop_drop_block(const uint8_t* xq, const float* 
  * other mode. */
 jetfp8_status jetfp8_test_set_gemm_path(int mode);
 
+/* ---------------------------------------------------------------------------
+ * FP4 variant of the precision flow (next row N4).  The digest names carrying
+ * the unified precision flow to FP4 on Blackwell as future work ([digest]
+ * 未来方向, item (1)) and defines no FP4 format; this variant keeps the flow's
+ * property that a token's forward result does not depend on its batch
+ * ([summary] Figure 5), on the NVFP4-style format the tensor cores scale in
+ * hardware (tcgen05.mma kind::mxf4nvf4, block scales applied by the MMA):
+ *   codes  E2M1 (sign, 2 exponent bits, 1 mantissa bit; magnitudes 0, 0.5, 1,
+ *          1.5, 2, 3, 4, 6), two per byte, element 2i in the low nibble:
+ *          uint8 [R, K/2], row-major;
+ *   block scales  one E4M3 code per 16 consecutive elements of a row, in the
+ *          blocked layout: byte ((r/128·K/64 + b/4)·32 + r mod 32)·16 +
+ *          ((r/32) mod 4)·4 + b mod 4 for row r, block b (512-byte atoms of
+ *          128 rows × 64 elements); jetfp8_nvfp4_scale_bytes(R, K) bytes,
+ *          rows past R inside the last atom carry zero scales;
+ *   row scales  FP32 [R], one per row (token of X, output channel of W).
+ * Rule, every step one correctly rounded FP32 operation:
+ *   g = amax_row/2688 (1 if the row is zero), h = 6·g,
+ *   s_b = E4M3(amax_b/h) (round to nearest even, saturating at 448),
+ *   d_b = s_b·g,  q = E2M1(x/d_b) (nearest even, saturating at ±6; a zero
+ *   with the sign of x when d_b = 0).
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of the block-scale array for R rows of K elements (K a multiple of
+ * 64): ceil(R/128)·(K/64)·512; 0 for invalid sizes. */
+size_t jetfp8_nvfp4_scale_bytes(int64_t R, int64_t K);
+
+/* Quantise the bf16 rows x [R, K] (K a multiple of 64; 32-byte aligned) to the
+ * FP4 variant: codes q [R, K/2], block scales sf (blocked layout above) and row
+ * scales g [R] (all 16-byte aligned, caller-owned; the call writes every byte
+ * of q, sf and g, padding-row scales included).  A row's result depends only
+ * on that row.  Errors: JETFP8_ERR_INVALID_ARG (null pointer, R <= 0),
+ * JETFP8_ERR_UNSUPPORTED_SHAPE (K not a multiple of 64, or too large),
+ * JETFP8_ERR_MISALIGNED, JETFP8_ERR_CUDA / JETFP8_ERR_UNSUPPORTED (no sm_103 device). */
+jetfp8_status jetfp8_quant_nvfp4(const void* x_bf16, int64_t R, int64_t K, uint8_t* q, uint8_t* sf,
+                                 float* g, cudaStream_t stream);
+
+/* FP4 forward GEMM  Y[m,n] = bf16(RN(RN(D[m,n]·gx[m])·gw[n])),
+ *   D[m,n] = Σ_k dec(xq[m,k])·dec(xsf[m,k/16])·dec(wq[n,k])·dec(wsf[n,k/16]),
+ * accumulated in FP32 by the tensor core (block scales applied in the MMA).
+ * xq [M, K/2], xsf, gx [M] from jetfp8_quant_nvfp4 of X; wq [N, K/2], wsf, gw [N]
+ * from jetfp8_quant_nvfp4 of W; y bf16 [M, N] (caller-owned, 16-byte aligned).
+ * N and K multiples of 256.  Errors as jetfp8_quant_nvfp4; a device-side
+ * timeout is reported by jetfp8_get_last_device_error. */
+jetfp8_status jetfp8_gemm_fprop_nvfp4(const uint8_t* xq, const uint8_t* xsf, const float* gx,
+                                      const uint8_t* wq, const uint8_t* wsf, const float* gw, int64_t M,
+                                      int64_t N, int64_t K, void* y_bf16, cudaStream_t stream);
+
 /* Set the environment variable JETFP8_LOG (to anything but "" or "0") and every
  * entry point prints its name and sizes to stderr when called. */
 

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_binding_covers_every_declared_symbol():
     from fp8_mixed_granularity_gb300 import jetfp8
     # entry points that return something other than a status are bound apart
-    not_status = {"jetfp8_status_string", "jetfp8_rmsnorm_bwd_workspace_bytes"}
+    not_status = {"jetfp8_status_string", "jetfp8_rmsnorm_bwd_workspace_bytes", "jetfp8_nvfp4_scale_bytes"}
     for name in _declared():
         if name not in not_status:
             assert name in jetfp8.SIGNATURES, name
@@ -118,6 +118,32 @@ def test_rmsnorm_bwd_many_row_chunks_validated(lib):
     ws = lib.jetfp8_rmsnorm_bwd_workspace_bytes(M, H)
     A = P(1 << 20)
     assert fn(A, A, A, A, M, H, A, A, A, SZ(ws), None) == 4         # JETFP8_ERR_CUDA, not a shape error
+
+
+def test_nvfp4_validation(lib):
+    """The FP4 entry points check shapes and pointers before the device; the
+    block-scale size follows the blocked layout (512-byte atoms of 128 rows ×
+    64 elements)."""
+    P, I64, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.jetfp8_nvfp4_scale_bytes.restype = SZ
+    lib.jetfp8_nvfp4_scale_bytes.argtypes = [I64, I64]
+    assert lib.jetfp8_nvfp4_scale_bytes(1, 64) == 512
+    assert lib.jetfp8_nvfp4_scale_bytes(128, 4096) == 64 * 512
+    assert lib.jetfp8_nvfp4_scale_bytes(129, 4096) == 2 * 64 * 512
+    assert lib.jetfp8_nvfp4_scale_bytes(128, 100) == 0
+    q = lib.jetfp8_quant_nvfp4
+    q.argtypes = [P, I64, I64, P, P, P, P]
+    assert q(None, 4, 64, P(64), P(64), P(64), None) == 1            # null input
+    assert q(P(64), 0, 64, P(64), P(64), P(64), None) == 1           # R <= 0
+    assert q(P(64), 4, 96, P(64), P(64), P(64), None) == 2           # K not a multiple of 64
+    assert q(P(48), 4, 64, P(64), P(64), P(64), None) == 3           # bf16 input needs 32 B
+    gm = lib.jetfp8_gemm_fprop_nvfp4
+    gm.argtypes = [P, P, P, P, P, P, I64, I64, I64, P, P]
+    A = P(64)
+    assert gm(A, A, A, A, A, A, 4, 384, 256, A, None) == 2           # N not a multiple of 256
+    assert gm(A, A, A, A, A, A, 4, 256, 320, A, None) == 2           # K not a multiple of 256
+    assert gm(A, A, A, A, A, A, 0, 256, 256, A, None) == 1           # M <= 0
+    assert gm(A, None, A, A, A, A, 4, 256, 256, A, None) == 1        # null block scales
 
 
 def test_grouped_wgrad_validation(lib):
