@@ -681,6 +681,40 @@ def mlp_config(torch, J, W, dev, peaks, steps, M=16384, H=4096, I=14336):
             "tflops": flops / (ms * 1e-3) / 1e12, "launches_per_step": 15}
 
 
+def nvfp4_config(torch, J, W, dev, peaks, steps, M=8192):
+    """The FP4 variant of the flow on the Llama-3.1-8B forward linears at M
+    tokens: the row quantiser of the activation and the block-scaled FProp of
+    each linear (weights quantised once, outside the timed launches), against
+    the FP4 dense peak taken as the measured bf16 burst figure times the
+    nominal FP4/BF16 ratio (13.5 / 2.25 = 6)."""
+    peak = 6.0 * peaks["bf16"]
+    res = {"peak_tflops": peak, "peak_note": f"6 x {peaks['source']} burst bf16 (nominal FP4/BF16 ratio), of {peaks['source']}"}
+    lins = {"qkv": (4096, 6144), "o": (4096, 4096), "gate_up": (4096, 28672), "down": (14336, 4096)}
+    per = {}
+    total_ms, total_flops = 0.0, 0.0
+    for name, (K, N) in lins.items():
+        x = W.device_activations(M, K, dev, seed=700)
+        w = W.device_normal((N, K), 0.02, dev, seed=701)
+        xq, xsf, gx = J.empty_nvfp4(M, K, dev)
+        wq, wsf, gw = J.empty_nvfp4(N, K, dev)
+        J.jetfp8_quant_nvfp4(w, wq, wsf, gw)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        qms = _events_ms(torch, lambda: J.jetfp8_quant_nvfp4(x, xq, xsf, gx), steps)
+        gms = _events_ms(torch, lambda: J.jetfp8_gemm_fprop_nvfp4(xq, xsf, gx, wq, wsf, gw, y), steps)
+        f = 2.0 * M * N * K
+        qbytes = M * K * (2 + 0.5 + 1 / 16) + 4 * M
+        per[name] = {"fprop_us": gms * 1e3, "fprop_tflops": f / (gms * 1e-3) / 1e12,
+                     "fprop_frac": f / (gms * 1e-3) / 1e12 / peak, "quant_us": qms * 1e3,
+                     "quant_gbs": qbytes / (qms * 1e-3) / 1e9}
+        total_ms += gms
+        total_flops += f
+        del x, w, xq, xsf, gx, wq, wsf, gw, y
+    res["per_linear"] = per
+    res["fprop_tflops_all"] = total_flops / (total_ms * 1e-3) / 1e12
+    res["tokens"] = M
+    return res
+
+
 def run_configs(args, torch, J, W, dev, peaks):
     steps = max(5, min(args.steps, 10))
     out = {"decode_qwen3_8b": decode_config(torch, J, W, dev, peaks)}
@@ -688,6 +722,8 @@ def run_configs(args, torch, J, W, dev, peaks):
     out["dense32b_training"] = b32_config(torch, J, W, dev, peaks, steps)
     torch.cuda.empty_cache()
     out["gated_mlp_chain"] = mlp_config(torch, J, W, dev, peaks, steps)
+    torch.cuda.empty_cache()
+    out["nvfp4_variant_fprop"] = nvfp4_config(torch, J, W, dev, peaks, steps)
     torch.cuda.empty_cache()
     J.jetfp8_get_last_device_error()
     return out
@@ -766,7 +802,8 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
 # ---------------------------------------------------------------------------
 CASES = {"fprop", "dgrad", "wgrad", "quant_act", "rmsnorm_quant", "quant_weight",
          "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd", "fprop_quant", "fprop_then_quant",
-         "rmsnorm_bwd", "decoder_layer", "wgrad_grouped", "wgrad_separate", "fp8_library_probe"}
+         "rmsnorm_bwd", "decoder_layer", "wgrad_grouped", "wgrad_separate", "fp8_library_probe",
+         "fprop_nvfp4", "quant_nvfp4"}
 
 
 def run_case(args):
@@ -848,6 +885,23 @@ def run_case(args):
         ws = torch.empty(J.jetfp8_rmsnorm_bwd_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
         fn = lambda: J.jetfp8_rmsnorm_bwd(x, gamma, rstd, dy, dx, dg, ws)  # noqa: E731
         _time_case(args, fn, M * K * QUANT_BYTES[args.case], "GB/s", [M, N, K])
+        return
+    if args.case in ("fprop_nvfp4", "quant_nvfp4"):
+        # FP4 variant: the row quantiser of X [M, K] (bf16 in; codes, block and
+        # row scales out), or the block-scaled FProp Y = X̂ Ŵᵀ [M, N]
+        x = W.device_activations(M, K, dev, seed=1)
+        xq, xsf, gx = J.empty_nvfp4(M, K, dev)
+        if args.case == "quant_nvfp4":
+            fn = lambda: J.jetfp8_quant_nvfp4(x, xq, xsf, gx)  # noqa: E731
+            _time_case(args, fn, M * K * (2 + 0.5 + 1 / 16) + 4 * M, "GB/s", [M, N, K])
+            return
+        w = W.device_normal((N, K), 0.02, dev, seed=2)
+        wq, wsf, gw = J.empty_nvfp4(N, K, dev)
+        J.jetfp8_quant_nvfp4(x, xq, xsf, gx)
+        J.jetfp8_quant_nvfp4(w, wq, wsf, gw)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        fn = lambda: J.jetfp8_gemm_fprop_nvfp4(xq, xsf, gx, wq, wsf, gw, y)  # noqa: E731
+        _time_case(args, fn, 2.0 * M * N * K, "TFLOP/s", [M, N, K])
         return
     if args.case in ("swiglu_quant", "swiglu_bwd"):
         # SwiGLU of an [M, 2I] gate/up output, I = N / 2 (N = the gate/up width)

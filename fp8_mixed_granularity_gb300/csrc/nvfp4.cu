@@ -26,7 +26,7 @@
 // scale-staging warpgroup writes one atom line per lane, unchanged, into its
 // own lane quarter.
 //
-// GEMM (persistent, one CTA per SM, 384 threads), tile 128 × 256, K in stages
+// GEMM (persistent, one CTA per SM, 512 threads), tile 128 × 256, K in stages
 // of 256 elements (128 bytes per row):
 //   warp 0      TMA producer: A 16 KB and B 32 KB (128-byte swizzle) and the
 //               stage's block-scale atoms (2 + 4 KB, bulk copies), one barrier.
@@ -35,7 +35,8 @@
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X per stage.
 //   warps 4-7   copy each stage's block scales from shared memory into the
 //               stage's TMEM scale columns (tcgen05.st), then signal the MMA.
-//   warps 8-11  epilogue: accumulator → row and column scales → bf16 → global.
+//   warps 8-15  epilogue, two warps per lane quarter (128 columns each):
+//               accumulator → row and column scales → bf16 → global.
 // The tensor core applies the block scales, so nothing is promoted per block.
 // Every wait is bounded (about 2 s); on expiry the kernel records an error
 // word and winds down.
@@ -155,7 +156,7 @@ constexpr int B_BYTES = BN * KSTAGE_BYTES;         // 32 KB
 constexpr int SFA_BYTES = 4 * 512;                 // four K = 64 MMAs × one 128-row atom
 constexpr int SFB_BYTES = (BN / 128) * 4 * 512;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;   // 54 KB
-constexpr int THREADS = 384;
+constexpr int THREADS = 512;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = BN;                       // columns 0..255: the accumulator
 constexpr int SF_COLS = 4 * 4 + 4 * 8;             // per stage: SFA 4 × 4, SFB 4 × 8 columns
@@ -240,7 +241,7 @@ k_gemm_nvfp4_fprop(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       mbar_init_s(smem_addr(&bars->sfready[s]), 4);
     }
     mbar_init_s(smem_addr(&bars->tfull), 1);
-    mbar_init_s(smem_addr(&bars->tempty), 4);
+    mbar_init_s(smem_addr(&bars->tempty), 8);
     mbar_init_s(smem_addr(&bars->done), 1);
     bars->abort_flag = 0;
     mbar_fence_init();
@@ -385,6 +386,7 @@ k_gemm_nvfp4_fprop(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   } else if (warp >= 8) {
     // ---------------- epilogue ----------------
     const uint32_t lq = (uint32_t)(warp & 3);
+    const int half = (warp - 8) >> 2;            // columns [128·half, 128·half + 128)
     uint32_t tj = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tj) {
       int mt, nt;
@@ -398,7 +400,7 @@ k_gemm_nvfp4_fprop(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       const float* gw = a.gw + (size_t)nt * BN;
       uint16_t* yr = a.y + (size_t)(row_ok ? row : 0) * a.N + (size_t)nt * BN;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = 128 * half; c0 < 128 * half + 128; c0 += 32) {
         uint32_t r[32];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
