@@ -89,6 +89,13 @@ def test_fprop_decode_tiles_bit_identical_to_training_tiles(dev):
     wq, sw, _ = q_weight(w, dev, with_t=False)
     y = _fprop(dev, xq, sx, wq, sw, torch.float32)
     _assert_close(h(y), O.gemm_fprop(h(xq), h(sx)[:, :64], h(wq), h(sw)), "decode fprop")
+    # and a ragged decode batch (100 rows) on 64-wide tiles (N = 6144), bf16 out
+    x = W.activations(100, 512, seed=4, stream=25)
+    w = W.weights(6144, 512, seed=4, stream=26)
+    xq, sx = q_act(x, dev)
+    wq, sw, _ = q_weight(w, dev, with_t=False)
+    y = _fprop(dev, xq, sx, wq, sw)
+    _assert_close(h(y.float()), O.gemm_fprop(h(xq), h(sx)[:, :100], h(wq), h(sw)), "decode fprop 64-wide")
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 512, 384), (200, 768, 256), (1, 256, 128), (1024, 2048, 1024)])
