@@ -496,6 +496,9 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
@@ -872,7 +875,7 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
           if (lane == 0) {
             // (a pair: on the leader's barrier, addressed through the cluster)
             if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->tempty[b]), 0));
-            else mbar_arrive(&bars->tempty[b]);
+            else mbar_arrive_relaxed(&bars->tempty[b]);
           }
         };
         if (COLS) {
