@@ -614,7 +614,7 @@ struct Q4Args {
   unsigned* err;
 };
 
-constexpr int kBf16WG = 3;     // warpgroups per CTA for 32 KB bf16 tiles (two-tile rings: 192 KB)
+constexpr int kBf16WG = 2;     // warpgroups per CTA for 32 KB bf16 tiles (two-tile rings: 128 KB); 3 spill at 85 registers and run slower
 
 // Q4: one read of the bf16 gradient → 1×128 row groups along N (stored as is)
 // and 128×1 column groups along M (stored transposed).
@@ -1249,8 +1249,15 @@ cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, in
   unsigned* err = device_error_word();
   if (err == nullptr) return cudaErrorInvalidValue;
   // rows up to 8192 wide stream whole through shared memory; wider rows take
-  // the register kernel (which reads each row twice)
-  if (H <= 4096) return launch_rmsnorm_tma<12, 2, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+  // the register kernel (which reads each row twice).  Rows up to 4096 wide:
+  // one slot per warp and more warps (20, or 24 for many rows) beat two slots
+  // per warp with 12 (measured at 8192 and 32768 rows × 4096: 3779 / 4886 vs
+  // 3246 / 4011 GB/s); the kernel is issue-bound and more warps hide more of
+  // each row's latency.
+  if (H <= 4096) {
+    if (M >= 16384) return launch_rmsnorm_tma<24, 1, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+    return launch_rmsnorm_tma<20, 1, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+  }
   if (H <= 8192) return launch_rmsnorm_tma<6, 2, 8192>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
   const unsigned grid = grid_for((size_t)M, kThreads / 32, 8);
   k_rmsnorm_quant<<<grid, kThreads, 0, st>>>(
