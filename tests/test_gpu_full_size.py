@@ -110,9 +110,10 @@ def test_rmsnorm_quant_full_size(dev):
 
 
 def test_grouped_wgrad_full_size(dev):
-    """The four WGrads of the Llama-3.1-8B layer at 8192 tokens in one grouped
-    launch (the benchmark's launch), bf16 ∇W: sampled row and column stripes
-    of the QKV and down-projection gradients against the oracle."""
+    """The four WGrads of the Llama-3.1-8B layer at 8192 tokens, bf16 ∇W: each
+    single launch (the benchmark's launches) equals its problem in one grouped
+    launch bit for bit, and sampled row and column stripes of the QKV and
+    down-projection gradients match the oracle."""
     lins = W.llama8b_training(M_TRAIN)
     rng = np.random.default_rng(6)
     ops, dws = [], []
@@ -128,6 +129,12 @@ def test_grouped_wgrad_full_size(dev):
         dws.append(torch.empty(lin.N, lin.K, dtype=torch.bfloat16, device=dev))
     J.jetfp8_gemm_wgrad_grouped([(*o, dw) for o, dw in zip(ops, dws)])
     check_errors()
+    for o, dw in zip(ops, dws):
+        single = torch.empty_like(dw)
+        J.jetfp8_gemm_wgrad(*o, single)
+        check_errors()
+        assert torch.equal(single, dw)
+        del single
     for i in (0, 3):
         dyqT, sdyT, xqT, sxT = (h(t) for t in ops[i])
         N, K = dws[i].shape
