@@ -12,7 +12,8 @@
 //   * one FP32 scale per row (a token of X, an output channel of W):
 //       g = RN(amax_row / 2688), h = RN(6·g), s_b = E4M3(RN(amax_b / h)),
 //       d_b = RN(s_b·g), q = E2M1(RN(x / d_b))  (a signed zero when d_b = 0),
-//     every step one correctly rounded FP32 operation.
+//     every step one correctly rounded FP32 operation (the element quotients
+//     by the division-free exact sequence in quot2).
 //   Y[m,n] = bf16(RN(RN(D[m,n]·gx[m])·gw[n])),  D = Σ_k x̂q·ŵq (block-scaled).
 //
 // Block scales live in a blocked layout that the GEMM moves into tensor memory
@@ -82,6 +83,28 @@ __device__ __forceinline__ uint32_t e4m3_code(float v) {
   return r & 0xFFu;
 }
 
+// Correctly rounded quotients (x0/d, x1/d) without a division: two Markstein
+// corrections of q0 = RN(x·y), y = RN(1/d) (P. Markstein, IBM J. Res. Dev.
+// 34(1), 1990), on -x and -y so the sign of a zero survives; the same
+// sequence as the E4M3 quantisers'.  Exact while every intermediate is normal,
+// which holds for d >= 2^-90 whenever the quotient is 2^-11 or larger; smaller
+// quotients stay below 2^-10 with the sign of x, and every such value has the
+// E2M1 code of a zero.
+__device__ __forceinline__ float2 quot2(float x0, float x1, uint64_t s2, uint64_t ny2) {
+  uint64_t nx, q;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(nx) : "f"(-x0), "f"(-x1));
+  asm("{\n\t.reg .b64 r;\n\t"
+      "mul.rn.f32x2 %0, %1, %3;\n\t"
+      "fma.rn.f32x2 r, %0, %2, %1;\n\t"
+      "fma.rn.f32x2 %0, r, %3, %0;\n\t"
+      "fma.rn.f32x2 r, %0, %2, %1;\n\t"
+      "fma.rn.f32x2 %0, r, %3, %0;\n\t}"
+      : "=&l"(q) : "l"(nx), "l"(s2), "l"(ny2));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(q));
+  return r;
+}
+
 __device__ __forceinline__ size_t scale_offset(uint32_t r, uint32_t b, uint32_t kg) {
   return ((size_t)((r >> 7) * kg + (b >> 2)) * 32u + (r & 31u)) * 16u + ((r >> 5) & 3u) * 4u + (b & 3u);
 }
@@ -129,15 +152,27 @@ k_quant_nvfp4_rows(const uint16_t* __restrict__ x, uint32_t R, uint32_t K, uint8
       const uint32_t s = e4m3_code(__fdiv_rn(ab, h));
       const float d = __fmul_rn(dec_e4m3x2(s).x, g);
       uint32_t c[2] = {0u, 0u};
+      if (d >= 0x1p-90f) {
+        const float ny = -__frcp_rn(d);
+        uint64_t s2, ny2;
+        asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(d));
+        asm("mov.b64 %0, {%1, %1};" : "=l"(ny2) : "f"(ny));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t byte;
-        if (d > 0.0f) {
-          byte = e2m1x2(__fdiv_rn(f[i].x, d), __fdiv_rn(f[i].y, d));
-        } else {
-          byte = ((__float_as_uint(f[i].x) >> 31) << 3) | ((__float_as_uint(f[i].y) >> 31) << 7);
+        for (int i = 0; i < 8; ++i) {
+          const float2 qq = quot2(f[i].x, f[i].y, s2, ny2);
+          c[i >> 2] |= e2m1x2(qq.x, qq.y) << (8 * (i & 3));
         }
-        c[i >> 2] |= byte << (8 * (i & 3));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t byte;
+          if (d > 0.0f) {
+            byte = e2m1x2(__fdiv_rn(f[i].x, d), __fdiv_rn(f[i].y, d));
+          } else {
+            byte = ((__float_as_uint(f[i].x) >> 31) << 3) | ((__float_as_uint(f[i].y) >> 31) << 7);
+          }
+          c[i >> 2] |= byte << (8 * (i & 3));
+        }
       }
       *reinterpret_cast<uint2*>(qr + 8u * b) = make_uint2(c[0], c[1]);
       sf[scale_offset(r, b, kg)] = (uint8_t)s;

@@ -137,3 +137,23 @@ def test_hand_cases():
     got = division_free_quotient(x, S)
     assert np.array_equal(got.view(np.uint32), _rn32_div_exact(x, S).view(np.uint32))
     assert np.signbit(got[4]) and not np.signbit(got[3]) and got[3] == 0
+
+
+def test_fp4_block_scales():
+    """The FP4 variant's quantiser runs the same sequence with d = RN(s_b·g)
+    (an E4M3 block scale times an FP32 row scale) for d >= 2^-90: bf16 elements
+    of every magnitude up to 8·d, both signs, under block scales of every E4M3
+    exponent and random row scales."""
+    rng = np.random.default_rng(11)
+    mags = _bf16_magnitudes()
+    e4m3 = np.array([(1 + m / 8) * 2.0 ** e for e in range(-6, 9) for m in range(8)], np.float64)
+    n = 0
+    for sb in e4m3[::3]:
+        for g in np.ldexp(rng.uniform(1, 2, 3), rng.integers(-60, 20, 3)).astype(np.float32):
+            d = np.float32(np.float32(sb) * g)
+            if d < np.float32(2.0 ** -90):
+                continue
+            m = mags[mags <= np.float32(8) * d]
+            x = np.concatenate([m, -m]).astype(np.float32)
+            n += _check(x, np.full(x.shape, d, np.float32))
+    assert n > 1_000_000
