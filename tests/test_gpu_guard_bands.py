@@ -136,3 +136,37 @@ def test_gemms_write_only_their_outputs(dev, M):
         J.jetfp8_gemm_wgrad_grouped([(dyqT, sdyT, xqT, sxT, d) for d in dws])
     check_errors()
     g.check()
+
+
+@pytest.mark.parametrize("M", [300, 1])
+def test_pair_and_fp4_write_only_their_outputs(dev, M):
+    """The CTA-pair GEMM kernel (ragged M: the second CTA of a pair may have no
+    rows) and the FP4 variant's quantiser (codes, blocked scales with their
+    padding rows, row scales) and FProp."""
+    g = Guarded(dev)
+    N, K = 512, 512
+    xq = torch.empty(M, K, dtype=torch.uint8, device=dev)
+    sx = torch.empty(*J.scale_shape(M, K), dtype=torch.float32, device=dev)
+    J.jetfp8_quant_act_1x128(W.device_activations(M, K, dev, seed=6), xq, sx)
+    wq = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    sw = torch.empty(N // 128, K // 128, dtype=torch.float32, device=dev)
+    J.jetfp8_quant_weight_128x128(W.device_normal((N, K), 0.02, dev, seed=7), wq, sw, None)
+    y = g((M, N), torch.bfloat16)
+    J.jetfp8_test_set_gemm_path(2)
+    try:
+        J.jetfp8_gemm_fprop(xq, sx, wq, sw, y)
+        y32 = g((M, N), torch.float32)
+        J.jetfp8_gemm_fprop(xq, sx, wq, sw, y32)
+    finally:
+        J.jetfp8_test_set_gemm_path(0)
+    x4 = W.device_activations(M, K, dev, seed=8)
+    xq4 = g((M, K // 2), torch.uint8)
+    xsf4 = g((J.jetfp8_nvfp4_scale_bytes(M, K),), torch.uint8)
+    gx4 = g((M,), torch.float32)
+    J.jetfp8_quant_nvfp4(x4, xq4, xsf4, gx4)
+    wq4, wsf4, gw4 = J.empty_nvfp4(N // 2, K, dev)
+    J.jetfp8_quant_nvfp4(W.device_normal((N // 2, K), 0.02, dev, seed=9), wq4, wsf4, gw4)
+    y4 = g((M, N // 2), torch.bfloat16)
+    J.jetfp8_gemm_fprop_nvfp4(xq4, xsf4, gx4, wq4, wsf4, gw4, y4)
+    check_errors()
+    g.check()
