@@ -272,6 +272,25 @@ jetfp8_status jetfp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t
   return from_cuda(launch_quant_weight(w_bf16, N, K, q, s, qT, stream));
 }
 
+jetfp8_status jetfp8_quant_weight_grouped(int count, const void* const* w_bf16, const int64_t* N,
+                                          const int64_t* K, uint8_t* const* q, float* const* s,
+                                          uint8_t* const* qT, cudaStream_t stream) {
+  log_call("jetfp8_quant_weight_grouped", count, 0);
+  if (count < 1 || count > JETFP8_MAX_GROUP || w_bf16 == nullptr || N == nullptr || K == nullptr ||
+      q == nullptr || s == nullptr)
+    return JETFP8_ERR_INVALID_ARG;
+  Check c;
+  for (int i = 0; i < count; ++i) {
+    // as jetfp8_quant_weight_128x128, problem by problem
+    c.bf(w_bf16[i]).ptr(q[i]).ptr(s[i]).ptr(qT == nullptr ? nullptr : qT[i], false).mult128(N[i])
+        .mult128(K[i]).fits(N[i], K[i]);
+    if (c.st != JETFP8_OK) return c.st;
+  }
+  c.device();
+  if (c.st != JETFP8_OK) return c.st;
+  return from_cuda(launch_quant_weight_grouped(count, w_bf16, N, K, q, s, qT, stream));
+}
+
 jetfp8_status jetfp8_requant_rowgrp_to_colgrp(const uint8_t* q, const float* s, int64_t M,
                                               int64_t K, uint8_t* qT, float* sT,
                                               cudaStream_t stream) {

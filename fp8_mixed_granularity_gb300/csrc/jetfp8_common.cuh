@@ -179,17 +179,15 @@ __device__ __forceinline__ QScale qscale_from_s(float s, bool slow) {
   return g;
 }
 
-// Four E4M3 codes (byte k = value k) of the bf16 values in w0 (values 0, 1)
-// and w1 (values 2, 3) under group constants g (not slow).
-__device__ __forceinline__ uint32_t codes4_bf16(uint32_t w0, uint32_t w1, const QScale& g) {
+// Four E4M3 codes (byte k = value k) of the bf16 values whose negations are
+// in nw0 (values 0, 1) and nw1 (values 2, 3), under group constants g (not slow).
+__device__ __forceinline__ uint32_t codes4_negbf16(uint32_t nw0, uint32_t nw1, const QScale& g) {
   uint32_t c;
-  asm("{\n\t.reg .b32 a0, a1, a2, a3, n0, n1;\n\t.reg .b64 x0, x1, q0, q1, r0, r1;\n\t.reg .b16 l, h;\n\t"
-      "xor.b32 n0, %1, 0x80008000;\n\t"
-      "xor.b32 n1, %2, 0x80008000;\n\t"
-      "shl.b32 a0, n0, 16;\n\t"
-      "and.b32 a1, n0, 0xFFFF0000;\n\t"
-      "shl.b32 a2, n1, 16;\n\t"
-      "and.b32 a3, n1, 0xFFFF0000;\n\t"
+  asm("{\n\t.reg .b32 a0, a1, a2, a3;\n\t.reg .b64 x0, x1, q0, q1, r0, r1;\n\t.reg .b16 l, h;\n\t"
+      "shl.b32 a0, %1, 16;\n\t"
+      "and.b32 a1, %1, 0xFFFF0000;\n\t"
+      "shl.b32 a2, %2, 16;\n\t"
+      "and.b32 a3, %2, 0xFFFF0000;\n\t"
       "mov.b64 x0, {a0, a1};\n\t"
       "mov.b64 x1, {a2, a3};\n\t"
       "mul.rn.f32x2 q0, x0, %4;\n\t"
@@ -207,8 +205,13 @@ __device__ __forceinline__ uint32_t codes4_bf16(uint32_t w0, uint32_t w1, const 
       "cvt.rn.satfinite.e4m3x2.f32 l, a1, a0;\n\t"
       "cvt.rn.satfinite.e4m3x2.f32 h, a3, a2;\n\t"
       "mov.b32 %0, {l, h};\n\t}"
-      : "=r"(c) : "r"(w0), "r"(w1), "l"(g.s2), "l"(g.ny2));
+      : "=r"(c) : "r"(nw0), "r"(nw1), "l"(g.s2), "l"(g.ny2));
   return c;
+}
+
+// The same for the bf16 values themselves in w0 (values 0, 1) and w1 (values 2, 3).
+__device__ __forceinline__ uint32_t codes4_bf16(uint32_t w0, uint32_t w1, const QScale& g) {
+  return codes4_negbf16(w0 ^ 0x80008000u, w1 ^ 0x80008000u, g);
 }
 
 // The same for FP32 values given negated as two packed pairs (nx0 = (-v0, -v1),

@@ -13,6 +13,11 @@ cudaError_t launch_quant_rowgroups(const void* x, int64_t M, int64_t K, uint8_t*
                                    cudaStream_t st);
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,
                                 uint8_t* qT, cudaStream_t st);
+// Q2 for `count` weights (1..JETFP8_MAX_GROUP) in one launch; qT may be NULL
+// (no transposes) or hold NULL entries.
+cudaError_t launch_quant_weight_grouped(int count, const void* const* w, const int64_t* N, const int64_t* K,
+                                        uint8_t* const* q, float* const* s, uint8_t* const* qT,
+                                        cudaStream_t st);
 cudaError_t launch_requant_row2col(const uint8_t* q, const float* s, int64_t M, int64_t K,
                                    uint8_t* qT, float* sT, cudaStream_t st);
 cudaError_t launch_quant_grad_dual(const void* dy, int64_t M, int64_t N, uint8_t* q_row,

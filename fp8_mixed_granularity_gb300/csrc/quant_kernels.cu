@@ -159,6 +159,52 @@ __device__ __forceinline__ uint32_t half_warp_qscales(const float (&amax)[8], fl
   return mask;
 }
 
+// Max over the 16 lanes of a half-warp of 8 per-lane column values a[0..7],
+// returned in the lane l of column l mod 8.  Each exchange step hands the
+// partner the half of the columns it keeps (lane bit 0 picks the column's bit 0,
+// bit 1 its bit 1, bit 2 its bit 2), so 8 shuffles replace 32.
+__device__ __forceinline__ float half_warp_colmax8(const float (&a)[8]) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const bool b0 = lane & 1u, b1 = lane & 2u, b2 = lane & 4u;
+  float r1[4], r2[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b0 ? a[2 * i + 1] : a[2 * i], send = b0 ? a[2 * i] : a[2 * i + 1];
+    r1[i] = fmaxf(keep, __shfl_xor_sync(kFull, send, 1));
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float keep = b1 ? r1[2 * j + 1] : r1[2 * j], send = b1 ? r1[2 * j] : r1[2 * j + 1];
+    r2[j] = fmaxf(keep, __shfl_xor_sync(kFull, send, 2));
+  }
+  const float keep = b2 ? r2[1] : r2[0], send = b2 ? r2[0] : r2[1];
+  const float r3 = fmaxf(keep, __shfl_xor_sync(kFull, send, 4));
+  return fmaxf(r3, __shfl_xor_sync(kFull, r3, 8));
+}
+
+// half_warp_qscales for maxima already reduced so that lane l holds group
+// (l mod 8)'s maximum.
+__device__ __forceinline__ uint32_t half_warp_qscales_of(float a, float (&s)[8], float (&ny)[8]) {
+  const uint32_t base = threadIdx.x & 16u;
+  const float s_mine = make_scale(a).s;
+  const float ny_mine = -__frcp_rn(s_mine);
+  const bool slow = a != 0.0f && a < kQuotientMinAmax;
+  const uint32_t mask = (__ballot_sync(kFull, slow) >> base) & 0xFFu;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    s[i] = __shfl_sync(kFull, s_mine, base + i);
+    ny[i] = __shfl_sync(kFull, ny_mine, base + i);
+  }
+  return mask;
+}
+
+// max(|a|, |b|, |c|) in one three-input maximum.
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
+  return r;
+}
+
 __device__ __forceinline__ QScale qscale_of(float s, float ny) {
   QScale g;
   g.s = s;
@@ -174,16 +220,19 @@ __device__ __forceinline__ void record_timeout(volatile int* abort_word, unsigne
 }
 
 // 8 codes held as (lo, hi) with byte i from rotated slot i, i.e. tile row
-// (i + k) mod 8 -> bytes in row order: a left rotation of the 64-bit value by
-// k bytes (k = 0..7).
-__device__ __forceinline__ uint2 unrotate8(uint32_t lo, uint32_t hi, uint32_t k) {
-  if (k & 4u) {
-    const uint32_t t = lo;
-    lo = hi;
-    hi = t;
+// (i + k) mod 8 -> bytes in row order (byte r <- byte (r - k) mod 8): two byte
+// permutes whose selectors depend only on k (0..7), formed once per thread.
+__device__ __forceinline__ uint2 unrotate_selectors(uint32_t k) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (uint32_t r = 0; r < 4; ++r) {
+    lo |= ((r - k) & 7u) << (4u * r);
+    hi |= ((r + 4u - k) & 7u) << (4u * r);
   }
-  const uint32_t sh = (k & 3u) * 8u;
-  return make_uint2(__funnelshift_l(hi, lo, sh), __funnelshift_l(lo, hi, sh));
+  return make_uint2(lo, hi);
+}
+__device__ __forceinline__ uint2 unrotate8(uint32_t lo, uint32_t hi, uint2 sel) {
+  return make_uint2(__byte_perm(lo, hi, sel.x), __byte_perm(lo, hi, sel.y));
 }
 
 // Offset of 16-byte chunk c (0..7) of row r in a box of 128-byte rows stored
@@ -201,25 +250,71 @@ __device__ __forceinline__ void load_group16(uint32_t gb, uint32_t l8, uint32_t 
   w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
 
-// One lane's 16 bf16 values of a group (8 packed words): the group's maximum
-// over its 8 lanes, its scale, and the 16 codes as (first half, second half).
-__device__ __forceinline__ void group16_codes(const uint32_t (&w)[8], bool valid, float& S, uint2& c0, uint2& c1) {
-  uint32_t m = amax2(amax2(amax2(w[0], w[1]), amax2(w[2], w[3])), amax2(amax2(w[4], w[5]), amax2(w[6], w[7])));
+// One lane's 16 bf16 values of a group, given negated (8 packed words of -x):
+// the group's maximum over its 8 lanes, its scale, and the 16 codes of x as
+// (first half, second half).
+__device__ __forceinline__ void group16_codes_neg(const uint32_t (&nw)[8], bool valid, float& S, uint2& c0,
+                                                  uint2& c1) {
+  uint32_t m = amax2(amax2(amax2(nw[0], nw[1]), amax2(nw[2], nw[3])), amax2(amax2(nw[4], nw[5]), amax2(nw[6], nw[7])));
   m &= 0x7FFF7FFFu;
   float amax = valid ? fmaxf(bf_lo(m), bf_hi(m)) : 0.0f;
   amax = group8_max(amax);
   S = make_scale(amax).s;
   uint32_t c[4];
   if (amax != 0.0f && amax < kQuotientMinAmax) {
+    constexpr float k96 = 0x1p96f;
+    const QScale g = qscale_from_s(S * k96, false);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) c[k] = codes4_tiny(bf2_to_f2(w[2 * k]), bf2_to_f2(w[2 * k + 1]), S);
+    for (int k = 0; k < 4; ++k) {
+      const float2 a = bf2_to_f2(nw[2 * k]), b = bf2_to_f2(nw[2 * k + 1]);
+      c[k] = codes4_neg_f32(pack_f2(a.x * k96, a.y * k96), pack_f2(b.x * k96, b.y * k96), g);
+    }
   } else {
     const QScale g = qscale_from_s(S, false);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) c[k] = codes4_bf16(w[2 * k], w[2 * k + 1], g);
+    for (int k = 0; k < 4; ++k) c[k] = codes4_negbf16(nw[2 * k], nw[2 * k + 1], g);
   }
   c0 = make_uint2(c[0], c[1]);
   c1 = make_uint2(c[2], c[3]);
+}
+
+// The same for the values themselves (8 packed words of x).
+__device__ __forceinline__ void group16_codes(const uint32_t (&w)[8], bool valid, float& S, uint2& c0, uint2& c1) {
+  uint32_t nw[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) nw[k] = w[k] ^ 0x80008000u;
+  group16_codes_neg(nw, valid, S, c0, c1);
+}
+
+// c plus the squares of one lane's 16 bf16 values (8 packed words), added in
+// element order, each step one FMA on the bf16 operands (the square is exact in FP32).
+__device__ __forceinline__ float add_squares16(const uint32_t (&w)[8], float c) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, l, l, %0;\n\t"
+        "fma.rn.f32.bf16 %0, h, h, %0;\n\t}"
+        : "+f"(c) : "r"(w[e]));
+  return c;
+}
+
+// For a pair of bf16 x (wx) and γ (wg): -bf16(RN(RN(x·γ)·r)) as a bf16 pair,
+// given nr2 = (-r, -r).  x·γ is one FMA on the bf16 operands with a -0 addend,
+// exact while |x·γ| is a normal FP32 number; the product with -r is one FP32
+// rounding, then the bf16 rounding (both symmetric, so the result is -y).
+__device__ __forceinline__ uint32_t neg_norm_pair(uint32_t wx, uint32_t wg, uint64_t nr2) {
+  uint32_t o;
+  asm("{\n\t.reg .b16 xl, xh, gl, gh;\n\t.reg .b32 pl, ph;\n\t.reg .b64 p;\n\t"
+      "mov.b32 {xl, xh}, %1;\n\t"
+      "mov.b32 {gl, gh}, %2;\n\t"
+      "fma.rn.f32.bf16 pl, xl, gl, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 ph, xh, gh, 0f80000000;\n\t"
+      "mov.b64 p, {pl, ph};\n\t"
+      "mul.rn.f32x2 p, p, %3;\n\t"
+      "mov.b64 {pl, ph}, p;\n\t"
+      "cvt.rn.bf16x2.f32 %0, ph, pl;\n\t}"
+      : "=r"(o) : "r"(wx), "r"(wg), "l"(nr2));
+  return o;
 }
 
 constexpr uint32_t kSeg = 2048;   // Q1 unit: 4 KB of bf16
@@ -307,7 +402,11 @@ k_quant_rows_tma(const uint16_t* __restrict__ x, uint32_t M, uint32_t K, uint32_
 // tree, the 32 lanes by a butterfly; r = RN(1/sqrt(RN(Σx²·RN(1/H)) + eps))
 // (IEEE reciprocal square root).  With at most 16 + 4 + 5 roundings on a sum
 // of positive terms, the relative error of Σx² is at most 25·2^-24 (first
-// order), and that of r at most 14.25·2^-24.
+// order), and that of r at most 14.25·2^-24.  y = bf16(RN(RN(x·γ)·r)): x·γ is
+// exact (a product of two bf16 values) while it stays a normal FP32 number, which
+// holds for every row whose Σx² is itself accurate (|x| within about 1e-19..1e19)
+// when 1e-19 < |γ| < 1e19; the quantiser then works on -y, which the same
+// roundings give directly from -r.
 template <int W, int D, uint32_t SLOT_ELEMS>
 __global__ void __launch_bounds__(32 * W, 1)
 k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
@@ -364,12 +463,7 @@ k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__
       if (grp < ng) {
         uint32_t w[8];
         load_group16(sb + grp * 256u, l8, w);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 f = bf2_to_f2(w[e]);
-          c = __fmaf_rn(f.x, f.x, c);
-          c = __fmaf_rn(f.y, f.y, c);
-        }
+        c = add_squares16(w, c);
       }
       cs[k] = c;
     }
@@ -382,6 +476,7 @@ k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__
     for (int o = 16; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, o));
     const float r = __frsqrt_rn(__fadd_rn(__fmul_rn(ss, inv_h), eps));
     if (lane == 0) rstd[row] = r;
+    const uint64_t nr2 = pack_f2(-r, -r);
     for (uint32_t g0 = 0; g0 < ng; g0 += 4) {
       const uint32_t grp = g0 + g4;
       const bool valid = grp < ng;
@@ -393,23 +488,23 @@ k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__
 #pragma unroll
         for (int k = 0; k < 8; ++k) wx[k] = wg[k] = 0;
       }
-      uint32_t yb[8];
+      uint32_t nyb[8];   // -y
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float2 t = mul2(mul2(bf2_to_f2(wx[k]), make_float2(r, r)), bf2_to_f2(wg[k]));
-        yb[k] = f2_to_bf2(t.x, t.y);
-      }
+      for (int k = 0; k < 8; ++k) nyb[k] = neg_norm_pair(wx[k], wg[k], nr2);
       float S;
       uint2 c0, c1;
-      group16_codes(yb, valid, S, c0, c1);
+      group16_codes_neg(nyb, valid, S, c0, c1);
       if (valid) {
         uint8_t* qg = q + (size_t)row * H + grp * 128u;
         *reinterpret_cast<uint2*>(qg + l8 * 8u) = c0;
         *reinterpret_cast<uint2*>(qg + 64u + l8 * 8u) = c1;
         if (y != nullptr) {
+          constexpr uint32_t kNeg = 0x80008000u;
           uint16_t* yr = y + (size_t)row * H + grp * 128u;
-          *reinterpret_cast<uint4*>(yr + l8 * 8u) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-          *reinterpret_cast<uint4*>(yr + 64u + l8 * 8u) = make_uint4(yb[4], yb[5], yb[6], yb[7]);
+          *reinterpret_cast<uint4*>(yr + l8 * 8u) =
+              make_uint4(nyb[0] ^ kNeg, nyb[1] ^ kNeg, nyb[2] ^ kNeg, nyb[3] ^ kNeg);
+          *reinterpret_cast<uint4*>(yr + 64u + l8 * 8u) =
+              make_uint4(nyb[4] ^ kNeg, nyb[5] ^ kNeg, nyb[6] ^ kNeg, nyb[7] ^ kNeg);
         }
         if (l8 == 0) s[(size_t)grp * ld_s + row] = S;
       }
@@ -655,7 +750,7 @@ k_quant_grad_dual_tma(const __grid_constant__ CUtensorMap map, const Q4Args a) {
       const uint32_t rg = tid & 15u, cg = tid >> 4;
       uint8_t* qp = a.qT_col + (n0 + 8 * cg) * a.M + m0 + 8 * rg;
       col_codes_bf16(w, sc, ny, slow, [&](int j, uint32_t lo, uint32_t hi) {
-        *reinterpret_cast<uint2*>(qp + (size_t)j * a.M) = unrotate8(lo, hi, rg & 7u);
+        *reinterpret_cast<uint2*>(qp + (size_t)j * a.M) = unrotate8(lo, hi, unrotate_selectors(rg & 7u));
       });
       if (rg == 0) {
         float* sp = a.sT_col + (size_t)mb * a.N + n0 + 8 * cg;
@@ -672,23 +767,49 @@ struct Q2Args {
   uint8_t* q;
   float* s;
   uint8_t* qT;
+};
+
+// Up to JETFP8_MAX_GROUP weights quantised by one launch: problem p owns the
+// global tiles [tile_end[p-1], tile_end[p]) (tile_end[-1] = 0), each problem's
+// tiles in its own row-major block order.
+struct Q2Params {
+  CUtensorMap map[JETFP8_MAX_GROUP];
+  Q2Args a[JETFP8_MAX_GROUP];
+  uint32_t tile_end[JETFP8_MAX_GROUP];
+  uint32_t count;
   unsigned* err;
 };
 
 // Q2: 128×128 weight blocks; the optional transposed payload Ŵᵀ holds the
 // same codes (each column of the block quantised again with the block's scale).
 __global__ void __launch_bounds__(256 * kBf16WG, 1)
-k_quant_weight_tma(const __grid_constant__ CUtensorMap map, const Q2Args a) {
-  const uint32_t kblocks = a.K / 128, ntiles = (a.N / 128) * kblocks;
+k_quant_weight_tma(const __grid_constant__ Q2Params P) {
   const uint64_t pol = policy_evict_first();
+  // global tile -> (problem, tile within it)
+  auto locate = [&](uint32_t tile, uint32_t& local) {
+    uint32_t p = 0, start = 0;
+#pragma unroll
+    for (uint32_t i = 0; i + 1 < JETFP8_MAX_GROUP; ++i)
+      if (i + 1 < P.count && tile >= P.tile_end[i]) {
+        p = i + 1;
+        start = P.tile_end[i];
+      }
+    local = tile - start;
+    return p;
+  };
   auto issue = [&](uint32_t tile, uint32_t dst, uint32_t fb) {
-    const int n0 = (int)(tile / kblocks) * 128, k0 = (int)(tile % kblocks) * 128;
-    tma_g2s_2d(dst, &map, fb, k0, n0, pol);
-    tma_g2s_2d(dst + 16384u, &map, fb, k0 + 64, n0, pol);
+    uint32_t lt;
+    const uint32_t p = locate(tile, lt), kblocks = P.a[p].K / 128;
+    const int n0 = (int)(lt / kblocks) * 128, k0 = (int)(lt % kblocks) * 128;
+    tma_g2s_2d(dst, &P.map[p], fb, k0, n0, pol);
+    tma_g2s_2d(dst + 16384u, &P.map[p], fb, k0 + 64, n0, pol);
   };
   auto consume = [&](uint32_t tile, uint32_t sb, uint32_t wg, uint32_t tid, uint32_t j, TileRing* ring,
                      auto release) {
-    const uint32_t nb = tile / kblocks, kb = tile % kblocks;
+    uint32_t lt;
+    const Q2Args& a = P.a[locate(tile, lt)];
+    const uint32_t kblocks = a.K / 128;
+    const uint32_t nb = lt / kblocks, kb = lt % kblocks;
     const size_t n0 = (size_t)nb * 128, k0 = (size_t)kb * 128;
     uint32_t w[8][4];
     load_rows_bf16(sb, tid, w);
@@ -709,7 +830,7 @@ k_quant_weight_tma(const __grid_constant__ CUtensorMap map, const Q2Args a) {
       mbar_arrive_s(rb);   // release: the write above is seen by the waiters
     }
     if (!mbar_wait_bounded(rb, (j >> 1) & 1u)) {
-      if ((tid & 31u) == 0) record_timeout(nullptr, a.err);
+      if ((tid & 31u) == 0) record_timeout(nullptr, P.err);
       if (a.qT != nullptr) release();
       return;
     }
@@ -735,11 +856,11 @@ k_quant_weight_tma(const __grid_constant__ CUtensorMap map, const Q2Args a) {
       const uint32_t rgc = tid & 15u, cgc = tid >> 4;
       uint8_t* tp = a.qT + (k0 + 8 * cgc) * a.N + n0 + 8 * rgc;
       col_codes_bf16(w, sc, ny, slow, [&](int c, uint32_t lo, uint32_t hi) {
-        *reinterpret_cast<uint2*>(tp + (size_t)c * a.N) = unrotate8(lo, hi, rgc & 7u);
+        *reinterpret_cast<uint2*>(tp + (size_t)c * a.N) = unrotate8(lo, hi, unrotate_selectors(rgc & 7u));
       });
     }
   };
-  run_tile_pipeline<kBf16WG, 32768u, 32768u>(ntiles, a.err, issue, consume);
+  run_tile_pipeline<kBf16WG, 32768u, 32768u>(P.tile_end[P.count - 1], P.err, issue, consume);
 }
 
 struct Q3Args {
@@ -800,23 +921,15 @@ k_requant_row2col_tma(const __grid_constant__ CUtensorMap map, const Q3Args a) {
     float amax[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      float m = 0.0f;
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const float2 v = bits_f2(nx[j][p]);
-        m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
-      }
+      const float2 v0 = bits_f2(nx[j][0]), v1 = bits_f2(nx[j][1]), v2 = bits_f2(nx[j][2]), v3 = bits_f2(nx[j][3]);
+      const float m = max3_abs(max3_abs(v0.x, v0.y, v1.x), max3_abs(v1.y, v2.x, v2.y), max3_abs(v3.x, v3.y, 0.0f));
       amax[j] = m;
     }
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1)
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) amax[jj] = fmaxf(amax[jj], __shfl_xor_sync(kFull, amax[jj], o));
     float sc[8], ny[8];
-    const uint32_t slow = half_warp_qscales(amax, sc, ny);
+    const uint32_t slow = half_warp_qscales_of(half_warp_colmax8(amax), sc, ny);
     uint8_t* qp = a.qT + (k0 + 8 * cg) * a.M + m0 + 8 * rg;
     auto put = [&](int jj, uint32_t lo, uint32_t hi) {
-      *reinterpret_cast<uint2*>(qp + (size_t)jj * a.M) = unrotate8(lo, hi, rg & 7u);
+      *reinterpret_cast<uint2*>(qp + (size_t)jj * a.M) = unrotate8(lo, hi, unrotate_selectors(rg & 7u));
     };
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) {
@@ -1171,23 +1284,36 @@ cudaError_t launch_quant_rowgroups(const void* x, int64_t M, int64_t K, uint8_t*
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,
-                                uint8_t* qT, cudaStream_t st) {
+cudaError_t launch_quant_weight_grouped(int count, const void* const* w, const int64_t* N, const int64_t* K,
+                                        uint8_t* const* q, float* const* s, uint8_t* const* qT,
+                                        cudaStream_t st) {
   unsigned* err = device_error_word();
-  if (err == nullptr) return cudaErrorInvalidValue;
-  CUtensorMap map;
-  if (!encode_map_2d(&map, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2,
-                     64, 128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-    return cudaErrorInvalidValue;
+  if (err == nullptr || count < 1 || count > JETFP8_MAX_GROUP) return cudaErrorInvalidValue;
+  Q2Params P{};
+  P.count = (uint32_t)count;
+  P.err = err;
+  size_t tiles = 0;
+  for (int i = 0; i < count; ++i) {
+    if (!encode_map_2d(&P.map[i], w[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K[i], (uint64_t)N[i],
+                       (uint64_t)K[i] * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+      return cudaErrorInvalidValue;
+    P.a[i] = Q2Args{(uint32_t)N[i], (uint32_t)K[i], q[i], s[i], qT == nullptr ? nullptr : qT[i]};
+    tiles += (size_t)(N[i] / 128) * (K[i] / 128);
+    if (tiles > 0xFFFFFFFFu) return cudaErrorInvalidValue;
+    P.tile_end[i] = (uint32_t)tiles;
+  }
   auto kern = k_quant_weight_tma;
   constexpr int smem = kBf16WG * kRing * 32768 + 1024;
   static int done[64] = {0};
   cudaError_t e = opt_in_smem(kern, smem, done);
   if (e != cudaSuccess) return e;
-  const size_t tiles = (size_t)(N / 128) * (K / 128);
-  kern<<<grid_for(tiles, kBf16WG, 1), 256 * kBf16WG, smem, st>>>(
-      map, Q2Args{(uint32_t)N, (uint32_t)K, q, s, qT, err});
+  kern<<<grid_for(tiles, kBf16WG, 1), 256 * kBf16WG, smem, st>>>(P);
   return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,
+                                uint8_t* qT, cudaStream_t st) {
+  return launch_quant_weight_grouped(1, &w, &N, &K, &q, &s, &qT, st);
 }
 
 cudaError_t launch_requant_row2col(const uint8_t* q, const float* s, int64_t M, int64_t K,
@@ -1250,13 +1376,15 @@ cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, in
   if (err == nullptr) return cudaErrorInvalidValue;
   // rows up to 8192 wide stream whole through shared memory; wider rows take
   // the register kernel (which reads each row twice).  Rows up to 4096 wide:
-  // one slot per warp and more warps (20, or 24 for many rows) beat two slots
-  // per warp with 12 (measured at 8192 and 32768 rows × 4096: 3779 / 4886 vs
-  // 3246 / 4011 GB/s); the kernel is issue-bound and more warps hide more of
-  // each row's latency.
+  // one slot per warp and as many warps as shared memory holds (27, one CTA
+  // per SM): the kernel is issue-bound and more warps hide more of each row's
+  // latency; 8192 rows then take exactly two rounds.  Graph-timed at 8192 and
+  // 32768 rows × 4096: 18, 20, 24, 27 warps give 4304 / 4803, 4254 / 5193,
+  // 3821 / 5487, 4717 / 5548 GB/s.  Fewer than 4096 rows spread over more SMs
+  // with 8 warps per CTA.
   if (H <= 4096) {
-    if (M >= 16384) return launch_rmsnorm_tma<24, 1, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
-    return launch_rmsnorm_tma<20, 1, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+    if (M >= 4096) return launch_rmsnorm_tma<27, 1, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+    return launch_rmsnorm_tma<8, 1, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
   }
   if (H <= 8192) return launch_rmsnorm_tma<6, 2, 8192>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
   const unsigned grid = grid_for((size_t)M, kThreads / 32, 8);

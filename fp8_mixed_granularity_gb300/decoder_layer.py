@@ -57,16 +57,13 @@ def llama8b() -> LayerShape:
 
 
 class _QLinear:
-    """One FP8 linear: weight quantisation, FProp, and the backward pair."""
+    """One FP8 linear: its quantised weight (filled by the layer's grouped Q2), FProp, and the backward pair."""
 
     def __init__(self, N: int, K: int, dev):
         self.N, self.K = N, K
         self.wq = torch.empty(N, K, dtype=_U8, device=dev)
         self.sw = torch.empty(N // 128, K // 128, dtype=_F32, device=dev)
         self.wqT = torch.empty(K, N, dtype=_U8, device=dev)
-
-    def quantise_weight(self, w):
-        J.jetfp8_quant_weight_128x128(w, self.wq, self.sw, self.wqT)
 
     def fprop(self, xq, sx):
         y = torch.empty(xq.shape[0], self.N, dtype=_BF, device=xq.device)
@@ -123,8 +120,9 @@ class DecoderLayerFP8:
     def forward(self, x, batch: int, seq: int):
         s, w, dev = self.s, self.w, self.dev
         T, D = x.shape
-        for lin, name in ((self.qkv, "wqkv"), (self.o, "wo"), (self.gu, "wgu"), (self.down, "wd")):
-            lin.quantise_weight(w[name])
+        # the four weights in one grouped launch (each output as the single launch's)
+        J.jetfp8_quant_weight_grouped([(w[name], lin.wq, lin.sw, lin.wqT) for lin, name in (
+            (self.qkv, "wqkv"), (self.o, "wo"), (self.gu, "wgu"), (self.down, "wd"))])
         # attention block: RMSNorm fused with the 1×128 quantiser, QKV, attention, O
         xq1, sx1 = J.empty_rowgroup_quant(T, D, dev)
         rstd1 = torch.empty(T, dtype=_F32, device=dev)

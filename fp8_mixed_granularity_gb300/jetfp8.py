@@ -40,6 +40,7 @@ SIGNATURES = {
     "jetfp8_gemm_dgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_wgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_wgrad_grouped": [_INT, _P, _P, _P, _P, _I64, _P, _P, _P, _INT, _P],
+    "jetfp8_quant_weight_grouped": [_INT, _P, _P, _P, _P, _P, _P, _P],
     "jetfp8_test_gemm_fprop_drop_block": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _INT, _P],
     "jetfp8_gemm_fprop_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "jetfp8_gemm_dgrad_quant": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
@@ -232,6 +233,28 @@ def jetfp8_gemm_wgrad_grouped(problems, stream=None):
     _check(load_library().jetfp8_gemm_wgrad_grouped(
         n, arrs[0], arrs[1], arrs[2], arrs[3], M, (ctypes.c_int64 * n)(*Ns), (ctypes.c_int64 * n)(*Ks),
         arrs[4], _out_dt(problems[0][4]), _stream(stream)), "jetfp8_gemm_wgrad_grouped")
+
+
+def jetfp8_quant_weight_grouped(problems, stream=None):
+    """Q2 of up to MAX_GROUP weights in one launch.  `problems`: a list of
+    (w, q, s, qT) as for jetfp8_quant_weight_128x128 (qT may be None)."""
+    n = len(problems)
+    if not 1 <= n <= MAX_GROUP:
+        raise JetFP8Error(f"jetfp8_quant_weight_grouped: {n} problems (1..{MAX_GROUP})")
+    cols = [[] for _ in range(4)]
+    Ns, Ks = [], []
+    for w, q, s, qT in problems:
+        N, K = w.shape
+        cols[0].append(_ptr(w, _BF, (N, K), "w"))
+        cols[1].append(_ptr(q, _U8, (N, K), "q"))
+        cols[2].append(_ptr(s, _F, (N // 128, K // 128), "s"))
+        cols[3].append(_ptr(qT, _U8, (K, N), "qT"))
+        Ns.append(N)
+        Ks.append(K)
+    arrs = [(ctypes.c_void_p * n)(*c) for c in cols]
+    _check(load_library().jetfp8_quant_weight_grouped(
+        n, arrs[0], (ctypes.c_int64 * n)(*Ns), (ctypes.c_int64 * n)(*Ks), arrs[1], arrs[2], arrs[3],
+        _stream(stream)), "jetfp8_quant_weight_grouped")
 
 
 def jetfp8_gemm_fprop_quant(xq, sx, wq, sw, yq, ys, y=None, stream=None):

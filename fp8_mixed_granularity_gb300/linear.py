@@ -51,19 +51,24 @@ class LinearBuffers:
             self.t.update(rstd=e(M, dt=f32))
 
     # Each method returns the number of kernels it launched.
-    def forward(self, x: torch.Tensor, w: torch.Tensor, gamma: torch.Tensor | None = None,
+    def forward(self, x: torch.Tensor, w: torch.Tensor | None, gamma: torch.Tensor | None = None,
                 stream=None, events=None) -> int:
+        """Input quantiser, Q2 of w (skipped when w is None: the weight was
+        already quantised, e.g. by `quant_weights_grouped`) and FProp."""
         t = self.t
         if self.rmsnorm:
             _timed(events, "rmsnorm_quant",
                    lambda: J.jetfp8_rmsnorm_quant(x, gamma, 1e-6, t["xq"], t["sx"], t["rstd"], None, stream), stream)
         else:
             _timed(events, "quant_act", lambda: J.jetfp8_quant_act_1x128(x, t["xq"], t["sx"], stream), stream)
-        _timed(events, "quant_weight",
-               lambda: J.jetfp8_quant_weight_128x128(w, t["wq"], t["sw"], t["wqT"], stream), stream)
+        n = 2
+        if w is not None:
+            _timed(events, "quant_weight",
+                   lambda: J.jetfp8_quant_weight_128x128(w, t["wq"], t["sw"], t["wqT"], stream), stream)
+            n += 1
         _timed(events, "gemm_fprop",
                lambda: J.jetfp8_gemm_fprop(t["xq"], t["sx"], t["wq"], t["sw"], t["y"], stream), stream)
-        return 3
+        return n
 
     def backward(self, dy: torch.Tensor, stream=None, events=None, wgrad: bool = True) -> int:
         """Q4, F2, Q3 and (unless `wgrad` is False, for a later grouped
@@ -80,6 +85,19 @@ class LinearBuffers:
         _timed(events, "gemm_wgrad",
                lambda: J.jetfp8_gemm_wgrad(t["dyqT"], t["sdyT"], t["xqT"], t["sxT"], t["dw"], stream), stream)
         return 4
+
+
+def quant_weights_grouped(bufs, weights, stream=None, events=None) -> int:
+    """Q2 (with the transposes) of the weights of several linears in grouped
+    launches of up to MAX_GROUP weights each, before their forwards (which then
+    take w=None).  Returns the number of launches."""
+    n = 0
+    for i in range(0, len(bufs), J.MAX_GROUP):
+        probs = [(w, b.t["wq"], b.t["sw"], b.t["wqT"])
+                 for b, w in zip(bufs[i:i + J.MAX_GROUP], weights[i:i + J.MAX_GROUP])]
+        _timed(events, "quant_weight_grouped", lambda: J.jetfp8_quant_weight_grouped(probs, stream), stream)
+        n += 1
+    return n
 
 
 def wgrad_grouped(bufs, stream=None, events=None) -> int:

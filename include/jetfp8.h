@@ -118,6 +118,9 @@ jetfp8_status jetfp8_quant_grad_dual(const void* dy_bf16, int64_t M, int64_t N,
 
 /* R1 — RMSNorm fused with the 1×128 quantiser ([digest] 方法步骤详情, step 5).
  *   r = 1/sqrt(mean(x²) + eps),  y = bf16((x·r)·γ),  then Q1 on y.
+ *   y is evaluated in FP32 and lies within one bf16 ulp of the exact value (rows
+ *   up to 8192 wide form RN(RN(x·γ)·r), x·γ exact for |x·γ| in the normal FP32
+ *   range); the codes and scales are exactly Q1's on the returned y.
  *   x      bf16 [M, H],  gamma bf16 [H]
  *   q      E4M3 [M, H],  s fp32 [H/128][roundup(M,4)]
  *   rstd   fp32 [M]      (kept for the backward)
@@ -179,6 +182,24 @@ jetfp8_status jetfp8_gemm_wgrad_grouped(int count, const uint8_t* const* dyqT,
                                         const float* const* sxT, int64_t M, const int64_t* N,
                                         const int64_t* K, void* const* dw,
                                         jetfp8_out_dtype out_dtype, cudaStream_t stream);
+
+/* Q2 for up to JETFP8_MAX_GROUP weights at once (the operation is Q2's,
+ * [digest] 方法步骤详情, step 1; grouping is a scheduling choice the pages do not
+ * discuss): the weights a step quantises together, e.g. the four linears of a
+ * layer, in one persistent launch, so the pipeline fills and drains once.
+ * Problem i is the jetfp8_quant_weight_128x128 call
+ *   (w_bf16[i], N[i], K[i], q[i], s[i], qT ? qT[i] : NULL)
+ * and its outputs equal that call's bit for bit.  w_bf16, N, K, q, s and qT are
+ * HOST arrays of `count` entries (qT itself may be NULL: no transposes; an
+ * entry may be NULL: none for that weight); the pointers they hold are device
+ * pointers with the layouts and alignment of jetfp8_quant_weight_128x128.
+ * Outputs must not overlap one another or any input.  1 <= count <=
+ * JETFP8_MAX_GROUP, else JETFP8_ERR_INVALID_ARG; shape errors as the single
+ * call.  The arrays are read before the call returns; the launch is
+ * asynchronous on `stream`. */
+jetfp8_status jetfp8_quant_weight_grouped(int count, const void* const* w_bf16, const int64_t* N,
+                                          const int64_t* K, uint8_t* const* q, float* const* s,
+                                          uint8_t* const* qT, cudaStream_t stream);
 
 /* F1 and F2 with the 1×128 quantiser fused into the epilogue ([digest] 方法步骤详情,
  * step 5: the quantisation is fused into the neighbouring kernels to cut its

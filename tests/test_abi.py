@@ -169,6 +169,28 @@ def test_grouped_wgrad_validation(lib):
     assert call(2, 256, [128, 128], [128, 128], ptr=72) == 3               # misaligned pointers
 
 
+def test_grouped_quant_weight_validation(lib):
+    """The grouped weight quantiser refuses a bad problem count, null arrays and
+    any problem's bad shape or alignment before touching the device."""
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    fn = lib.jetfp8_quant_weight_grouped
+    fn.argtypes = [ctypes.c_int, P, P, P, P, P, P, P]
+
+    def call(count, Ns, Ks, ptr=64, w=True, q=True, qT=True):
+        n = max(len(Ns), 1)
+        arr = (P * n)(*([ptr] * n))
+        return fn(count, arr if w else None, (I64 * n)(*Ns), (I64 * n)(*Ks), arr if q else None, arr,
+                  arr if qT else None, None)
+
+    assert call(0, [128], [128]) == 1                                # no problems
+    assert call(5, [128] * 5, [128] * 5) == 1                        # above the group limit
+    assert call(2, [128, 128], [128, 128], w=False) == 1             # null weight array
+    assert call(2, [128, 128], [128, 128], q=False) == 1             # null code array
+    assert call(3, [128, 384, 200], [128, 128, 128]) == 2            # problem 2's N
+    assert call(2, [128, 128], [128, 100], qT=False) == 2            # problem 1's K, no transposes
+    assert call(2, [128, 128], [128, 128], ptr=72) == 3              # misaligned pointers
+
+
 def test_failure_hook_validation(lib):
     """The failure-path test hook checks its block index before the device."""
     P, I64 = ctypes.c_void_p, ctypes.c_int64

@@ -120,6 +120,30 @@ def test_quant_weight_without_transpose(dev):
     assert np.array_equal(h(q), oq) and np.array_equal(h(s), os_)
 
 
+def test_quant_weight_grouped_equals_single(dev):
+    """Four weights of different shapes (one without a transpose) in one grouped
+    launch: every output equals the single launch's bit for bit and the oracle's."""
+    shapes = [(384, 256), (128, 128), (256, 640), (512, 384)]
+    probs, singles = [], []
+    for i, (N, K) in enumerate(shapes):
+        w = W.weights(N, K, seed=60 + i).to(dev)
+        out = (torch.empty(N, K, dtype=torch.uint8, device=dev),
+               torch.empty(N // 128, K // 128, dtype=torch.float32, device=dev),
+               None if i == 1 else torch.empty(K, N, dtype=torch.uint8, device=dev))
+        probs.append((w, *out))
+        singles.append(q_weight(w.cpu(), dev, with_t=i != 1))
+    J.jetfp8_quant_weight_grouped(probs)
+    check_errors()
+    for i, ((w, q, s, qT), (q1, s1, qT1)) in enumerate(zip(probs, singles)):
+        assert torch.equal(q, q1) and torch.equal(s, s1), i
+        if qT is not None:
+            assert torch.equal(qT, qT1), i
+        oq, os_, oqT = O.quant_weight_128x128(W.bf16_values(w.cpu()))
+        assert np.array_equal(h(q), oq) and np.array_equal(h(s), os_), i
+        if qT is not None:
+            assert np.array_equal(h(qT), oqT), i
+
+
 @pytest.mark.parametrize("M,K", [(256, 512), (128, 128), (1024, 1536)])
 def test_requant_parity(dev, M, K):
     x = W.activations(M, K, seed=0, stream=7)
