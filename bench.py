@@ -49,8 +49,8 @@ REF_ROWS, REF_COLS = 128, 1024       # CPU sample: 128 tokens × 1024 output fea
 # (8192 x 28672 x 4096) from a single-pass ncu capture, and the SHA-256 (first 16 hex
 # digits) of the GEMM sources it was captured on.  When the sources differ from that
 # digest the figure no longer describes the kernel and `traffic` is reported as null.
-GATEUP_FPROP_DRAM_BYTES = 603294720
-GATEUP_FPROP_DRAM_SRC = "25bc2664c453ef79"
+GATEUP_FPROP_DRAM_BYTES = 605948416
+GATEUP_FPROP_DRAM_SRC = "6ab8905622dd69f5"
 GEMM_SOURCES = ("gemm_tcgen05.cu", "jetfp8_common.cuh", "jetfp8_internal.h")
 
 # algorithmic bytes per element of each quantiser (inputs read + outputs written)
@@ -816,7 +816,7 @@ def run_e2e(bufs, inputs, args, torch, gemm_flops, world):
 CASES = {"fprop", "dgrad", "wgrad", "quant_act", "rmsnorm_quant", "quant_weight",
          "quant_grad_dual", "requant", "swiglu_quant", "swiglu_bwd", "fprop_quant", "fprop_then_quant",
          "rmsnorm_bwd", "decoder_layer", "wgrad_grouped", "wgrad_separate", "fp8_library_probe",
-         "fprop_nvfp4", "quant_nvfp4"}
+         "fprop_nvfp4", "quant_nvfp4", "quant_weight_grouped"}
 
 
 def run_case(args):
@@ -884,6 +884,15 @@ def run_case(args):
                     t = b.t
                     J.jetfp8_gemm_wgrad(t["dyqT"], t["sdyT"], t["xqT"], t["sxT"], t["dw"])
         _time_case(args, fn, sum(l.gemm_flops for l in lins), "TFLOP/s", [M, 0, 0])
+        return
+    if args.case == "quant_weight_grouped":
+        # the four Llama-3.1-8B layer weights (with transposes) in one grouped launch
+        from fp8_mixed_granularity_gb300.linear import quant_weights_grouped
+        lins = W.llama8b_training(128)
+        bufs = [LinearBuffers(lin, dev) for lin in lins]
+        ws = [W.device_normal((lin.N, lin.K), 0.02, dev, seed=5 + i) for i, lin in enumerate(lins)]
+        nbytes = sum(lin.N * lin.K * QUANT_BYTES["quant_weight"] for lin in lins)
+        _time_case(args, lambda: quant_weights_grouped(bufs, ws), nbytes, "GB/s", [0, 0, 0])
         return
     if args.case == "rmsnorm_bwd":
         # RMSNorm backward on an [M, H] = [M, K] activation with its forward's r
