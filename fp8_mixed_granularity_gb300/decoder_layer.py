@@ -85,6 +85,8 @@ class _QLinear:
         xqT, sxT = J.empty_rowgroup_quant(self.K, M, dev)
         J.jetfp8_requant_rowgrp_to_colgrp(xq, sx, xqT, sxT)
         dw = torch.empty(self.N, self.K, dtype=_F32, device=dev)
+        # the quantised gradient of the last backward (references only), for inspection
+        self.last = dict(dyq=dyq, sdy=sdy)
         return dx, (dyqT, sdyT, xqT, sxT, dw)
 
 
@@ -175,4 +177,7 @@ class DecoderLayerFP8:
         dx = dh1 + dn1
         J.jetfp8_gemm_wgrad_grouped(list(wgrads.values()))
         grads.update({k: p[4] for k, p in wgrads.items()})
+        # the backward's intermediates (references only), for inspection
+        self.trace = dict(dh=dh, dgu=dgu, dxn2=dxn2, dn2=dn2, dh1=dh1, dattn=dattn, dqkv=dqkv,
+                          dxn1=dxn1, dn1=dn1, wgrad=wgrads)
         return dx, grads

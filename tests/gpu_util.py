@@ -59,3 +59,24 @@ def gemm_tol_ok(got, ref, rel=1e-2, rms_frac=1e-3):
     bound = rel * np.abs(ref) + rms_frac * rms
     ratio = np.abs(got - ref) / np.maximum(bound, 1e-300)
     return bool(np.all(ratio <= 1.0)), float(ratio.max()) if ratio.size else 0.0
+
+
+def rmsnorm_bwd_bounds(xf, gf, r, dyf):
+    """For the RMSNorm backward on FP64 copies of its inputs (x, γ, the GPU's r,
+    dy): the exact ∇x before rounding and the per-element bound on the kernel's
+    FP32 evaluation error (each FP32 operation rounded separately, row sums as
+    16-term FP32 chunks added in FP32 and combined in FP64; factor 2 margin),
+    and the bound on ∇γ (FP32 sums over 128-row chunks added in FP64)."""
+    U = 2.0 ** -24
+    M, H = xf.shape
+    gdy = dyf * gf[None, :]
+    S = np.abs(gdy * xf).sum(axis=1)
+    dot = (gdy * xf).sum(axis=1)
+    c = r ** 3 * dot / H
+    exact = r[:, None] * gdy - xf * c[:, None]
+    dc = r ** 3 / H * (17 + H / 512) * U * S + U * np.abs(c)
+    bound = 2 * (2 * U * np.abs(r[:, None] * gdy) + np.abs(xf) * dc[:, None]
+                 + U * np.abs(xf * c[:, None]) + U * np.abs(exact))
+    terms = np.abs(dyf * xf * r[:, None]).sum(axis=0)
+    chunks = (M + 127) // 128
+    return exact, bound, lambda odg: 2 * ((3 * 128 + chunks) * U * terms + U * np.abs(odg))

@@ -10,10 +10,9 @@ import torch
 from fp8_mixed_granularity_gb300 import jetfp8 as J
 from fp8_mixed_granularity_gb300 import workloads as W
 from oracle import jetfp8_oracle as O
-from tests.gpu_util import check_errors, h
+from tests.gpu_util import check_errors, h, rmsnorm_bwd_bounds
 
 pytestmark = pytest.mark.gpu
-U = 2.0 ** -24
 
 
 @pytest.fixture(scope="module")
@@ -50,14 +49,7 @@ def test_rmsnorm_bwd_parity(dev, M, H):
     odx, odg = O.rmsnorm_bwd(xf, gf, r, dyf)
 
     # exact ∇x before rounding, and the FP32 evaluation error bound per element
-    gdy = dyf * gf[None, :]
-    S = np.abs(gdy * xf).sum(axis=1)
-    dot = (gdy * xf).sum(axis=1)
-    c = r ** 3 * dot / H
-    exact = r[:, None] * gdy - xf * c[:, None]
-    dc = r ** 3 / H * (17 + H / 512) * U * S + U * np.abs(c)
-    bound = 2 * (2 * U * np.abs(r[:, None] * gdy) + np.abs(xf) * dc[:, None]
-                 + U * np.abs(xf * c[:, None]) + U * np.abs(exact))
+    exact, bound, dg_bound_of = rmsnorm_bwd_bounds(xf, gf, r, dyf)
     ulp = np.ldexp(1.0, np.frexp(np.abs(exact))[1] - 8)
     gdx = h(dx.float()).astype(np.float64)
     assert np.all(np.abs(gdx - exact) <= ulp + bound)
@@ -65,10 +57,7 @@ def test_rmsnorm_bwd_parity(dev, M, H):
     sure = bound < ulp / 8
     assert np.mean(gdx[sure] == odx[sure]) > 0.999
 
-    terms = np.abs(dyf * xf * r[:, None]).sum(axis=0)
-    chunks = (M + 127) // 128
-    dg_bound = 2 * ((3 * 128 + chunks) * U * terms + U * np.abs(odg))
-    assert np.all(np.abs(h(dg).astype(np.float64) - odg) <= dg_bound)
+    assert np.all(np.abs(h(dg).astype(np.float64) - odg) <= dg_bound_of(odg))
 
 
 def test_rmsnorm_bwd_is_deterministic(dev):
