@@ -86,6 +86,12 @@ __device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, ui
       : "memory");
 }
 
+// Asks L2 to fetch `bytes` (a multiple of 16) from global address src (16-byte
+// aligned); nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Tiled 2-D copy of one box at (x, y) (x in elements of the innermost
 // dimension; x·element size a multiple of 16 bytes).
 __device__ __forceinline__ void tma_g2s_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,

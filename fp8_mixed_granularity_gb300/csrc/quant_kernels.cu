@@ -1044,9 +1044,10 @@ k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gam
 //   ∇γ_j = Σ_rows dy_j·x_j·r
 // ∇x: one warp per row, 8 lanes per 128-wide group as in R1; the row sum is
 // accumulated like R1's Σx² (16-term FP32 chunk sums per lane, lanes in FP64).
-// ∇γ: deterministic two-stage column sums — FP32 partial sums over 128-row
-// chunks into the caller's workspace [chunks][H], then each column's partials
-// added in a fixed order in FP64.
+// Rows up to 4096 wide run the fused kernel below (∇x and the ∇γ partial sums
+// in one pass over x and ∇y).  Wider rows: ∇γ by deterministic two-stage column
+// sums — FP32 partial sums over 128-row chunks into the caller's workspace
+// [chunks][H], then each column's partials added in a fixed order in FP64.
 // ---------------------------------------------------------------------------
 constexpr int kNormBwdRows = 128;   // rows per ∇γ partial sum
 
@@ -1137,6 +1138,136 @@ k_rmsnorm_bwd_dgamma_partial(const uint16_t* __restrict__ x, const float* __rest
       ay = __fadd_rn(ay, __fmul_rn(__fmul_rn(fd.y, fx.y), r));
     }
     *reinterpret_cast<float2*>(ws + (size_t)p * H + col) = make_float2(ax, ay);
+  }
+}
+
+// The fused backward for rows up to 4096 wide: W warps per CTA, one CTA per SM
+// (the accumulators fill shared memory), warp w of CTA b owning the rows
+// b·W + w + k·W·gridDim.  Each row's ∇x is formed exactly as by
+// k_rmsnorm_bwd_dx (x and ∇y are read twice; few enough rows are in flight for
+// the second read to come from L2), and its ∇γ terms RN(RN(dy·x)·r) are added,
+// in row order, to the warp's own FP32 accumulator row in shared memory.  At the
+// end the CTA adds its W rows in warp order (FP32) into its workspace row; the
+// CTA rows are then added in a fixed order in FP64 (k_rmsnorm_bwd_dgamma_reduce).
+// An accumulator row keeps lane l8's 16 columns 128g + 16·l8 + 4i + (0..3) at
+// 128g + 32i + 4·l8 + (0..3), so the eight lanes of a group touch 128
+// consecutive bytes per access.
+constexpr uint32_t kNormBwdMaxCtas = 152;   // workspace rows: at most one per CTA
+
+template <int W>
+__global__ void __launch_bounds__(32 * W, 1)
+k_rmsnorm_bwd_fused(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
+                    const float* __restrict__ rstd, const uint16_t* __restrict__ dy, uint32_t M,
+                    uint32_t H, double inv_h, uint16_t* __restrict__ dx, float* __restrict__ ws) {
+  extern __shared__ __align__(16) float acc_s[];   // [W][H]
+  constexpr int U = 4;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u, g4 = lane >> 3, l8 = lane & 7u;
+  const uint32_t GW = gridDim.x * W;
+  const uint32_t groups = H / 128;
+  float* acc = acc_s + (size_t)warp * H;
+  for (uint32_t i = 4 * lane; i < H; i += 128) *reinterpret_cast<float4*>(acc + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncwarp();
+  uint64_t pol_keep, pol_drop;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_drop));
+  // each warp asks L2 for its next row of x and ∇y while it works on the
+  // current one, so DRAM keeps streaming through the row's FP64 step and second
+  // pass (measured at 16384 × 4096: 108 µs one row ahead, 130 two rows ahead,
+  // 133 without; the three-kernel path 137)
+  auto prefetch_row = [&](uint32_t row) {
+    if (lane == 0 && row < M) {
+      bulk_prefetch_l2(x + (size_t)row * H, H * 2u);
+      bulk_prefetch_l2(dy + (size_t)row * H, H * 2u);
+    }
+  };
+  prefetch_row(blockIdx.x * W + warp);
+  for (uint32_t row = blockIdx.x * W + warp; row < M; row += GW) {
+    const uint16_t* xr = x + (size_t)row * H;
+    const uint16_t* dr = dy + (size_t)row * H;
+    prefetch_row(row + GW);
+    float dot = 0.0f;
+    for (uint32_t g0 = 0; g0 < groups; g0 += 4 * U) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t grp = g0 + 4 * u + g4;
+        if (grp >= groups) continue;
+        uint32_t rx[8], rd[8], rg[8];
+        ld32_policy(xr + grp * 128 + l8 * 16, rx, pol_keep);
+        ld32_policy(dr + grp * 128 + l8 * 16, rd, pol_keep);
+        ld32_cached(gamma + grp * 128 + l8 * 16, rg);
+        float cs = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const float2 fx = bf2_to_f2(rx[w]), fd = bf2_to_f2(rd[w]), fg = bf2_to_f2(rg[w]);
+          cs = __fmaf_rn(__fmul_rn(fd.x, fg.x), fx.x, cs);
+          cs = __fmaf_rn(__fmul_rn(fd.y, fg.y), fx.y, cs);
+        }
+        dot = __fadd_rn(dot, cs);
+      }
+    }
+    double d = (double)dot;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(kFull, d, o);
+    const float r = rstd[row];
+    float c = 0.0f;
+    // (1/H in FP64: a relative error of 2^-53, far below c's FP32 rounding)
+    if (lane == 0) c = (float)((double)r * (double)r * (double)r * d * inv_h);
+    c = __shfl_sync(kFull, c, 0);
+    constexpr int U2 = 4;   // groups per lane whose loads are in flight together
+    for (uint32_t g0 = 0; g0 < groups; g0 += 4 * U2) {
+      uint32_t rx[U2][8], rd[U2][8], rg[U2][8];
+#pragma unroll
+      for (int u = 0; u < U2; ++u) {
+        const uint32_t grp = g0 + 4 * u + g4;
+        if (grp >= groups) continue;
+        ld32_policy(xr + grp * 128 + l8 * 16, rx[u], pol_drop);
+        ld32_policy(dr + grp * 128 + l8 * 16, rd[u], pol_drop);
+        ld32_cached(gamma + grp * 128 + l8 * 16, rg[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < U2; ++u) {
+        const uint32_t grp = g0 + 4 * u + g4;
+        if (grp >= groups) continue;
+        uint32_t out[8];
+        float t[16];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const float2 fx = bf2_to_f2(rx[u][w]), fd = bf2_to_f2(rd[u][w]), fg = bf2_to_f2(rg[u][w]);
+          const float a = __fsub_rn(__fmul_rn(r, __fmul_rn(fd.x, fg.x)), __fmul_rn(fx.x, c));
+          const float b = __fsub_rn(__fmul_rn(r, __fmul_rn(fd.y, fg.y)), __fmul_rn(fx.y, c));
+          out[w] = f2_to_bf2(a, b);
+          t[2 * w] = __fmul_rn(__fmul_rn(fd.x, fx.x), r);
+          t[2 * w + 1] = __fmul_rn(__fmul_rn(fd.y, fx.y), r);
+        }
+        st32(dx + (size_t)row * H + grp * 128 + l8 * 16, out);
+        float* ap = acc + grp * 128 + 4 * l8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float4 v = *reinterpret_cast<float4*>(ap + 32 * i);
+          v.x = __fadd_rn(v.x, t[4 * i]);
+          v.y = __fadd_rn(v.y, t[4 * i + 1]);
+          v.z = __fadd_rn(v.z, t[4 * i + 2]);
+          v.w = __fadd_rn(v.w, t[4 * i + 3]);
+          *reinterpret_cast<float4*>(ap + 32 * i) = v;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // stored index s = 128g + 32i + 4l + e holds column 128g + 16l + 4i + e
+  float* wrow = ws + (size_t)blockIdx.x * H;
+  for (uint32_t s4 = 4 * threadIdx.x; s4 < H; s4 += 4 * 32 * W) {
+    float4 v = *reinterpret_cast<const float4*>(acc_s + s4);
+#pragma unroll
+    for (int w = 1; w < W; ++w) {
+      const float4 u = *reinterpret_cast<const float4*>(acc_s + (size_t)w * H + s4);
+      v.x = __fadd_rn(v.x, u.x);
+      v.y = __fadd_rn(v.y, u.y);
+      v.z = __fadd_rn(v.z, u.z);
+      v.w = __fadd_rn(v.w, u.w);
+    }
+    const uint32_t g = s4 >> 7, i = (s4 >> 5) & 3u, l = (s4 >> 2) & 7u;
+    *reinterpret_cast<float4*>(wrow + 128 * g + 16 * l + 4 * i) = v;
   }
 }
 
@@ -1394,8 +1525,36 @@ cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, in
   return cudaGetLastError();
 }
 
+// Warps per CTA of the fused backward (0: rows too wide, the three-kernel path).
+inline int norm_bwd_warps(int64_t H) { return H <= 4096 ? 8 : 0; }
+// Workspace rows of the fused backward: one per CTA (at most kNormBwdMaxCtas).
+inline int64_t norm_bwd_ctas(int64_t M, int64_t H) {
+  const int64_t w = norm_bwd_warps(H), need = (M + w - 1) / w;
+  return need < (int64_t)kNormBwdMaxCtas ? need : (int64_t)kNormBwdMaxCtas;
+}
+
 size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H) {
+  if (norm_bwd_warps(H) > 0) return (size_t)norm_bwd_ctas(M, H) * (size_t)H * sizeof(float);
   return (size_t)((M + kNormBwdRows - 1) / kNormBwdRows) * (size_t)H * sizeof(float);
+}
+
+template <int W>
+cudaError_t launch_rmsnorm_bwd_fused(const uint16_t* x, const uint16_t* gamma, const float* rstd,
+                                     const uint16_t* dy, int64_t M, int64_t H, uint16_t* dx,
+                                     float* dgamma, float* ws, cudaStream_t st) {
+  auto kern = k_rmsnorm_bwd_fused<W>;
+  const int smem = W * (int)H * (int)sizeof(float);
+  // (opted in once per device at the widest rows the instance serves, 4096)
+  static int done[64] = {0};
+  cudaError_t e = opt_in_smem(kern, W * 4096 * (int)sizeof(float), done);
+  if (e != cudaSuccess) return e;
+  int64_t ctas = norm_bwd_ctas(M, H);
+  if (ctas > num_sms()) ctas = num_sms();
+  kern<<<(unsigned)ctas, 32 * W, smem, st>>>(x, gamma, rstd, dy, (uint32_t)M, (uint32_t)H, 1.0 / (double)H, dx,
+                                             ws);
+  k_rmsnorm_bwd_dgamma_reduce<<<(unsigned)((H + 31) / 32), kThreads, 0, st>>>(ws, (uint32_t)ctas,
+                                                                            (uint32_t)H, dgamma);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_bwd(const void* x, const void* gamma, const float* rstd, const void* dy,
@@ -1403,6 +1562,9 @@ cudaError_t launch_rmsnorm_bwd(const void* x, const void* gamma, const float* rs
                                cudaStream_t st) {
   const auto* xb = static_cast<const uint16_t*>(x);
   const auto* db = static_cast<const uint16_t*>(dy);
+  const auto* gb = static_cast<const uint16_t*>(gamma);
+  auto* dxb = static_cast<uint16_t*>(dx);
+  if (norm_bwd_warps(H) == 8) return launch_rmsnorm_bwd_fused<8>(xb, gb, rstd, db, M, H, dxb, dgamma, ws, st);
   const unsigned grid = grid_for((size_t)M, kThreads / 32, 8);
   k_rmsnorm_bwd_dx<<<grid, kThreads, 0, st>>>(xb, static_cast<const uint16_t*>(gamma), rstd, db,
                                               (uint32_t)M, (uint32_t)H, static_cast<uint16_t*>(dx));

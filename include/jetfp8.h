@@ -299,13 +299,18 @@ jetfp8_status jetfp8_gemm_fprop_nvfp4(const uint8_t* xq, const uint8_t* xsf, con
  * pages fuse the forward only; this is the exact derivative of R1's
  * y = (x·r)·γ, r = 1/sqrt(mean(x²) + eps), using the r that R1 saved):
  *   ∇x_i = r·(dy_i·γ_i) − x_i·r³·(Σ_j dy_j·γ_j·x_j)/H       (FP32, rounded to bf16)
- *   ∇γ_j = Σ_rows dy_j·x_j·r                                 (deterministic: FP32 sums
- *          over 128-row chunks, chunks added in a fixed order in FP64)
+ *   ∇γ_j = Σ_rows dy_j·x_j·r                                 (deterministic on a given
+ *          GPU: rows up to 4096 wide — FP32 sums over the rows each warp of a
+ *          persistent CTA owns, the CTA's 8 warps added in warp order in FP32, the
+ *          CTAs' sums added in a fixed order in FP64; wider rows — FP32 sums over
+ *          128-row chunks, chunks added in a fixed order in FP64)
  *   x bf16 [M, H], gamma bf16 [H], rstd fp32 [M] (R1's output), dy bf16 [M, H]
  *   dx bf16 [M, H], dgamma fp32 [H]
  *   workspace: caller-owned device memory of at least
  *              jetfp8_rmsnorm_bwd_workspace_bytes(M, H) bytes (16-byte aligned),
- *              overwritten by the call; JETFP8_ERR_INVALID_ARG if smaller.
+ *              overwritten by the call; JETFP8_ERR_INVALID_ARG if smaller.  The
+ *              size is min(ceil(M/8), 152)·H·4 bytes for H <= 4096 and
+ *              ceil(M/128)·H·4 bytes for wider rows.
  * H multiple of 128, M >= 1. */
 size_t jetfp8_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H);
 jetfp8_status jetfp8_rmsnorm_bwd(const void* x_bf16, const void* gamma_bf16, const float* rstd,
@@ -320,7 +325,8 @@ jetfp8_status jetfp8_rmsnorm_bwd(const void* x_bf16, const void* gamma_bf16, con
  * memory.  Results equal jetfp8_rmsnorm_bwd's bit for bit.
  *   Arguments as jetfp8_rmsnorm_bwd without workspace / workspace_bytes.
  *   JETFP8_ERR_UNSUPPORTED_SHAPE when jetfp8_rmsnorm_bwd_workspace_bytes(M, H)
- *   exceeds 8 MiB (ceil(M/128)·H·4 bytes; e.g. M <= 65536 rows at H = 4096).
+ *   exceeds 8 MiB, which only rows wider than 4096 can reach (ceil(M/128)·H·4
+ *   bytes; e.g. M <= 16384 rows at H = 16384, M <= 32768 at H = 8192).
  *   All calls share the one scratch array: calls that overlap in time (on
  *   other streams or from other host threads) race and must be serialised by
  *   the caller; calls on one stream are ordered and safe. */

@@ -66,7 +66,10 @@ def rmsnorm_bwd_bounds(xf, gf, r, dyf):
     dy): the exact ∇x before rounding and the per-element bound on the kernel's
     FP32 evaluation error (each FP32 operation rounded separately, row sums as
     16-term FP32 chunks added in FP32 and combined in FP64; factor 2 margin),
-    and the bound on ∇γ (FP32 sums over 128-row chunks added in FP64)."""
+    and the bound on ∇γ.  ∇γ is an FP32 chain over at most 128 rows per partial
+    (a 128-row chunk, or one warp's rows plus the warps of its CTA; each term
+    two roundings) and FP64 additions of the partials: (3·128 + partials)
+    roundings per term covers both with rows per warp below 370."""
     U = 2.0 ** -24
     M, H = xf.shape
     gdy = dyf * gf[None, :]

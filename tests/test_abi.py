@@ -73,9 +73,13 @@ def test_validation_rejects_before_touching_the_device(lib):
     # RMSNorm backward: workspace size and a too-small workspace
     lib.jetfp8_rmsnorm_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.jetfp8_rmsnorm_bwd_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
-    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(300, 256) == 3 * 256 * 4
+    # rows up to 4096 wide: one workspace row per CTA of 8 warps (at most 152 CTAs)
+    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(300, 256) == 38 * 256 * 4
+    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(100000, 4096) == 152 * 4096 * 4
+    # wider rows: one workspace row per 128-row chunk
+    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(300, 8192) == 3 * 8192 * 4
     assert lib.jetfp8_rmsnorm_bwd(P(64), P(64), P(64), P(64), ctypes.c_int64(300), ctypes.c_int64(256),
-                                  P(64), P(64), P(64), ctypes.c_size_t(3 * 256 * 4 - 4), None) == 1
+                                  P(64), P(64), P(64), ctypes.c_size_t(38 * 256 * 4 - 4), None) == 1
     # WGrad needs M multiple of 128
     assert lib.jetfp8_gemm_wgrad(P(64), P(64), P(64), P(64), 100, 128, 128, P(64), 0, None) == 2
     # non-positive M
@@ -95,20 +99,22 @@ def test_noalloc_rejects_scratch_above_8mib(lib):
     fn.argtypes = [P, P, P, P, I64, I64, P, P, P]
     lib.jetfp8_rmsnorm_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.jetfp8_rmsnorm_bwd_workspace_bytes.argtypes = [I64, I64]
-    H = 4096
-    # 512 chunks of 128 rows × 4096 columns × 4 B is exactly 8 MiB; one more row is too many
-    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(128 * 512, H) == (8 << 20)
-    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(128 * 512 + 1, H) > (8 << 20)
+    # rows up to 4096 wide never need more than 152 rows of at most 4096 floats
+    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(1 << 24, 4096) == 152 * 4096 * 4
+    H = 16384
+    # 128 chunks of 128 rows × 16384 columns × 4 B is exactly 8 MiB; one more row is too many
+    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(128 * 128, H) == (8 << 20)
+    assert lib.jetfp8_rmsnorm_bwd_workspace_bytes(128 * 128 + 1, H) > (8 << 20)
     A = P(1 << 20)
-    assert fn(A, A, A, A, 128 * 512 + 1, H, A, A, None) == 2      # JETFP8_ERR_UNSUPPORTED_SHAPE
+    assert fn(A, A, A, A, 128 * 128 + 1, H, A, A, None) == 2      # JETFP8_ERR_UNSUPPORTED_SHAPE
     # the largest size passes the size check and stops at the device check (no GPU here)
-    assert fn(A, A, A, A, 128 * 512, H, A, A, None) == 4          # JETFP8_ERR_CUDA
+    assert fn(A, A, A, A, 128 * 128, H, A, A, None) == 4          # JETFP8_ERR_CUDA
 
 
 def test_rmsnorm_bwd_many_row_chunks_validated(lib):
-    """A shape with more 128-row chunks than a grid's y dimension holds
-    (65535) is accepted by validation: the partial-sum kernel loops over its
-    chunks.  Here validation stops at the device check (no GPU)."""
+    """A shape with many rows at a narrow width (more than 65535 128-row chunks,
+    the grid's y limit of the wide-row path) is accepted by validation.  Here
+    validation stops at the device check (no GPU)."""
     if __import__("torch").cuda.is_available():
         pytest.skip("placeholder addresses: only where no GPU can be reached")
     P, I64, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
