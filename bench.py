@@ -296,11 +296,11 @@ def gemm_sources_digest():
 
 def launch_medians(events_per_step):
     """{(linear, kind): median launch ms} over the timed steps.  Each step's
-    events are a list of (linear, kind, start, end)."""
+    launches are a list of (linear, kind, ms)."""
     per = {}
     for evs in events_per_step:
-        for lname, kind, s, e in evs:
-            per.setdefault((lname, kind), []).append(s.elapsed_time(e))
+        for lname, kind, ms in evs:
+            per.setdefault((lname, kind), []).append(ms)
     return {k: float(np.median(v)) for k, v in per.items()}, {k: len(v) for k, v in per.items()}
 
 
@@ -321,7 +321,7 @@ def run_ours(args):
     g.build()
     from fp8_mixed_granularity_gb300 import jetfp8 as J
     from fp8_mixed_granularity_gb300 import workloads as W
-    from fp8_mixed_granularity_gb300.linear import LinearBuffers, quant_weights_grouped
+    from fp8_mixed_granularity_gb300.linear import EventLog, LinearBuffers, quant_weights_grouped
 
     lins = W.llama8b_training()
     norm_fed = {"qkv", "gate_up"}
@@ -342,12 +342,12 @@ def run_ours(args):
         # its WGrad as a launch of its own (four single WGrads measure faster
         # than the grouped launch of the four: 1.97 vs 2.10 ms).  With `events`
         # (a list), every launch is bracketed by CUDA events on its stream.
-        ev = None if events is None else []
+        ev = None if events is None else type(events)()
         n = quant_weights_grouped(bufs, [inp[1] for inp in inputs], events=ev)
         if events is not None:
             events.extend((GROUPED, kind, s, e) for kind, s, e in ev)
         for b, (x, w, dy, gamma) in zip(bufs, inputs):
-            ev = None if events is None else []
+            ev = None if events is None else type(events)()
             n += b.forward(x, None, gamma, events=ev)
             n += b.backward(dy, events=ev)
             if events is not None:
@@ -390,16 +390,41 @@ def run_ours(args):
     torch.cuda.synchronize()
     host_t1 = time.time()
     launches = per_step * args.steps
-    # --- then K eager steps with CUDA events around every launch (the breakdown) ---
+    # --- then the breakdown: the step captured again with a CUDA event-record
+    # node around every launch, replayed K times (each replay's times read before
+    # the next); where this torch cannot put events in a graph, K eager steps
+    # with CUDA events around every launch ---
+    breakdown_how = "graph"
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        breakdown_how = "eager"
+    if breakdown_how == "graph":
+        graph_ev = torch.cuda.CUDAGraph()
+        captured = EventLog()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph_ev, stream=cap):
+                step(captured)
+        torch.cuda.current_stream().wait_stream(cap)
+        graph_ev.replay()
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            graph_ev.replay()
+            torch.cuda.synchronize()
+            events_per_step.append([(ln, kind, s.elapsed_time(e)) for ln, kind, s, e in captured])
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
+    eager_events = []
     for _ in range(args.steps):
         ev = []
         step(ev)
-        events_per_step.append(ev)
+        eager_events.append(ev)
     e1.record()
     torch.cuda.synchronize()
+    if breakdown_how == "eager":
+        events_per_step = [[(ln, kind, s.elapsed_time(e)) for ln, kind, s, e in ev] for ev in eager_events]
     sampler.mark(host_t0, time.time())
     clocks = sampler.stop()
     if world > 1:
@@ -471,8 +496,10 @@ def run_ours(args):
             "all_gemm_launches": {"achieved": gemm_tflops, "frac": gemm_tflops / fp8_peak},
         },
         "breakdown": {
-            "timing": ("median of each launch over K eager steps run right after the graph-timed region "
-                       "(CUDA events on the launching stream around every launch)"),
+            "timing": ("median of each launch over K replays of the step captured as a CUDA graph with an "
+                       "event-record node around every launch" if breakdown_how == "graph" else
+                       "median of each launch over K eager steps (CUDA events on the launching stream "
+                       "around every launch)"),
             "eager_ms_per_step": eager_ms,
             "gemm_tflops": {k: layer_flops / (v * 1e-3) / 1e12 for k, v in gemm_ms.items()},
             "gemm_frac": {k: layer_flops / (v * 1e-3) / 1e12 / fp8_peak for k, v in gemm_ms.items()},

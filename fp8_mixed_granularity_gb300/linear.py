@@ -112,6 +112,12 @@ def wgrad_grouped(bufs, stream=None, events=None) -> int:
     return n
 
 
+class EventLog(list):
+    """A list for `events` whose CUDA events are created as graph event-record
+    nodes (`external`), for timing launches inside a captured CUDA graph."""
+    external = True
+
+
 def _timed(events, name, fn, stream=None):
     """Run fn, which launches on `stream` (None: the current stream); if
     `events` (a list) is given, bracket it with CUDA events recorded on that
@@ -120,8 +126,9 @@ def _timed(events, name, fn, stream=None):
         fn()
         return
     st = torch.cuda.current_stream() if stream is None else stream
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
+    kw = {"external": True} if getattr(events, "external", False) else {}
+    s = torch.cuda.Event(enable_timing=True, **kw)
+    e = torch.cuda.Event(enable_timing=True, **kw)
     s.record(st)
     fn()
     e.record(st)
