@@ -209,9 +209,36 @@ __device__ __forceinline__ uint32_t codes4_negbf16(uint32_t nw0, uint32_t nw1, c
   return c;
 }
 
-// The same for the bf16 values themselves in w0 (values 0, 1) and w1 (values 2, 3).
+// The same for the bf16 values themselves in w0 (values 0, 1) and w1 (values 2, 3):
+// each negated FP32 value in one integer operation, (w << 16) + 2^31 for the low
+// half (adding 2^31 modulo 2^32 flips bit 31) and (w & 0xFFFF0000) ^ 2^31 for the
+// high half (lop3, table 0x6A = (a & b) ^ c).
 __device__ __forceinline__ uint32_t codes4_bf16(uint32_t w0, uint32_t w1, const QScale& g) {
-  return codes4_negbf16(w0 ^ 0x80008000u, w1 ^ 0x80008000u, g);
+  uint32_t c;
+  asm("{\n\t.reg .b32 a0, a1, a2, a3;\n\t.reg .b64 x0, x1, q0, q1, r0, r1;\n\t.reg .b16 l, h;\n\t"
+      "mad.lo.u32 a0, %1, 65536, 0x80000000;\n\t"
+      "lop3.b32 a1, %1, 0xFFFF0000, 0x80000000, 0x6A;\n\t"
+      "mad.lo.u32 a2, %2, 65536, 0x80000000;\n\t"
+      "lop3.b32 a3, %2, 0xFFFF0000, 0x80000000, 0x6A;\n\t"
+      "mov.b64 x0, {a0, a1};\n\t"
+      "mov.b64 x1, {a2, a3};\n\t"
+      "mul.rn.f32x2 q0, x0, %4;\n\t"
+      "mul.rn.f32x2 q1, x1, %4;\n\t"
+      "fma.rn.f32x2 r0, q0, %3, x0;\n\t"
+      "fma.rn.f32x2 r1, q1, %3, x1;\n\t"
+      "fma.rn.f32x2 q0, r0, %4, q0;\n\t"
+      "fma.rn.f32x2 q1, r1, %4, q1;\n\t"
+      "fma.rn.f32x2 r0, q0, %3, x0;\n\t"
+      "fma.rn.f32x2 r1, q1, %3, x1;\n\t"
+      "fma.rn.f32x2 q0, r0, %4, q0;\n\t"
+      "fma.rn.f32x2 q1, r1, %4, q1;\n\t"
+      "mov.b64 {a0, a1}, q0;\n\t"
+      "mov.b64 {a2, a3}, q1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, a1, a0;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h, a3, a2;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(c) : "r"(w0), "r"(w1), "l"(g.s2), "l"(g.ny2));
+  return c;
 }
 
 // The same for FP32 values given negated as two packed pairs (nx0 = (-v0, -v1),

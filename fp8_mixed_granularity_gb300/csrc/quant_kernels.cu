@@ -250,40 +250,42 @@ __device__ __forceinline__ void load_group16(uint32_t gb, uint32_t l8, uint32_t 
   w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
 
-// One lane's 16 bf16 values of a group, given negated (8 packed words of -x):
-// the group's maximum over its 8 lanes, its scale, and the 16 codes of x as
-// (first half, second half).
-__device__ __forceinline__ void group16_codes_neg(const uint32_t (&nw)[8], bool valid, float& S, uint2& c0,
-                                                  uint2& c1) {
-  uint32_t m = amax2(amax2(amax2(nw[0], nw[1]), amax2(nw[2], nw[3])), amax2(amax2(nw[4], nw[5]), amax2(nw[6], nw[7])));
+// One lane's 16 bf16 values of a group (8 packed words; of -x when NEG, of x
+// otherwise): the group's maximum over its 8 lanes, its scale, and the 16 codes
+// of x as (first half, second half).
+template <bool NEG>
+__device__ __forceinline__ void group16_codes_of(const uint32_t (&w)[8], bool valid, float& S, uint2& c0,
+                                                 uint2& c1) {
+  uint32_t m = amax2(amax2(amax2(w[0], w[1]), amax2(w[2], w[3])), amax2(amax2(w[4], w[5]), amax2(w[6], w[7])));
   m &= 0x7FFF7FFFu;
   float amax = valid ? fmaxf(bf_lo(m), bf_hi(m)) : 0.0f;
   amax = group8_max(amax);
   S = make_scale(amax).s;
   uint32_t c[4];
   if (amax != 0.0f && amax < kQuotientMinAmax) {
-    constexpr float k96 = 0x1p96f;
-    const QScale g = qscale_from_s(S * k96, false);
+    constexpr float k96 = NEG ? 0x1p96f : -0x1p96f;   // the scaled negated values
+    const QScale g = qscale_from_s(S * 0x1p96f, false);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float2 a = bf2_to_f2(nw[2 * k]), b = bf2_to_f2(nw[2 * k + 1]);
+      const float2 a = bf2_to_f2(w[2 * k]), b = bf2_to_f2(w[2 * k + 1]);
       c[k] = codes4_neg_f32(pack_f2(a.x * k96, a.y * k96), pack_f2(b.x * k96, b.y * k96), g);
     }
   } else {
     const QScale g = qscale_from_s(S, false);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) c[k] = codes4_negbf16(nw[2 * k], nw[2 * k + 1], g);
+    for (int k = 0; k < 4; ++k)
+      c[k] = NEG ? codes4_negbf16(w[2 * k], w[2 * k + 1], g) : codes4_bf16(w[2 * k], w[2 * k + 1], g);
   }
   c0 = make_uint2(c[0], c[1]);
   c1 = make_uint2(c[2], c[3]);
 }
 
-// The same for the values themselves (8 packed words of x).
+__device__ __forceinline__ void group16_codes_neg(const uint32_t (&nw)[8], bool valid, float& S, uint2& c0,
+                                                  uint2& c1) {
+  group16_codes_of<true>(nw, valid, S, c0, c1);
+}
 __device__ __forceinline__ void group16_codes(const uint32_t (&w)[8], bool valid, float& S, uint2& c0, uint2& c1) {
-  uint32_t nw[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) nw[k] = w[k] ^ 0x80008000u;
-  group16_codes_neg(nw, valid, S, c0, c1);
+  group16_codes_of<false>(w, valid, S, c0, c1);
 }
 
 // c plus the squares of one lane's 16 bf16 values (8 packed words), added in
