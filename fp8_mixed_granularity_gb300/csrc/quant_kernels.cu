@@ -138,27 +138,6 @@ __device__ __forceinline__ float h2f(uint16_t b) {
   return f;
 }
 
-// Quotient constants of 8 groups whose maxima every lane of a half-warp holds
-// (amax[i] for group i): lane l computes group (l mod 8)'s S and -RN(1/S),
-// and the half-warp shares them by shuffle; bit i of the returned mask marks
-// group i as slow (0 < amax < kQuotientMinAmax).
-__device__ __forceinline__ uint32_t half_warp_qscales(const float (&amax)[8], float (&s)[8], float (&ny)[8]) {
-  const uint32_t lane = threadIdx.x & 31u, me = lane & 7u, base = lane & 16u;
-  float a = amax[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) a = (me == (uint32_t)i) ? amax[i] : a;
-  const float s_mine = make_scale(a).s;
-  const float ny_mine = -__frcp_rn(s_mine);
-  const bool slow = a != 0.0f && a < kQuotientMinAmax;
-  const uint32_t mask = (__ballot_sync(kFull, slow) >> base) & 0xFFu;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    s[i] = __shfl_sync(kFull, s_mine, base + i);
-    ny[i] = __shfl_sync(kFull, ny_mine, base + i);
-  }
-  return mask;
-}
-
 // Max over the 16 lanes of a half-warp of 8 per-lane column values a[0..7],
 // returned in the lane l of column l mod 8.  Each exchange step hands the
 // partner the half of the columns it keeps (lane bit 0 picks the column's bit 0,
@@ -182,8 +161,10 @@ __device__ __forceinline__ float half_warp_colmax8(const float (&a)[8]) {
   return fmaxf(r3, __shfl_xor_sync(kFull, r3, 8));
 }
 
-// half_warp_qscales for maxima already reduced so that lane l holds group
-// (l mod 8)'s maximum.
+// Quotient constants of 8 groups whose maxima are already reduced so that lane
+// l holds group (l mod 8)'s: lane l computes that group's S and -RN(1/S), and the
+// half-warp shares them by shuffle; bit i of the returned mask marks group i as
+// slow (0 < amax < kQuotientMinAmax).
 __device__ __forceinline__ uint32_t half_warp_qscales_of(float a, float (&s)[8], float (&ny)[8]) {
   const uint32_t base = threadIdx.x & 16u;
   const float s_mine = make_scale(a).s;
@@ -626,39 +607,77 @@ __device__ __forceinline__ void load_cols_bf16(uint32_t sbase, uint32_t tid, uin
   }
 }
 
-// Max over the 16 lanes of a half-warp of packed bf16 magnitudes.
-__device__ __forceinline__ uint32_t half_warp_amax2(uint32_t v) {
+// Maxima over a half-warp of 8 per-lane values held as 4 packed bf16 pairs
+// r[k] = (value 2k, value 2k + 1) (magnitudes; sign bits not meaningful),
+// reduced transposed: each exchange hands the partner the half of the values it
+// keeps, so 5 shuffles replace 16.  Lane l (bits b0, b1, b2 of l) ends with the
+// maximum of value 4·b1 + 2·b0 + b2; value i sits in lane half_warp_lane_of(i).
+__device__ __forceinline__ float half_warp_max8_packed(const uint32_t (&r)[4]) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const bool b0 = lane & 1u, b1 = lane & 2u, b2 = lane & 4u;
+  uint32_t r1[2];
 #pragma unroll
-  for (int o = 8; o >= 1; o >>= 1) v = amax2(v, __shfl_xor_sync(kFull, v, o));
-  return v & 0x7FFF7FFFu;
-}
-
-// Row pass: the 8 rows' group maxima (each row's 128-column group spans the
-// half-warp) as floats.
-__device__ __forceinline__ void row_group_amax(const uint32_t (&w)[8][4], float (&amax)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    const uint32_t m0 = amax2(amax2(w[i][0], w[i][1]), amax2(w[i][2], w[i][3]));
-    const uint32_t m1 = amax2(amax2(w[i + 1][0], w[i + 1][1]), amax2(w[i + 1][2], w[i + 1][3]));
-    // rows i (low half) and i+1 (high half): low halves against high halves
-    const uint32_t a = half_warp_amax2(amax2(__byte_perm(m0, m1, 0x5410), __byte_perm(m0, m1, 0x7632)));
-    amax[i] = bf_lo(a);
-    amax[i + 1] = bf_hi(a);
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t keep = b0 ? r[2 * j + 1] : r[2 * j], send = b0 ? r[2 * j] : r[2 * j + 1];
+    r1[j] = amax2(keep, __shfl_xor_sync(kFull, send, 1));
   }
+  const uint32_t keep = b1 ? r1[1] : r1[0], send = b1 ? r1[0] : r1[1];
+  const uint32_t r2 = amax2(keep, __shfl_xor_sync(kFull, send, 2)) & 0x7FFF7FFFu;
+  const float lo = bf_lo(r2), hi = bf_hi(r2);
+  const float r3 = fmaxf(b2 ? hi : lo, __shfl_xor_sync(kFull, b2 ? lo : hi, 4));
+  return fmaxf(r3, __shfl_xor_sync(kFull, r3, 8));
+}
+__host__ __device__ constexpr uint32_t half_warp_lane_of(int i) {
+  return (uint32_t)(((i >> 1) & 1) | ((i >> 2) << 1) | ((i & 1) << 2));
 }
 
-// Column pass: the maxima of the thread's 8 columns over the 128 rows of the
-// tile (the column group spans the half-warp).
-__device__ __forceinline__ void col_group_amax(const uint32_t (&w)[8][4], float (&amax)[8]) {
+// Group constants of 8 groups whose maxima half_warp_max8_packed left one per
+// lane: lane l computes its group's S and -RN(1/S), the half-warp shares them by
+// shuffle; bit i of the returned mask marks group i as slow.
+__device__ __forceinline__ uint32_t half_warp_qscales_packed(float a, float (&s)[8], float (&ny)[8]) {
+  const uint32_t base = threadIdx.x & 16u;
+  const float s_mine = make_scale(a).s;
+  const float ny_mine = -__frcp_rn(s_mine);
+  const uint32_t bits = (__ballot_sync(kFull, a != 0.0f && a < kQuotientMinAmax) >> base) & 0xFFu;
+  uint32_t mask = 0;
+  if (bits) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mask |= ((bits >> half_warp_lane_of(i)) & 1u) << i;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    s[i] = __shfl_sync(kFull, s_mine, base + half_warp_lane_of(i));
+    ny[i] = __shfl_sync(kFull, ny_mine, base + half_warp_lane_of(i));
+  }
+  return mask;
+}
+
+// Row pass: the constants of the 8 rows' groups (each row's 128-column group
+// spans the half-warp).
+__device__ __forceinline__ uint32_t row_group_qscales(const uint32_t (&w)[8][4], float (&s)[8], float (&ny)[8]) {
+  uint32_t r[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t m0 = amax2(amax2(w[2 * k][0], w[2 * k][1]), amax2(w[2 * k][2], w[2 * k][3]));
+    const uint32_t m1 = amax2(amax2(w[2 * k + 1][0], w[2 * k + 1][1]), amax2(w[2 * k + 1][2], w[2 * k + 1][3]));
+    // rows 2k (low half) and 2k+1 (high half): low halves against high halves
+    r[k] = amax2(__byte_perm(m0, m1, 0x5410), __byte_perm(m0, m1, 0x7632));
+  }
+  return half_warp_qscales_packed(half_warp_max8_packed(r), s, ny);
+}
+
+// Column pass: the constants of the thread's 8 columns' groups (the maxima over
+// the 128 rows of the tile; a column group spans the half-warp).
+__device__ __forceinline__ uint32_t col_group_qscales(const uint32_t (&w)[8][4], float (&s)[8], float (&ny)[8]) {
+  uint32_t r[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t m = w[0][c];
 #pragma unroll
     for (int i = 1; i < 8; ++i) m = amax2(m, w[i][c]);
-    m = half_warp_amax2(m);
-    amax[2 * c] = bf_lo(m);
-    amax[2 * c + 1] = bf_hi(m);
+    r[c] = m;
   }
+  return half_warp_qscales_packed(half_warp_max8_packed(r), s, ny);
 }
 
 // Codes of the 8 rows of a row-pass block under per-row constants (s[i],
@@ -730,9 +749,8 @@ k_quant_grad_dual_tma(const __grid_constant__ CUtensorMap map, const Q4Args a) {
     {  // row groups
       uint32_t w[8][4];
       load_rows_bf16(sb, tid, w);
-      float amax[8], sc[8], ny[8];
-      row_group_amax(w, amax);
-      const uint32_t slow = half_warp_qscales(amax, sc, ny);
+      float sc[8], ny[8];
+      const uint32_t slow = row_group_qscales(w, sc, ny);
       const uint32_t rg = tid >> 4, cg = tid & 15u;
       uint8_t* qp = a.q_row + (m0 + 8 * rg) * a.N + n0 + 8 * cg;
       row_codes_bf16(w, sc, ny, slow, [&](int i, uint2 c) { *reinterpret_cast<uint2*>(qp + (size_t)i * a.N) = c; });
@@ -746,9 +764,8 @@ k_quant_grad_dual_tma(const __grid_constant__ CUtensorMap map, const Q4Args a) {
       uint32_t w[8][4];
       load_cols_bf16(sb, tid, w);
       release();
-      float amax[8], sc[8], ny[8];
-      col_group_amax(w, amax);
-      const uint32_t slow = half_warp_qscales(amax, sc, ny);
+      float sc[8], ny[8];
+      const uint32_t slow = col_group_qscales(w, sc, ny);
       const uint32_t rg = tid & 15u, cg = tid >> 4;
       uint8_t* qp = a.qT_col + (n0 + 8 * cg) * a.M + m0 + 8 * rg;
       col_codes_bf16(w, sc, ny, slow, [&](int j, uint32_t lo, uint32_t hi) {
