@@ -13,7 +13,7 @@
 //       g = RN(amax_row / 2688), h = RN(6·g), s_b = E4M3(RN(amax_b / h)),
 //       d_b = RN(s_b·g), q = E2M1(RN(x / d_b))  (a signed zero when d_b = 0),
 //     every step one correctly rounded FP32 operation (the element quotients
-//     by the division-free exact sequence in quot2).
+//     by the division-free exact sequence in quot2_bf16).
 //   Y[m,n] = bf16(RN(RN(D[m,n]·gx[m])·gw[n])),  D = Σ_k x̂q·ŵq (block-scaled).
 //
 // Block scales live in a blocked layout that the GEMM moves into tensor memory
@@ -90,19 +90,38 @@ __device__ __forceinline__ uint32_t e4m3_code(float v) {
 // which holds for d >= 2^-90 whenever the quotient is 2^-11 or larger; smaller
 // quotients stay below 2^-10 with the sign of x, and every such value has the
 // E2M1 code of a zero.
-__device__ __forceinline__ float2 quot2(float x0, float x1, uint64_t s2, uint64_t ny2) {
-  uint64_t nx, q;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(nx) : "f"(-x0), "f"(-x1));
-  asm("{\n\t.reg .b64 r;\n\t"
-      "mul.rn.f32x2 %0, %1, %3;\n\t"
-      "fma.rn.f32x2 r, %0, %2, %1;\n\t"
+// Here for the two bf16 values of w (first value in the low half), each negated
+// FP32 value formed in one integer operation: (w << 16) + 2^31 (adding 2^31
+// modulo 2^32 flips bit 31) and (w & 0xFFFF0000) ^ 2^31 (lop3, table 0x6A).
+__device__ __forceinline__ float2 quot2_bf16(uint32_t w, uint64_t s2, uint64_t ny2) {
+  uint64_t q;
+  asm("{\n\t.reg .b32 a0, a1;\n\t.reg .b64 nx, r;\n\t"
+      "mad.lo.u32 a0, %1, 65536, 0x80000000;\n\t"
+      "lop3.b32 a1, %1, 0xFFFF0000, 0x80000000, 0x6A;\n\t"
+      "mov.b64 nx, {a0, a1};\n\t"
+      "mul.rn.f32x2 %0, nx, %3;\n\t"
+      "fma.rn.f32x2 r, %0, %2, nx;\n\t"
       "fma.rn.f32x2 %0, r, %3, %0;\n\t"
-      "fma.rn.f32x2 r, %0, %2, %1;\n\t"
+      "fma.rn.f32x2 r, %0, %2, nx;\n\t"
       "fma.rn.f32x2 %0, r, %3, %0;\n\t}"
-      : "=&l"(q) : "l"(nx), "l"(s2), "l"(ny2));
+      : "=&l"(q) : "r"(w), "l"(s2), "l"(ny2));
   float2 r;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(q));
   return r;
+}
+
+// Per half of two packed bf16 pairs: a value whose magnitude is max(|a|, |b|)
+// (sign bit not meaningful).
+__device__ __forceinline__ uint32_t bf_amax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// The largest magnitude among 8 packed bf16 pairs, as a float.
+__device__ __forceinline__ float bf_amax16(const uint32_t (&w)[8]) {
+  const uint32_t m = bf_amax2(bf_amax2(bf_amax2(w[0], w[1]), bf_amax2(w[2], w[3])),
+                              bf_amax2(bf_amax2(w[4], w[5]), bf_amax2(w[6], w[7]))) & 0x7FFF7FFFu;
+  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ size_t scale_offset(uint32_t r, uint32_t b, uint32_t kg) {
@@ -127,11 +146,7 @@ k_quant_nvfp4_rows(const uint16_t* __restrict__ x, uint32_t R, uint32_t K, uint8
     for (uint32_t b = lane; b < nb; b += 32) {
       uint32_t w[8];
       ld_block16(xr + 16u * b, w);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float2 f = bf2_to_f2(w[i]);
-        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
+      amax = fmaxf(amax, bf_amax16(w));
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, o));
@@ -142,13 +157,7 @@ k_quant_nvfp4_rows(const uint16_t* __restrict__ x, uint32_t R, uint32_t K, uint8
     for (uint32_t b = lane; b < nb; b += 32) {
       uint32_t w[8];
       ld_block16(xr + 16u * b, w);
-      float2 f[8];
-      float ab = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        f[i] = bf2_to_f2(w[i]);
-        ab = fmaxf(ab, fmaxf(fabsf(f[i].x), fabsf(f[i].y)));
-      }
+      const float ab = bf_amax16(w);
       const uint32_t s = e4m3_code(__fdiv_rn(ab, h));
       const float d = __fmul_rn(dec_e4m3x2(s).x, g);
       uint32_t c[2] = {0u, 0u};
@@ -159,17 +168,18 @@ k_quant_nvfp4_rows(const uint16_t* __restrict__ x, uint32_t R, uint32_t K, uint8
         asm("mov.b64 %0, {%1, %1};" : "=l"(ny2) : "f"(ny));
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float2 qq = quot2(f[i].x, f[i].y, s2, ny2);
+          const float2 qq = quot2_bf16(w[i], s2, ny2);
           c[i >> 2] |= e2m1x2(qq.x, qq.y) << (8 * (i & 3));
         }
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
+          const float2 fi = bf2_to_f2(w[i]);
           uint32_t byte;
           if (d > 0.0f) {
-            byte = e2m1x2(__fdiv_rn(f[i].x, d), __fdiv_rn(f[i].y, d));
+            byte = e2m1x2(__fdiv_rn(fi.x, d), __fdiv_rn(fi.y, d));
           } else {
-            byte = ((__float_as_uint(f[i].x) >> 31) << 3) | ((__float_as_uint(f[i].y) >> 31) << 7);
+            byte = ((__float_as_uint(fi.x) >> 31) << 3) | ((__float_as_uint(fi.y) >> 31) << 7);
           }
           c[i >> 2] |= byte << (8 * (i & 3));
         }
