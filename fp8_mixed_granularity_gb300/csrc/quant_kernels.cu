@@ -60,22 +60,6 @@ __device__ __forceinline__ float group8_max(float v) {
   v = fmaxf(v, __shfl_xor_sync(kFull, v, 1));
   return v;
 }
-// One lane's 16 values (8 packed pairs) of a 1×128 group held by 8 lanes,
-// all bf16 values: group amax, scale, and the 16 codes (4 words, first value
-// in the low byte).
-__device__ __forceinline__ uint4 quant16(const float2 (&f)[8], bool valid, float& S) {
-  float amax = 0.0f;
-  if (valid) {
-#pragma unroll
-    for (int w = 0; w < 8; ++w) amax = fmaxf(amax, fmaxf(fabsf(f[w].x), fabsf(f[w].y)));
-  }
-  const GroupScale g = make_scale(group8_max(amax));
-  S = g.s;
-  uint32_t c[4];
-  quant_pairs<8>(f, g, c);
-  return make_uint4(c[0], c[1], c[2], c[3]);
-}
-
 // ===========================================================================
 // TMA-fed quantisers.  Two shapes of work:
 //  * row streams (Q1, R1): each warp owns a private ring of shared-memory
@@ -1038,18 +1022,17 @@ k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gam
 #pragma unroll
         for (int w = 0; w < 8; ++w) rx[w] = rg[w] = 0;
       }
-      float2 f[8];
       uint32_t yb[8];
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         const float2 t = mul2(mul2(bf2_to_f2(rx[w]), make_float2(r, r)), bf2_to_f2(rg[w]));
         yb[w] = f2_to_bf2(t.x, t.y);
-        f[w] = bf2_to_f2(yb[w]);
       }
       float S;
-      const uint4 c = quant16(f, valid, S);
+      uint2 c0, c1;
+      group16_codes(yb, valid, S, c0, c1);
       if (valid) {
-        *reinterpret_cast<uint4*>(q + (size_t)row * H + grp * 128 + l8 * 16) = c;
+        *reinterpret_cast<uint4*>(q + (size_t)row * H + grp * 128 + l8 * 16) = make_uint4(c0.x, c0.y, c1.x, c1.y);
         if (y != nullptr) st32(y + (size_t)row * H + grp * 128 + l8 * 16, yb);
         if (l8 == 0) s[(size_t)grp * ld_s + row] = S;
       }
@@ -1337,7 +1320,6 @@ k_swiglu_quant(const uint16_t* __restrict__ gu, uint32_t M, uint32_t I, uint32_t
 #pragma unroll
         for (int w = 0; w < 8; ++w) rg[w] = ru[w] = 0;
       }
-      float2 f[8];
       uint32_t hb[8];
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
@@ -1348,12 +1330,13 @@ k_swiglu_quant(const uint16_t* __restrict__ gu, uint32_t M, uint32_t I, uint32_t
         const float a = __fmul_rn(__fdividef(gg.x, 1.0f + __expf(-gg.x)), uu.x);
         const float b = __fmul_rn(__fdividef(gg.y, 1.0f + __expf(-gg.y)), uu.y);
         hb[w] = f2_to_bf2(a, b);
-        f[w] = bf2_to_f2(hb[w]);
       }
+      // the lane's 16 values of h (consecutive) quantised with its group's scale
       float S;
-      const uint4 c = quant16(f, valid, S);
+      uint2 c0, c1;
+      group16_codes(hb, valid, S, c0, c1);
       if (valid) {
-        *reinterpret_cast<uint4*>(q + (size_t)row * I + grp * 128 + l8 * 16) = c;
+        *reinterpret_cast<uint4*>(q + (size_t)row * I + grp * 128 + l8 * 16) = make_uint4(c0.x, c0.y, c1.x, c1.y);
         if (h != nullptr) st32(h + (size_t)row * I + grp * 128 + l8 * 16, hb);
         if (l8 == 0) s[(size_t)grp * ld_s + row] = S;
       }
