@@ -81,11 +81,12 @@ __device__ __forceinline__ float group8_max(float v) {
 //    rotated order i -> 8·(t%16) + ((i + t%16) mod 8), which spreads a
 //    half-warp's reads over all banks under the 128-byte swizzle; its codes
 //    are rotated back into row order before the store.
-// Codes use the bracketing products of quant_pair (jetfp8_common.cuh), four
-// at a time, with the undecided case (and scales whose reciprocal overflows)
-// taken by one branch per thread and pass that redoes the pass with IEEE
-// divisions.  Of the 8 group scales a half-warp needs, each lane computes one
-// and the others arrive by shuffle.  Every wait is bounded (jetfp8_tma.cuh);
+// Codes come from the exact division-free quotient of jetfp8_common.cuh
+// (codes4_bf16 and relatives: two Markstein corrections of RN(x·RN(1/S)) on the
+// negated values), four at a time in packed FP32 pairs; groups whose maximum is
+// below 2^-80 run the same sequence on operands scaled by 2^96.  Of the 8 group
+// scales a half-warp needs, each lane computes one and the others arrive by
+// shuffle.  Every wait is bounded (jetfp8_tma.cuh);
 // on expiry the kernel records the error word, stops issuing copies, waits
 // for the copies it issued and returns.
 // ===========================================================================
