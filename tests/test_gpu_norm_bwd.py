@@ -38,7 +38,8 @@ def _run(dev, x, gamma, dy):
     return rstd, dx, dg, ws
 
 
-@pytest.mark.parametrize("M,H", [(64, 4096), (300, 1024), (1, 128), (1000, 512)])
+# rows up to 4096 wide take the fused kernel; wider rows the three-kernel path
+@pytest.mark.parametrize("M,H", [(64, 4096), (300, 1024), (1, 128), (1000, 512), (200, 8192), (130, 5120)])
 def test_rmsnorm_bwd_parity(dev, M, H):
     x = W.activations(M, H, seed=9)
     gamma = W.uniform((H,), 0.5, 1.5, seed=9, stream=1)

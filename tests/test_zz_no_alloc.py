@@ -22,7 +22,7 @@ def dev():
     return d
 
 
-@pytest.mark.parametrize("M,H", [(1000, 512), (4096, 4096), (1, 128)])
+@pytest.mark.parametrize("M,H", [(1000, 512), (4096, 4096), (1, 128), (300, 8192)])
 def test_noalloc_matches_workspace_entry_point(dev, M, H):
     x = W.activations(M, H, seed=12).to(dev)
     gamma = W.uniform((H,), 0.5, 1.5, seed=12, stream=1).to(dev)
