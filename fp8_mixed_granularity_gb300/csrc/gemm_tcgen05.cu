@@ -18,26 +18,30 @@
 //   warp 1      allocates 512 TMEM columns; one lane issues tcgen05.mma
 //               (M=128, N=BN, K=32, E4M3×E4M3→FP32) four times per block into
 //               the next TMEM accumulator, then commits.
-//   warps 2-3   idle; with warps 0-1 they form the control warpgroup, which
-//               gives registers back (setmaxnreg.dec) to the promotion warps.
+//   warp 2      uniform scales: stage forwarder (hands each block's operand
+//               stage back once its accumulator is complete).
+//   warp 3      column scales: scale loader (bulk-copies each block's row and
+//               column scales into a ring of shared-memory slots).
+//               Warps 0-3 form the control warpgroup, which gives registers
+//               back (setmaxnreg.dec) to the promotion warps.
 //   warps 4-11  two warpgroups; warpgroup w owns output columns
 //               [w·BN/2, (w+1)·BN/2) of the tile, each warp the 32 TMEM lanes
 //               (tile rows) it may access.  Per block they load the partial
 //               from TMEM, hand the accumulator back as soon as the last piece
 //               is in registers, and promote with packed FP32 arithmetic;
 //               after the last block the tile is written out as bf16 or fp32.
-//               Scales are prefetched two blocks ahead into registers.
 //     uniform scales (FProp, DGrad: sB is one value per 128 output columns):
 //               each thread owns one row and 32-column chunks of it;
 //               promotion is one FMA per element with the product sA·sB,
-//               with the TMEM loads of the next two chunks in flight.
+//               with the TMEM loads of the next two chunks in flight; the
+//               scales are prefetched two blocks ahead into registers.
 //     column scales (WGrad: sB is one value per output column): the partial
 //               is read as 16-lane × 256-bit fragments, so a thread holds 4
 //               rows × 2 adjacent columns of every 8 and needs only a quarter
-//               of the column scales; each block the warp stages its row and
-//               column scales once through shared memory in that order.
-//               Promotion is (partial·sB)·sA, a multiply and an FMA per
-//               element, with the TMEM loads of the next two fragments in flight.
+//               of the column scales, which it reads (with its 4 row scales)
+//               from the block's slot of the scale ring.  Promotion is
+//               (partial·sB)·sA, a multiply and an FMA per element, with the
+//               TMEM loads of the next two fragments in flight.
 // A launch may carry up to four problems of one configuration (the WGrads of a
 // layer's linears, which share the token count): their tiles form one
 // persistent sequence, each tile computed exactly as in a launch of its own.
@@ -74,15 +78,16 @@ constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 384
 // the launch total, or setmaxnreg.inc would wait forever.  The host refuses to
 // launch unless the compiled kernel uses exactly LAUNCH_REGS.
 constexpr int LAUNCH_REGS = 168;
-// Grouped launches (several problems per launch) and CTA pairs give the
-// control warps 32: the TMA producer then also tracks which problem a tile
-// belongs to, or the pair's barriers.
-template <int G, bool PAIR> constexpr int CTRL_REGS = G > 1 ? 32 : 24;
-template <int G, bool PAIR> constexpr int EPI_REGS = G > 1 ? 232 : 240;
-static_assert(128 * CTRL_REGS<1, false> + 256 * EPI_REGS<1, false> <= THREADS * LAUNCH_REGS, "register split");
-static_assert(128 * CTRL_REGS<2, true> + 256 * EPI_REGS<2, true> <= THREADS * LAUNCH_REGS, "register split");
+// Every launch splits 24 / 240: grouped launches (whose control warps also
+// track which problem a tile belongs to) spill a few bytes in the control warps
+// that way, but the column-scale promotion runs 4.6 % faster than with 32 / 232.
+constexpr int CTRL_REGS = 24;
+constexpr int EPI_REGS = 240;
+static_assert(128 * CTRL_REGS + 256 * EPI_REGS <= THREADS * LAUNCH_REGS, "register split");
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int MAX_STAGES = 8, MAX_BUFS = 4;
+// column-mode scale ring depth, in 128-deep blocks (see the scale loader)
+constexpr int SRING = 8;
 // bf16 output leaves through shared memory in 32-row × 32-column chunks, one
 // 2 KB staging buffer per promotion warp, written to global memory by TMA.
 // The buffer uses the 64-byte swizzle: the 16-byte granule g of row r sits at
@@ -109,21 +114,19 @@ struct Cfg {
   // both K-major, N/8 at bits 17-22, M/16 at bits 24-28 (M = 256 for a pair).
   static constexpr uint32_t IDESC =
       (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((PAIR ? 2 * BM : BM) >> 4) << 24);
-  // Column-mode scale staging, per promotion warp and ring slot: the warp's
-  // 32 row scales, then its column scales ordered [g][GS] where group
-  // g = (c mod 8)/2 holds the columns c = 8j + 2g + {0,1} at 2j + {0,1} (GS
-  // pads the groups onto different banks).
-  static constexpr int GS = EPI_COLS / 4 + 4;
-  static constexpr int CB_F = 32 + 4 * GS;
-  static constexpr int COLBUF_BYTES = EPI_WARPS * 2 * CB_F * 4;
+  // Column mode: the scales of each 128-deep block — the tile's BN column
+  // scales, then this CTA's 128 row scales — arrive by bulk copy in a ring of
+  // SRING slots.  Uniform mode uses the same area to stage the fused output
+  // quantiser's codes (1 KB per promotion warp).
+  static constexpr int SSLOT_F = BN + BM;
+  static constexpr int AUX_BYTES =
+      SRING * SSLOT_F * 4 > EPI_WARPS * 1024 ? SRING * SSLOT_F * 4 : EPI_WARPS * 1024;
   static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES +
-                                    1024 /*barriers*/ + COLBUF_BYTES + EPI_WARPS * OUT_CHUNK_BYTES;
+                                    1024 /*barriers*/ + AUX_BYTES + EPI_WARPS * OUT_CHUNK_BYTES;
   static_assert(STAGES <= MAX_STAGES && ACC_BUFS <= MAX_BUFS, "barrier arrays");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
-  static_assert(GS % 4 == 0 && CB_F % 4 == 0, "16-byte aligned staging fields");
-  // the fused output quantiser stages 1 KB of codes per promotion warp there
-  static_assert(BN_ != 256 || COLBUF_BYTES >= EPI_WARPS * 1024, "code staging");
-  static_assert(COLBUF_BYTES % 128 == 0 && OUT_CHUNK_BYTES % 128 == 0,
+  static_assert((SSLOT_F * 4) % 16 == 0, "bulk-copy destinations 16-byte aligned");
+  static_assert(AUX_BYTES % 128 == 0 && OUT_CHUNK_BYTES % 128 == 0,
                 "output staging buffers (TMA store sources) 128-byte aligned");
 };
 
@@ -132,6 +135,8 @@ struct Barriers {
   uint64_t empty[MAX_STAGES];
   uint64_t tfull[MAX_BUFS];
   uint64_t tempty[MAX_BUFS];
+  uint64_t sfull[SRING];    // column mode: a block's scales have landed in their slot
+  uint64_t sempty[SRING];   // column mode: every promotion warp has read the slot
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
@@ -220,6 +225,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
+}
+
+// Polls two barriers at once (both lookups in flight together).
+__device__ __forceinline__ void mbar_try_wait2(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb, bool& oka,
+                                               bool& okb) {
+  uint32_t ra, rb;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%2], %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%4], %5;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "selp.u32 %1, 1, 0, q;\n\t}"
+      : "=r"(ra), "=r"(rb) : "r"(a), "r"(pa), "r"(b), "r"(pb) : "memory");
+  oka = ra != 0;
+  okb = rb != 0;
 }
 
 // Wait for the phase of parity `parity` to complete.  Gives up (false) after
@@ -537,37 +557,21 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 
-template <int EPI_COLS>
-struct ColScaleVec;
-template <>
-struct ColScaleVec<32> {
-  using T = float;   // not used: column mode runs with 128- or 256-wide tiles
-};
-template <>
-struct ColScaleVec<64> {
-  using T = float2;
-};
-template <>
-struct ColScaleVec<128> {
-  using T = float4;
-};
-
 template <int BN_, bool COLS, int G, bool PAIR>
 __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
   using C = Cfg<BN_, PAIR>;
   constexpr int BN = C::BN, STAGES = C::STAGES, ACC_BUFS = C::ACC_BUFS;
   constexpr int EPI_COLS = C::EPI_COLS, CHUNKS = C::CHUNKS;
-  using CsVec = typename ColScaleVec<EPI_COLS>::T;
   static_assert(!COLS || BN >= 128, "column-scale promotion needs 128- or 256-wide tiles");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   Barriers* bars = reinterpret_cast<Barriers*>(smem + STAGES * C::STAGE_BYTES);
-  // [8 promotion warps][2 ring slots][CB_F] scale staging (column mode)
-  float* colbuf = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES + 1024);
+  // column mode: [SRING][SSLOT_F] scale ring; uniform mode: [8 promotion warps][1 KB] code staging
+  uint8_t* aux = smem + STAGES * C::STAGE_BYTES + 1024;
   // [8 promotion warps][32 rows][32 bf16] output staging
-  uint8_t* outbuf = smem + STAGES * C::STAGE_BYTES + 1024 + C::COLBUF_BYTES;
+  uint8_t* outbuf = aux + C::AUX_BYTES;
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -596,6 +600,10 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
       // uniform scales a single CTA's also by the stage forwarder
       mbar_init(&bars->tempty[b], PAIR ? 2 * EPI_WARPS : (COLS ? EPI_WARPS : EPI_WARPS + 1));
     }
+    for (int s = 0; s < SRING; ++s) {
+      mbar_init(&bars->sfull[s], 1);
+      mbar_init(&bars->sempty[s], EPI_WARPS);
+    }
     mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -622,7 +630,7 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
   const uint32_t tmem = bars->tmem_base;
 
   if (warp < EPI_WARP0) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS<G, PAIR>));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS));
     if (warp == 0 && PAIR) {
       // ---------------- TMA producer (both CTAs of a pair) ----------------
       // Each CTA loads its 128 rows of A and its half of B; every copy counts
@@ -789,15 +797,57 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
           }
         }
       }
+    } else if (warp == 3 && COLS) {
+      // ---------------- scale loader (column mode) ----------------
+      // Block by block, in the order the promotion warps take them: once every
+      // promotion warp has read slot it mod SRING, the block's BN column scales
+      // and this CTA's 128 row scales go there by two bulk copies.  (The host
+      // launches column mode only for whole 128-row tiles, BN-wide column
+      // tiles and 16-byte aligned scale rows; a pair's second CTA past the
+      // last row tile loads no row scales — its rows are never stored.)
+      if (lane == 0) {
+        const uint32_t sfull0 = smem_u32(&bars->sfull[0]);
+        constexpr uint32_t SEMPTY_OFF = offsetof(Barriers, sempty) - offsetof(Barriers, sfull);
+        constexpr uint32_t ABORT_OFF = offsetof(Barriers, abort_flag) - offsetof(Barriers, sfull);
+        const uint32_t ring0 = smem_u32(aux);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
+          int local, mt, nt;
+          const int g = problem_of(kp, tile, local);
+          const DevArgs& p = kp.p[g];
+          tile_coords(p, local, mt, nt);
+          const int row0 = mt * TILE_M + (int)rank * BM;
+          const uint32_t rbytes = row0 < p.R ? BM * 4u : 0u;
+          const float* sa = p.sA + row0;
+          const float* sb = p.sB + (long long)nt * BN;
+          for (int kb = 0; kb < p.nKB; ++kb, ++it) {
+            const uint32_t slot = it % SRING, bar = sfull0 + 8 * slot;
+            if (!mbar_wait_s(bar + SEMPTY_OFF, ((it / SRING) & 1u) ^ 1u, sfull0 + ABORT_OFF)) {
+              fail();
+              ok = false;
+              break;
+            }
+            const uint32_t dst = ring0 + slot * (C::SSLOT_F * 4);
+            mbar_arrive_expect_tx(bar, BN * 4u + rbytes);
+            bulk_g2s_plain(dst, sb + (long long)kb * p.sb_k, BN * 4u, bar);
+            if (rbytes != 0) bulk_g2s_plain(dst + BN * 4u, sa + (long long)kb * p.ld_sA, rbytes, bar);
+          }
+        }
+        // every copy issued has landed before shared memory goes away
+        const uint32_t first = it > (uint32_t)SRING ? it - SRING : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          mbar_wait(&bars->sfull[j % SRING], (j / SRING) & 1u, abort_flag, false);
+      }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS<G, PAIR>));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
     // ---------------- promotion + epilogue ----------------
     const int ew = warp - EPI_WARP0;
     const int wg = ew >> 2;                 // column half of the tile
     const int lq = warp & 3;                // TMEM lane quarter this warp may access
     const uint32_t taddr_w = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(wg * EPI_COLS);
-    float* cbuf = colbuf + ew * 2 * C::CB_F;
+    const float* sring = reinterpret_cast<const float*>(aux);
     uint32_t acc_it = 0;
     bool ok = true;
     for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
@@ -810,31 +860,22 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
       const int col0 = nt * BN + wg * EPI_COLS;
       const bool row_ok = row < p.R;
       const int nkb = p.nKB;
-      // Scales are prefetched two blocks ahead into a two-slot register ring;
-      // the block loop is unrolled by two so every slot index is a
-      // compile-time constant and no register copy waits on a load in flight.
+      // Uniform mode: the scales are prefetched two blocks ahead into a
+      // two-slot register ring; the block loop is unrolled by two so every slot
+      // index is a compile-time constant and no register copy waits on a load
+      // in flight.  Column mode reads them from the scale ring.
       const float* sa_ptr = p.sA + row;
-      const float* sb_ptr = p.sB + (COLS ? (long long)col0 : (long long)(col0 / 128) * p.sb_j);
+      const float* sb_ptr = p.sB + (long long)(col0 / 128) * p.sb_j;
       auto load_sa = [&](int kb) {
-        return (row_ok && kb < nkb) ? __ldg(sa_ptr + (long long)kb * p.ld_sA) : 0.0f;
+        return (!COLS && row_ok && kb < nkb) ? __ldg(sa_ptr + (long long)kb * p.ld_sA) : 0.0f;
       };
       auto load_sb = [&](int kb) {
-        return kb < nkb ? __ldg(sb_ptr + (long long)kb * p.sb_k) : 0.0f;
-      };
-      auto load_cs = [&](int kb) {
-        CsVec v;
-        if (kb < nkb) v = __ldg(reinterpret_cast<const CsVec*>(sb_ptr + (long long)kb * p.sb_k) + lane);
-        else memset(&v, 0, sizeof(v));
-        return v;
+        return (!COLS && kb < nkb) ? __ldg(sb_ptr + (long long)kb * p.sb_k) : 0.0f;
       };
       float sa_r[2], sb_r[2];
-      CsVec cs_r[2];
-      sa_r[0] = load_sa(0);
-      sa_r[1] = load_sa(1);
-      if (COLS) {
-        cs_r[0] = load_cs(0);
-        cs_r[1] = load_cs(1);
-      } else {
+      if (!COLS) {
+        sa_r[0] = load_sa(0);
+        sa_r[1] = load_sa(1);
         sb_r[0] = load_sb(0);
         sb_r[1] = load_sb(1);
       }
@@ -851,58 +892,30 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
       auto block = [&](int kb, auto slot) -> bool {
         constexpr int SL = decltype(slot)::value;
         const uint32_t b = acc_it % ACC_BUFS, bph = (acc_it / ACC_BUFS) & 1u;
+        const uint32_t ss = acc_it % SRING, sph = (acc_it / SRING) & 1u;
         ++acc_it;
         uint64_t s2u = 0;
-        uint64_t sb[COLS ? CHUNKS : 1][4];
-        float sa_raw[4];
-        if (COLS) {
-          // stage the block's scales in the warp's slot SL (row of lane l at l;
-          // column scales at their fragment-order places), then read back the
-          // ones this lane's fragments need: rows lane/4 + 8i, and the column
-          // pairs of group lane mod 4
-          float* cb = cbuf + SL * C::CB_F;
-          cb[lane] = sa_r[SL];
-          if constexpr (EPI_COLS == 128) {
-            // columns 4l..4l+3: groups 2(l mod 2) and 2(l mod 2) + 1 at 2j = l - (l mod 2)
-            float* d = cb + 32 + (lane & 1) * 2 * C::GS + (lane & ~1);
-            *reinterpret_cast<float2*>(d) = make_float2(cs_r[SL].x, cs_r[SL].y);
-            *reinterpret_cast<float2*>(d + C::GS) = make_float2(cs_r[SL].z, cs_r[SL].w);
-          } else {
-            // columns 2l, 2l+1: group l mod 4 at 2j = 2(l/4)
-            *reinterpret_cast<float2*>(cb + 32 + (lane & 3) * C::GS + 2 * (lane >> 2)) =
-                *reinterpret_cast<const float2*>(&cs_r[SL]);
-          }
-          sa_r[SL] = load_sa(kb + 2);
-          cs_r[SL] = load_cs(kb + 2);
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sa_raw[i] = cb[(lane >> 2) + 8 * i];
-          const ulonglong2* cs = reinterpret_cast<const ulonglong2*>(cb + 32 + (lane & 3) * C::GS);
-#pragma unroll
-          for (int cq = 0; cq < (COLS ? CHUNKS : 1); ++cq) {
-            const ulonglong2 v0 = cs[2 * cq], v1 = cs[2 * cq + 1];
-            sb[cq][0] = v0.x;
-            sb[cq][1] = v0.y;
-            sb[cq][2] = v1.x;
-            sb[cq][3] = v1.y;
-          }
-        } else {
+        if (!COLS) {
           const float sc = sa_r[SL] * sb_r[SL];
           s2u = pack2(sc, sc);
           sa_r[SL] = load_sa(kb + 2);
           sb_r[SL] = load_sb(kb + 2);
         }
-        bool good = mbar_wait(&bars->tfull[b], bph, abort_flag, true);
+        // column mode: the block's scales must be in their ring slot as well
+        // (both barriers polled together; each is waited for alone only if needed)
+        bool good;
+        if constexpr (COLS) {
+          bool s_ok, t_ok;
+          mbar_try_wait2(smem_u32(&bars->sfull[ss]), sph, smem_u32(&bars->tfull[b]), bph, s_ok, t_ok);
+          good = (s_ok || mbar_wait(&bars->sfull[ss], sph, abort_flag, true)) &&
+                 (t_ok || mbar_wait(&bars->tfull[b], bph, abort_flag, true));
+        } else {
+          good = mbar_wait(&bars->tfull[b], bph, abort_flag, true);
+        }
         if (!good) fail();
         if (__any_sync(0xffffffffu, !good)) return false;
         tc_fence_after();
         const uint32_t tbase = taddr_w + b * BN;
-        // TMEM loads take well over a hundred cycles while the tensor core and
-        // TMA keep the SM busy, and tcgen05.wait::ld waits for all of a
-        // thread's loads: pieces go through a three-buffer ring, loaded two
-        // ahead of their promotion, with a wait after every second piece; the
-        // accumulator is handed back right after the wait that covers the
-        // last piece.
         auto release = [&]() {
           tc_fence_before();
           __syncwarp();
@@ -910,6 +923,9 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
             // (a pair: on the leader's barrier, addressed through the cluster)
             if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->tempty[b]), 0));
             else mbar_arrive_relaxed(&bars->tempty[b]);
+            // column mode: the warp's reads of the scale slot are done (this
+            // arrive orders them before the slot is refilled)
+            if constexpr (COLS) mbar_arrive(&bars->sempty[ss]);
           }
         };
         if (COLS) {
@@ -919,6 +935,19 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
           auto load = [&](int i) {
             tmem_ld16x256_x4(tbase + ((uint32_t)(16 * (i & 1)) << 16) + 32 * (i >> 1), r[i % 3]);
           };
+          // this lane's scales in the slot: rows lane/4 + 8i of the warp's 32,
+          // and per 32-column chunk cq the column pairs 32cq + 8j + 2(lane mod 4)
+          const float* sl = sring + ss * C::SSLOT_F;
+          const float* colp = sl + wg * EPI_COLS + 2 * (lane & 3);
+          uint64_t sbr[CHUNKS][4];
+#pragma unroll
+          for (int cq = 0; cq < CHUNKS; ++cq)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              sbr[cq][j] = *reinterpret_cast<const uint64_t*>(colp + 32 * cq + 8 * j);
+          float sa_raw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sa_raw[i] = sl[BN + lq * 32 + (lane >> 2) + 8 * i];
           load(0);
           load(1);
           uint64_t sal[2], sah[2];
@@ -932,7 +961,7 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
 #pragma unroll
           for (int i = 0; i < NF; ++i) {
             if (i + 2 < NF) load(i + 2);
-            promote_cols_frag(&acc[i >> 1][8 * (i & 1)], r[i % 3], sb[i >> 1], sal[i & 1], sah[i & 1]);
+            promote_cols_frag(&acc[i >> 1][8 * (i & 1)], r[i % 3], sbr[i >> 1], sal[i & 1], sah[i & 1]);
             if ((i & 1) && i + 1 < NF) {
               tmem_wait_ld16(r[(i + 1) % 3]);
               if (i + 2 < NF) tmem_tie16(r[(i + 2) % 3]);
@@ -1026,10 +1055,10 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
         // 128 columns are exactly one 1×128 group of its row) the group's
         // scale comes from the bf16-rounded values and each chunk's 32 codes
         // per row leave through a 1 KB staging buffer in the (here unused)
-        // column-scale staging area, so the codes are those of the 1×128
+        // column-scale ring area, so the codes are those of the 1×128
         // quantiser applied to the bf16 output.
         uint8_t* ob = outbuf + ew * OUT_CHUNK_BYTES;
-        uint8_t* qb = reinterpret_cast<uint8_t*>(colbuf) + ew * 1024;
+        uint8_t* qb = aux + ew * 1024;
         const bool fuse_q = !PAIR && EPI_COLS == 128 && p.out_q != nullptr;
         GroupScale gq{};
         if (fuse_q) {
@@ -1143,6 +1172,14 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
+// Column mode reads each block's scales with bulk copies of whole 128-row and
+// BN-column runs: rows and columns must fill their tiles and every scale row
+// must start on a 16-byte boundary.
+bool scale_ring_ok(const GemmArgs& x, int bn) {
+  return x.R % BM == 0 && x.C % bn == 0 && ((uintptr_t)x.sA & 15u) == 0 && ((uintptr_t)x.sB & 15u) == 0 &&
+         x.ld_sA % 4 == 0 && x.sb_k % 4 == 0;
+}
+
 }  // namespace
 
 namespace {
@@ -1184,6 +1221,7 @@ cudaError_t launch_cfg(const GemmArgs* a, int count, int dev, cudaStream_t st) {
       continue;
     }
     const GemmArgs& x = a[g];
+    if (COLS && !scale_ring_ok(x, BN)) return cudaErrorInvalidValue;
     if (!make_map(&kp.tmA[g], x.A, (uint64_t)x.Kc, (uint64_t)x.R, BM) ||
         !make_map(&kp.tmB[g], x.B, (uint64_t)x.Kc, (uint64_t)x.C, BN))
       return cudaErrorInvalidValue;
@@ -1262,6 +1300,7 @@ cudaError_t launch_pair(const GemmArgs* a, int count, int dev, cudaStream_t st) 
     }
     const GemmArgs& x = a[g];
     if (x.out_q != nullptr || x.drop_kb >= 0 || x.C % C::BN != 0) return cudaErrorInvalidValue;
+    if (COLS && !scale_ring_ok(x, C::BN)) return cudaErrorInvalidValue;
     if (!make_map(&kp.tmA[g], x.A, (uint64_t)x.Kc, (uint64_t)x.R, BM) ||
         !make_map(&kp.tmB[g], x.B, (uint64_t)x.Kc, (uint64_t)x.C, C::BN / 2))
       return cudaErrorInvalidValue;

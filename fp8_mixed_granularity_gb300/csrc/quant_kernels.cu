@@ -375,16 +375,24 @@ k_quant_rows_tma(const uint16_t* __restrict__ x, uint32_t M, uint32_t K, uint32_
 // holds for every row whose Σx² is itself accurate (|x| within about 1e-19..1e19)
 // when 1e-19 < |γ| < 1e19; the quantiser then works on -y, which the same
 // roundings give directly from -r.
-template <int W, int D, uint32_t SLOT_ELEMS>
+// With one slot per warp (D = 1) the row arrives in P parts, each with its own
+// barrier: once the quantising pass has left a part, the next row's copy of that
+// part is requested, so the next row streams in while this one is finished.
+template <int W, int D, uint32_t SLOT_ELEMS, int P>
 __global__ void __launch_bounds__(32 * W, 1)
 k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
                     float inv_h, uint32_t M, uint32_t H, uint32_t ld_s, uint8_t* __restrict__ q,
                     float* __restrict__ s, float* __restrict__ rstd, uint16_t* __restrict__ y,
                     unsigned* err) {
   extern __shared__ __align__(1024) uint8_t dsm[];
-  __shared__ __align__(8) uint64_t full[W][D];
+  __shared__ __align__(8) uint64_t full[W][D * P];
   __shared__ __align__(8) uint64_t gbar;
   constexpr uint32_t SLOT = SLOT_ELEMS * 2;
+  constexpr int NC = (int)(SLOT_ELEMS / 512);               // 4-group chunks of a slot
+  constexpr uint32_t GP = SLOT_ELEMS / 128 / P;             // groups per part
+  constexpr int KP = (int)GP / 4;                           // chunks per part
+  static_assert(P == 1 || D == 1, "parts need one slot per warp");
+  static_assert(KP >= 1 && NC % KP == 0, "a part is whole 4-group chunks");
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u, g4 = lane >> 3, l8 = lane & 7u;
   const uint32_t gsm = smem_addr(dsm);                       // γ
   const uint32_t slot0 = gsm + SLOT + warp * D * SLOT;
@@ -398,34 +406,37 @@ k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__
     bulk_g2s_plain(gsm, gamma, H * 2u, gb);
   }
   if (lane == 0) {
-    for (int d = 0; d < D; ++d) mbar_init_s(bar0 + 8 * d, 1);
+    for (int d = 0; d < D * P; ++d) mbar_init_s(bar0 + 8 * d, 1);
     mbar_fence_init();
   }
   __syncthreads();
   const uint64_t pol = policy_evict_first();
-  auto issue = [&](uint64_t j) {
+  // part p of unit j: groups [p·GP, min(ng, (p+1)·GP)) into slot j mod D
+  auto issue = [&](uint64_t j, uint32_t p) {
     const uint64_t row = gw + j * GW;
-    if (row >= M) return;
-    const uint32_t d = (uint32_t)(j % D);
-    mbar_expect_tx(bar0 + 8 * d, H * 2u);
-    bulk_g2s(slot0 + d * SLOT, x + (size_t)row * H, H * 2u, bar0 + 8 * d, pol);
+    const uint32_t lo = p * GP, hi = min(ng, lo + GP);
+    if (row >= M || lo >= hi) return;
+    const uint32_t d = (uint32_t)(j % D), bar = bar0 + 8 * (d * P + p);
+    mbar_expect_tx(bar, (hi - lo) * 256u);
+    bulk_g2s(slot0 + d * SLOT + lo * 256u, x + (size_t)row * H + lo * 128u, (hi - lo) * 256u, bar, pol);
   };
   if (lane == 0)
-    for (int d = 0; d < D; ++d) issue(d);
+    for (int d = 0; d < D; ++d)
+      for (int p = 0; p < P; ++p) issue(d, p);
   bool ok = mbar_wait_bounded(gb, 0);
   uint64_t j = 0;
   for (; ok && gw + j * GW < M; ++j) {
     const uint32_t row = (uint32_t)(gw + j * GW), d = (uint32_t)(j % D);
-    if (!mbar_wait_bounded(bar0 + 8 * d, (uint32_t)(j / D) & 1u)) {
-      ok = false;
-      break;
-    }
+    const uint32_t ph = (uint32_t)(j / D) & 1u;
     const uint32_t sb = slot0 + d * SLOT;
-    // chunk sums of the lane's groups g4, g4 + 4, ... (zero past the row)
-    constexpr int NC = (int)(SLOT_ELEMS / 512);
+    // chunk sums of the lane's groups g4, g4 + 4, ... (zero past the row); each
+    // part is waited for before its first chunk
+    bool got = true;
     float cs[NC];
 #pragma unroll
     for (int k = 0; k < NC; ++k) {
+      if (k % KP == 0 && (uint32_t)(k / KP) * GP < ng)
+        got = got && mbar_wait_bounded(bar0 + 8 * (d * P + k / KP), ph);
       const uint32_t grp = g4 + 4u * k;
       float c = 0.0f;
       if (grp < ng) {
@@ -434,6 +445,10 @@ k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__
         c = add_squares16(w, c);
       }
       cs[k] = c;
+    }
+    if (!got) {
+      ok = false;
+      break;
     }
 #pragma unroll
     for (int width = NC / 2; width >= 1; width /= 2)
@@ -476,14 +491,18 @@ k_rmsnorm_quant_tma(const uint16_t* __restrict__ x, const uint16_t* __restrict__
         }
         if (l8 == 0) s[(size_t)grp * ld_s + row] = S;
       }
+      // the warp has left part g0 / GP: the slot's next row may take it
+      if ((g0 + 4u) % GP == 0 || g0 + 4u >= ng) {
+        __syncwarp();
+        if (lane == 0) issue(j + D, g0 / GP);
+      }
     }
-    __syncwarp();
-    if (lane == 0) issue(j + D);
   }
   if (!ok && lane == 0) record_timeout(nullptr, err);
   if (lane == 0) {
     for (uint64_t jj = j; jj < j + D && gw + jj * GW < M; ++jj)
-      mbar_wait_bounded(bar0 + 8 * (uint32_t)(jj % D), (uint32_t)(jj / D) & 1u);
+      for (uint32_t p = 0; p < (uint32_t)P && p * GP < ng; ++p)
+        mbar_wait_bounded(bar0 + 8 * ((uint32_t)(jj % D) * P + p), (uint32_t)(jj / D) & 1u);
     if (warp == 0 && !ok) mbar_wait_bounded(gb, 0);
   }
 }
@@ -1489,10 +1508,10 @@ cudaError_t launch_quant_grad_dual(const void* dy, int64_t M, int64_t N, uint8_t
   return cudaGetLastError();
 }
 
-template <int W, int D, uint32_t SLOT>
+template <int W, int D, uint32_t SLOT, int P>
 cudaError_t launch_rmsnorm_tma(const void* x, const void* gamma, float eps, int64_t M, int64_t H,
                                uint8_t* q, float* s, float* rstd, void* y, unsigned* err, cudaStream_t st) {
-  auto kern = k_rmsnorm_quant_tma<W, D, SLOT>;
+  auto kern = k_rmsnorm_quant_tma<W, D, SLOT, P>;
   constexpr int smem = (1 + W * D) * (int)SLOT * 2;
   static int done[64] = {0};
   cudaError_t e = opt_in_smem(kern, smem, done);
@@ -1515,12 +1534,16 @@ cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, in
   // latency; 8192 rows then take exactly two rounds.  Graph-timed at 8192 and
   // 32768 rows × 4096: 18, 20, 24, 27 warps give 4304 / 4803, 4254 / 5193,
   // 3821 / 5487, 4717 / 5548 GB/s.  Fewer than 4096 rows spread over more SMs
-  // with 8 warps per CTA.
+  // with 8 warps per CTA.  Each row arrives in two halves, the next row's first
+  // half requested once the quantising pass has left it; graph-timed at 8192 /
+  // 32768 rows, one, two, four and eight parts give 4741 / 5305, 4752 / 5395,
+  // 4249 / 5212 and 3852 / 4710 GB/s (the waits and copies of more parts cost
+  // more than they hide).
   if (H <= 4096) {
-    if (M >= 4096) return launch_rmsnorm_tma<27, 1, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
-    return launch_rmsnorm_tma<8, 1, 4096>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+    if (M >= 4096) return launch_rmsnorm_tma<27, 1, 4096, 2>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+    return launch_rmsnorm_tma<8, 1, 4096, 2>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
   }
-  if (H <= 8192) return launch_rmsnorm_tma<6, 2, 8192>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+  if (H <= 8192) return launch_rmsnorm_tma<6, 2, 8192, 1>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
   const unsigned grid = grid_for((size_t)M, kThreads / 32, 8);
   k_rmsnorm_quant<<<grid, kThreads, 0, st>>>(
       static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma), eps, (uint32_t)M,
