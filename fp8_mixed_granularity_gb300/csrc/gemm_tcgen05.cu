@@ -173,6 +173,7 @@ struct KParams {
   CUtensorMap tmQ;
   DevArgs p[G];
   int tile_end[G];
+  int nkb;   // 128-deep blocks per tile, the same for every problem of a launch
 };
 
 // Global tile index -> (problem, tile index within that problem).
@@ -189,6 +190,19 @@ __device__ __forceinline__ int problem_of(const KParams<G>& kp, int tile, int& l
   return g;
 }
 
+// Field f of problem g as a chain of selects over constant-index parameter
+// reads: the control warps, on 24 registers, then make no indexed parameter
+// loads and keep no table (a grouped launch spilled and ran 10 % slower per
+// tile with indexed loads).
+template <int G, typename T>
+__device__ __forceinline__ T pick(const KParams<G>& kp, int g, T DevArgs::*f) {
+  T v = kp.p[0].*f;
+#pragma unroll
+  for (int i = 1; i < G; ++i)
+    if (g == i) v = kp.p[i].*f;
+  return v;
+}
+
 // Tile index -> (m tile, n tile).  Consecutive tiles (which run at the same
 // time on neighbouring SMs) share one operand tile; the other operand is
 // streamed once per band, so the order keeps the re-streamed operand the
@@ -200,6 +214,19 @@ __device__ __forceinline__ void tile_coords(const DevArgs& p, int tile, int& mt,
   } else {
     nt = tile % p.tiles_n;
     mt = tile / p.tiles_n;
+  }
+}
+// The same for problem g of a launch, through pick().
+template <int G>
+__device__ __forceinline__ void tile_coords_of(const KParams<G>& kp, int g, int tile, int& mt, int& nt) {
+  if (pick(kp, g, &DevArgs::m_fastest)) {
+    const int tm = pick(kp, g, &DevArgs::tiles_m);
+    mt = tile % tm;
+    nt = tile / tm;
+  } else {
+    const int tn = pick(kp, g, &DevArgs::tiles_n);
+    nt = tile % tn;
+    mt = tile / tn;
   }
 }
 
@@ -648,8 +675,8 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
         for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
           int local, mt, nt;
           const int g = problem_of(kp, tile, local);
-          tile_coords(kp.p[g], local, mt, nt);
-          const int nkb = kp.p[g].nKB;
+          tile_coords_of(kp, g, local, mt, nt);
+          const int nkb = kp.nkb;
           const CUtensorMap* const mA = &kp.tmA[g];   // tmB[g] lies G maps after it
           for (int kb = 0; kb < nkb; ++kb, ++it) {
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -693,13 +720,13 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
         for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
           int local, mt, nt;
           const int g = problem_of(kp, tile, local);
-          tile_coords(kp.p[g], local, mt, nt);
-          const int nkb = kp.p[g].nKB;
+          tile_coords_of(kp, g, local, mt, nt);
+          const int nkb = kp.nkb, drop_kb = pick(kp, g, &DevArgs::drop_kb);
           // tmB[g] lies G maps after tmA[g]: one live pointer
           const CUtensorMap* const mA = &kp.tmA[g];
           for (int kb = 0; kb < nkb; ++kb, ++it) {
             // test hook: leave this stage unfilled, so the MMA's bounded wait runs out
-            if (kb == kp.p[g].drop_kb) continue;
+            if (kb == drop_kb) continue;
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             const uint32_t full = full0 + 8 * s;
             if (!mbar_wait_s(full + EMPTY_OFF, ph ^ 1u, full0 + ABORT_OFF)) {
@@ -725,9 +752,10 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
       if (lane == 0 && rank == 0) {
         uint32_t it = 0, acc_it = 0;
         bool ok = true;
+        // (every tile has kp.nkb blocks: no per-problem lookup on this warp,
+        // whose few registers and issue latency the tensor core waits on)
+        const int nkb = kp.nkb;
         for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
-          int local;
-          const int nkb = kp.p[problem_of(kp, tile, local)].nKB;
           for (int kb = 0; kb < nkb; ++kb, ++it, ++acc_it) {
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             const uint32_t b = acc_it % ACC_BUFS, bph = (acc_it / ACC_BUFS) & 1u;
@@ -782,9 +810,8 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
       if (lane == 0) {
         uint32_t it = 0;
         bool ok = true;
+        const int nkb = kp.nkb;
         for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
-          int local;
-          const int nkb = kp.p[problem_of(kp, tile, local)].nKB;
           for (int kb = 0; kb < nkb; ++kb, ++it) {
             const uint32_t b = it % ACC_BUFS, bph = (it / ACC_BUFS) & 1u;
             if (!mbar_wait(&bars->tfull[b], bph, abort_flag, true)) {
@@ -815,13 +842,16 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
         for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
           int local, mt, nt;
           const int g = problem_of(kp, tile, local);
-          const DevArgs& p = kp.p[g];
-          tile_coords(p, local, mt, nt);
+          tile_coords_of(kp, g, local, mt, nt);
           const int row0 = mt * TILE_M + (int)rank * BM;
-          const uint32_t rbytes = row0 < p.R ? BM * 4u : 0u;
-          const float* sa = p.sA + row0;
-          const float* sb = p.sB + (long long)nt * BN;
-          for (int kb = 0; kb < p.nKB; ++kb, ++it) {
+          const uint32_t rbytes = row0 < pick(kp, g, &DevArgs::R) ? BM * 4u : 0u;
+          const float* sa = pick(kp, g, &DevArgs::sA) + row0;
+          const float* sb = pick(kp, g, &DevArgs::sB) + (long long)nt * BN;
+          // (strides in elements, 32 bits)
+          const uint32_t sa_step = (uint32_t)pick(kp, g, &DevArgs::ld_sA);
+          const uint32_t sb_step = (uint32_t)pick(kp, g, &DevArgs::sb_k);
+          const int nkb = kp.nkb;
+          for (int kb = 0; kb < nkb; ++kb, ++it) {
             const uint32_t slot = it % SRING, bar = sfull0 + 8 * slot;
             if (!mbar_wait_s(bar + SEMPTY_OFF, ((it / SRING) & 1u) ^ 1u, sfull0 + ABORT_OFF)) {
               fail();
@@ -830,8 +860,8 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
             }
             const uint32_t dst = ring0 + slot * (C::SSLOT_F * 4);
             mbar_arrive_expect_tx(bar, BN * 4u + rbytes);
-            bulk_g2s_plain(dst, sb + (long long)kb * p.sb_k, BN * 4u, bar);
-            if (rbytes != 0) bulk_g2s_plain(dst + BN * 4u, sa + (long long)kb * p.ld_sA, rbytes, bar);
+            bulk_g2s_plain(dst, sb + (size_t)kb * sb_step, BN * 4u, bar);
+            if (rbytes != 0) bulk_g2s_plain(dst + BN * 4u, sa + (size_t)kb * sa_step, rbytes, bar);
           }
         }
         // every copy issued has landed before shared memory goes away
@@ -851,26 +881,24 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
     uint32_t acc_it = 0;
     bool ok = true;
     for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
-      int local, mt, nt;
-      const int g = problem_of(kp, tile, local);
-      const DevArgs& p = kp.p[g];
-      tile_coords(p, local, mt, nt);
-      const int wrow0 = mt * TILE_M + (int)rank * BM + lq * 32;   // first tile row of this warp
-      const int row = wrow0 + lane;          // the row whose sA this lane fetches
-      const int col0 = nt * BN + wg * EPI_COLS;
-      const bool row_ok = row < p.R;
-      const int nkb = p.nKB;
+      const int nkb = kp.nkb;
       // Uniform mode: the scales are prefetched two blocks ahead into a
       // two-slot register ring; the block loop is unrolled by two so every slot
       // index is a compile-time constant and no register copy waits on a load
-      // in flight.  Column mode reads them from the scale ring.
-      const float* sa_ptr = p.sA + row;
-      const float* sb_ptr = p.sB + (long long)(col0 / 128) * p.sb_j;
+      // in flight.  Column mode reads them from the scale ring and needs
+      // nothing of the tile before its epilogue.
+      int local0, mt0, nt0;
+      const DevArgs& p0 = kp.p[problem_of(kp, tile, local0)];
+      tile_coords(p0, local0, mt0, nt0);
+      const int srow = mt0 * TILE_M + (int)rank * BM + lq * 32 + lane;   // the row whose sA this lane fetches
+      const bool srow_ok = srow < p0.R;
+      const float* sa_ptr = p0.sA + srow;
+      const float* sb_ptr = p0.sB + (long long)((nt0 * BN + wg * EPI_COLS) / 128) * p0.sb_j;
       auto load_sa = [&](int kb) {
-        return (!COLS && row_ok && kb < nkb) ? __ldg(sa_ptr + (long long)kb * p.ld_sA) : 0.0f;
+        return (!COLS && srow_ok && kb < nkb) ? __ldg(sa_ptr + (long long)kb * p0.ld_sA) : 0.0f;
       };
       auto load_sb = [&](int kb) {
-        return (!COLS && kb < nkb) ? __ldg(sb_ptr + (long long)kb * p.sb_k) : 0.0f;
+        return (!COLS && kb < nkb) ? __ldg(sb_ptr + (long long)kb * p0.sb_k) : 0.0f;
       };
       float sa_r[2], sb_r[2];
       if (!COLS) {
@@ -879,7 +907,7 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
         sb_r[0] = load_sb(0);
         sb_r[1] = load_sb(1);
       }
-      // uniform mode: acc[c][j] holds row `row`, columns 32c + 2j + {0,1};
+      // uniform mode: acc[c][j] holds row `srow`, columns 32c + 2j + {0,1};
       // column mode: acc[cq][8h + 2j + rs] holds row wrow0 + lane/4 + 8rs + 16h,
       // columns 32cq + 8j + 2(lane mod 4) + {0,1}
       uint64_t acc[CHUNKS][16];
@@ -997,6 +1025,16 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
         }
       }
       if (!ok) break;
+      // the epilogue: the tile's problem and coordinates, derived here so that
+      // a grouped launch keeps none of them live across the block loop
+      int local, mt, nt;
+      const int g = problem_of(kp, tile, local);
+      const DevArgs& p = kp.p[g];
+      tile_coords(p, local, mt, nt);
+      const int wrow0 = mt * TILE_M + (int)rank * BM + lq * 32;   // first tile row of this warp
+      const int row = wrow0 + lane;
+      const int col0 = nt * BN + wg * EPI_COLS;
+      const bool row_ok = row < p.R;
       if (COLS) {
         const int g2 = 2 * (lane & 3);
         if (p.out_fp32) {
@@ -1209,6 +1247,7 @@ cudaError_t launch_cfg(const GemmArgs* a, int count, int dev, cudaStream_t st) {
   if (err == nullptr) return cudaErrorInvalidValue;
   KParams<G> kp;
   memset(&kp, 0, sizeof(kp));
+  kp.nkb = (int)(a[0].Kc / BK);
   int tiles = 0;
   for (int g = 0; g < G; ++g) {
     if (g >= count) {
@@ -1240,6 +1279,7 @@ cudaError_t launch_cfg(const GemmArgs* a, int count, int dev, cudaStream_t st) {
     d.R = (int)x.R;
     d.C = (int)x.C;
     d.nKB = (int)(x.Kc / BK);
+    if (x.Kc != a[0].Kc) return cudaErrorInvalidValue;   // one block count per launch
     d.tiles_m = (int)((x.R + BM - 1) / BM);
     d.tiles_n = (int)(x.C / BN);
     d.m_fastest = x.R <= x.C ? 1 : 0;
@@ -1288,6 +1328,7 @@ cudaError_t launch_pair(const GemmArgs* a, int count, int dev, cudaStream_t st) 
   if (err == nullptr) return cudaErrorInvalidValue;
   KParams<G> kp;
   memset(&kp, 0, sizeof(kp));
+  kp.nkb = (int)(a[0].Kc / BK);
   int tiles = 0;
   for (int g = 0; g < G; ++g) {
     if (g >= count) {
@@ -1319,6 +1360,7 @@ cudaError_t launch_pair(const GemmArgs* a, int count, int dev, cudaStream_t st) 
     d.R = (int)x.R;
     d.C = (int)x.C;
     d.nKB = (int)(x.Kc / BK);
+    if (x.Kc != a[0].Kc) return cudaErrorInvalidValue;   // one block count per launch
     d.tiles_m = (int)((x.R + 2 * BM - 1) / (2 * BM));
     d.tiles_n = (int)(x.C / C::BN);
     d.m_fastest = x.R <= x.C ? 1 : 0;
