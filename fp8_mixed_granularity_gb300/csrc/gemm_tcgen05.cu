@@ -882,23 +882,27 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
     bool ok = true;
     for (int tile = cl; tile < num_tiles && ok; tile += ncl) {
       const int nkb = kp.nkb;
+      // the tile's problem and coordinates (a grouped launch derives them again
+      // after the block loop, so that none of them stays live across it: with
+      // its problem index known only at run time that spilled)
+      int local, mt, nt;
+      int g = problem_of(kp, tile, local);
+      tile_coords(kp.p[g], local, mt, nt);
+      int wrow0 = mt * TILE_M + (int)rank * BM + lq * 32;   // first tile row of this warp
+      int row = wrow0 + lane;                                 // the row whose sA this lane fetches
+      int col0 = nt * BN + wg * EPI_COLS;
+      bool row_ok = row < kp.p[g].R;
       // Uniform mode: the scales are prefetched two blocks ahead into a
       // two-slot register ring; the block loop is unrolled by two so every slot
       // index is a compile-time constant and no register copy waits on a load
-      // in flight.  Column mode reads them from the scale ring and needs
-      // nothing of the tile before its epilogue.
-      int local0, mt0, nt0;
-      const DevArgs& p0 = kp.p[problem_of(kp, tile, local0)];
-      tile_coords(p0, local0, mt0, nt0);
-      const int srow = mt0 * TILE_M + (int)rank * BM + lq * 32 + lane;   // the row whose sA this lane fetches
-      const bool srow_ok = srow < p0.R;
-      const float* sa_ptr = p0.sA + srow;
-      const float* sb_ptr = p0.sB + (long long)((nt0 * BN + wg * EPI_COLS) / 128) * p0.sb_j;
+      // in flight.  Column mode reads them from the scale ring.
+      const float* sa_ptr = kp.p[g].sA + row;
+      const float* sb_ptr = kp.p[g].sB + (long long)(col0 / 128) * kp.p[g].sb_j;
       auto load_sa = [&](int kb) {
-        return (!COLS && srow_ok && kb < nkb) ? __ldg(sa_ptr + (long long)kb * p0.ld_sA) : 0.0f;
+        return (!COLS && row_ok && kb < nkb) ? __ldg(sa_ptr + (long long)kb * kp.p[g].ld_sA) : 0.0f;
       };
       auto load_sb = [&](int kb) {
-        return (!COLS && kb < nkb) ? __ldg(sb_ptr + (long long)kb * p0.sb_k) : 0.0f;
+        return (!COLS && kb < nkb) ? __ldg(sb_ptr + (long long)kb * kp.p[g].sb_k) : 0.0f;
       };
       float sa_r[2], sb_r[2];
       if (!COLS) {
@@ -907,7 +911,7 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
         sb_r[0] = load_sb(0);
         sb_r[1] = load_sb(1);
       }
-      // uniform mode: acc[c][j] holds row `srow`, columns 32c + 2j + {0,1};
+      // uniform mode: acc[c][j] holds row `row`, columns 32c + 2j + {0,1};
       // column mode: acc[cq][8h + 2j + rs] holds row wrow0 + lane/4 + 8rs + 16h,
       // columns 32cq + 8j + 2(lane mod 4) + {0,1}
       uint64_t acc[CHUNKS][16];
@@ -920,7 +924,7 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
       auto block = [&](int kb, auto slot) -> bool {
         constexpr int SL = decltype(slot)::value;
         const uint32_t b = acc_it % ACC_BUFS, bph = (acc_it / ACC_BUFS) & 1u;
-        const uint32_t ss = acc_it % SRING, sph = (acc_it / SRING) & 1u;
+        const uint32_t ss = acc_it % SRING;
         ++acc_it;
         uint64_t s2u = 0;
         if (!COLS) {
@@ -934,6 +938,7 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
         bool good;
         if constexpr (COLS) {
           bool s_ok, t_ok;
+          const uint32_t sph = ((acc_it - 1) / SRING) & 1u;
           mbar_try_wait2(smem_u32(&bars->sfull[ss]), sph, smem_u32(&bars->tfull[b]), bph, s_ok, t_ok);
           good = (s_ok || mbar_wait(&bars->sfull[ss], sph, abort_flag, true)) &&
                  (t_ok || mbar_wait(&bars->tfull[b], bph, abort_flag, true));
@@ -1025,16 +1030,15 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
         }
       }
       if (!ok) break;
-      // the epilogue: the tile's problem and coordinates, derived here so that
-      // a grouped launch keeps none of them live across the block loop
-      int local, mt, nt;
-      const int g = problem_of(kp, tile, local);
+      if constexpr (G > 1) {
+        g = problem_of(kp, tile, local);
+        tile_coords(kp.p[g], local, mt, nt);
+        wrow0 = mt * TILE_M + (int)rank * BM + lq * 32;
+        row = wrow0 + lane;
+        col0 = nt * BN + wg * EPI_COLS;
+        row_ok = row < kp.p[g].R;
+      }
       const DevArgs& p = kp.p[g];
-      tile_coords(p, local, mt, nt);
-      const int wrow0 = mt * TILE_M + (int)rank * BM + lq * 32;   // first tile row of this warp
-      const int row = wrow0 + lane;
-      const int col0 = nt * BN + wg * EPI_COLS;
-      const bool row_ok = row < p.R;
       if (COLS) {
         const int g2 = 2 * (lane & 3);
         if (p.out_fp32) {
