@@ -1534,14 +1534,14 @@ cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, in
   // latency; 8192 rows then take exactly two rounds.  Graph-timed at 8192 and
   // 32768 rows × 4096: 18, 20, 24, 27 warps give 4304 / 4803, 4254 / 5193,
   // 3821 / 5487, 4717 / 5548 GB/s.  Fewer than 4096 rows spread over more SMs
-  // with 8 warps per CTA.  Each row arrives in two halves, the next row's first
-  // half requested once the quantising pass has left it; graph-timed at 8192 /
-  // 32768 rows, one, two, four and eight parts give 4741 / 5305, 4752 / 5395,
-  // 4249 / 5212 and 3852 / 4710 GB/s (the waits and copies of more parts cost
-  // more than they hide).
+  // with 8 warps per CTA.  Each row arrives in one piece: graph-timed at 8192 /
+  // 32768 rows, one, two, four and eight parts per row (the next row's part
+  // requested as soon as the quantising pass has left it) give 4741 / 5305,
+  // 4752 / 5395, 4249 / 5212 and 3852 / 4710 GB/s, but inside the layer step
+  // two parts measured 3299 - 3424 GB/s against 3410 - 3440 for one.
   if (H <= 4096) {
-    if (M >= 4096) return launch_rmsnorm_tma<27, 1, 4096, 2>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
-    return launch_rmsnorm_tma<8, 1, 4096, 2>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+    if (M >= 4096) return launch_rmsnorm_tma<27, 1, 4096, 1>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
+    return launch_rmsnorm_tma<8, 1, 4096, 1>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
   }
   if (H <= 8192) return launch_rmsnorm_tma<6, 2, 8192, 1>(x, gamma, eps, M, H, q, s, rstd, y, err, st);
   const unsigned grid = grid_for((size_t)M, kThreads / 32, 8);
