@@ -759,8 +759,15 @@ __device__ __forceinline__ void gemm_body(const KParams<G>& kp) {
           for (int kb = 0; kb < nkb; ++kb, ++it, ++acc_it) {
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             const uint32_t b = acc_it % ACC_BUFS, bph = (acc_it / ACC_BUFS) & 1u;
-            if (!mbar_wait(&bars->tempty[b], bph ^ 1u, abort_flag, true) ||
-                !mbar_wait(&bars->full[s], ph, abort_flag, true)) {
+            // a free accumulator and a full operand stage; with uniform scales
+            // both are polled at once (each waited for alone only if needed):
+            // decode FProp +3 %, FProp and DGrad +0.5 - 1 %, while the
+            // promotion-bound WGrad measured 2 % slower that way
+            bool e_ok = false, f_ok = false;
+            if constexpr (!COLS)
+              mbar_try_wait2(smem_u32(&bars->tempty[b]), bph ^ 1u, smem_u32(&bars->full[s]), ph, e_ok, f_ok);
+            if (!((e_ok || mbar_wait(&bars->tempty[b], bph ^ 1u, abort_flag, true)) &&
+                  (f_ok || mbar_wait(&bars->full[s], ph, abort_flag, true)))) {
               fail();
               ok = false;
               break;
