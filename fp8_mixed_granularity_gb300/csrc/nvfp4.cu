@@ -205,7 +205,9 @@ constexpr int THREADS = 512;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = BN;                       // columns 0..255: the accumulator
 constexpr int SF_COLS = 4 * 4 + 4 * 8;             // per stage: SFA 4 × 4, SFB 4 × 8 columns
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 1024;
+// + per epilogue warp one row of its 128 column scales (gw), read back as broadcasts
+constexpr int GWS_BYTES = 8 * 128 * 4;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 1024 + GWS_BYTES;
 static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the 128-byte swizzle");
 static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -430,22 +432,31 @@ k_gemm_nvfp4_fprop(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
   } else if (warp >= 8) {
     // ---------------- epilogue ----------------
+    // The row's scale and this warp's 128 column scales are fetched before the
+    // accumulator is waited for (the column scales into the warp's own row of
+    // shared memory, read back as broadcasts); the 128 columns are converted to
+    // bf16 in registers and the accumulator is handed back to the tensor core
+    // before the stores, so the next tile's MMAs run under them.
     const uint32_t lq = (uint32_t)(warp & 3);
     const int half = (warp - 8) >> 2;            // columns [128·half, 128·half + 128)
+    float* gws = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 1024) + (warp - 8) * 128;
     uint32_t tj = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tj) {
       int mt, nt;
       tile_mn(a, tile, mt, nt);
-      const bool good = wait_or_abort(smem_addr(&bars->tfull), tj & 1u, bars, a.err);
-      if (!__all_sync(kFullMask, good)) break;
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int row = mt * BM + (int)lq * 32 + lane;
       const bool row_ok = row < a.M;
       const float gx = row_ok ? __ldg(a.gx + row) : 0.0f;
-      const float* gw = a.gw + (size_t)nt * BN;
-      uint16_t* yr = a.y + (size_t)(row_ok ? row : 0) * a.N + (size_t)nt * BN;
-#pragma unroll 1
-      for (int c0 = 128 * half; c0 < 128 * half + 128; c0 += 32) {
+      const float4 g4 = __ldg(reinterpret_cast<const float4*>(a.gw + (size_t)nt * BN + 128 * half) + lane);
+      __syncwarp();   // the previous tile's reads of the row are done
+      *reinterpret_cast<float4*>(gws + 4 * lane) = g4;
+      __syncwarp();
+      const bool good = wait_or_abort(smem_addr(&bars->tfull), tj & 1u, bars, a.err);
+      if (!__all_sync(kFullMask, good)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      uint32_t o[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
@@ -455,25 +466,27 @@ k_gemm_nvfp4_fprop(const __grid_constant__ CUtensorMap tmA, const __grid_constan
               "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
               "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
               "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-            : "r"(tmem + ((lq * 32u) << 16) + (uint32_t)c0));
+            : "r"(tmem + ((lq * 32u) << 16) + (uint32_t)(128 * half + 32 * c)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (row_ok) {
-          uint32_t o[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float2 w2 = __ldg(reinterpret_cast<const float2*>(gw + c0) + j);
-            const float v0 = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * j]), gx), w2.x);
-            const float v1 = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), gx), w2.y);
-            o[j] = f2_to_bf2(v0, v1);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(yr + c0);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        for (int j = 0; j < 16; ++j) {
+          const float2 w2 = *reinterpret_cast<const float2*>(gws + 32 * c + 2 * j);
+          const float v0 = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * j]), gx), w2.x);
+          const float v1 = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), gx), w2.y);
+          o[c][j] = f2_to_bf2(v0, v1);
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive_s(smem_addr(&bars->tempty));
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(a.y + (size_t)row * a.N + (size_t)nt * BN + 128 * half);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[4 * c + j] = make_uint4(o[c][4 * j], o[c][4 * j + 1], o[c][4 * j + 2], o[c][4 * j + 3]);
+      }
     }
   }
 
