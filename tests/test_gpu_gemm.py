@@ -186,6 +186,28 @@ def _stripes(n, rng, k=2, width=128):
     return np.concatenate([np.arange(s, s + width) for s in starts])
 
 
+def test_wgrad_many_tiles_odd_block_count(dev):
+    """More output tiles than SMs (48 × 4 = 192, so some CTAs take two) and five
+    128-token blocks per tile: the per-block column- and row-scale slots (eight
+    of them, taken in block order across the CTA's tiles) wrap inside a tile and
+    between tiles at odd places.  Sampled row and column stripes against the
+    oracle."""
+    M, N, K = 640, 6144, 1024
+    rng = np.random.default_rng(17)
+    x = W.device_activations(M, K, dev, seed=17)
+    dy = W.device_normal((M, N), 1e-3, dev, seed=18)
+    xq, sx = q_act(x, dev)
+    xqT, sxT = requant(xq, sx, dev)
+    _, _, dyqT, sdyT = q_grad(dy, dev)
+    dw = torch.empty(N, K, dtype=torch.float32, device=dev)
+    J.jetfp8_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw)
+    check_errors()
+    hdT, hsdT, hxT, hsxT = h(dyqT), h(sdyT), h(xqT), h(sxT)
+    n_rows, k_cols = _stripes(N, rng), _stripes(K, rng)
+    _assert_close(h(dw[n_rows]), O.gemm_wgrad(hdT, hsdT, hxT, hsxT, rows=n_rows), "wgrad rows")
+    _assert_close(h(dw[:, k_cols]), O.gemm_wgrad(hdT, hsdT, hxT, hsxT, cols=k_cols), "wgrad cols")
+
+
 @pytest.mark.parametrize(
     "lin",
     [l for l in W.llama8b_training() if l.name in ("gate_up", "down")]

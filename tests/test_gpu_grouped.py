@@ -84,6 +84,20 @@ def test_grouped_wgrad_narrow_tiles_odd_blocks_and_oracle(dev):
     assert torch.equal(one.view(torch.int32), ref[1].view(torch.int32))
 
 
+def test_grouped_wgrad_many_tiles_odd_block_count(dev):
+    """Two problems with 192 + 128 output tiles (more than the SMs) and five
+    128-token blocks each: the scale-ring slots wrap at odd places inside tiles,
+    between tiles and between problems; the grouped launch equals the single
+    launches bit for bit."""
+    M = 640
+    shapes = [(6144, 1024), (4096, 1024)]
+    ops = [_operands(dev, M, N, K, seed=70 + i) for i, (N, K) in enumerate(shapes)]
+    ref = _separate(ops, torch.float32, dev)
+    got = _grouped(ops, torch.float32, dev)
+    for i, (a, b) in enumerate(zip(got, ref)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32)), f"problem {i}"
+
+
 def test_grouped_wgrad_rejects_mixed_token_counts(dev):
     a = _operands(dev, 128, 128, 128, seed=70)
     b = _operands(dev, 256, 128, 128, seed=71)
