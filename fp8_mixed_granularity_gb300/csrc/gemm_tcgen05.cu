@@ -1413,9 +1413,10 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   if (dev >= 64) return cudaErrorInvalidDevice;
   // 128×256 tiles (two TMEM accumulators) where the output width allows, else
   // 128×128.  Uniform-scale GEMMs with fewer 128×256 tiles than SMs (decode-sized
-  // M) take the widest of 128 or 64 columns that gives every SM a tile, so more
-  // SMs stream the weights; the arithmetic of every output element (its MMA
-  // blocks and promotion order) does not depend on the tile width.
+  // M) take 128 columns, or 64 where 128-wide tiles leave SMs without one and the
+  // 64-wide ones still fit in one wave, so that more SMs stream the weights; the
+  // arithmetic of every output element (its MMA blocks and promotion order) does
+  // not depend on the tile width.
   const bool cols = a.b_mode == BScale::kColumn;
   if (use_pair(a)) return cols ? launch_pair<true, 1>(&a, 1, dev, st) : launch_pair<false, 1>(&a, 1, dev, st);
   if (cols)
@@ -1423,9 +1424,13 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   // the fused quantiser needs a thread's 128 columns to be a whole 1×128 group
   if (a.out_q != nullptr)
     return a.C % 256 == 0 ? launch_cfg<256, false, 1>(&a, 1, dev, st) : cudaErrorInvalidValue;
+  // (a decode batch of 256 rows on the 6144-wide QKV projection has 96 tiles of
+  // 128 columns but 192 of 64: a second wave of the serial K loop would cost more
+  // than the narrower tiles save)
   const int64_t tiles_m = (a.R + BM - 1) / BM, sms = num_sms();
   if (a.C % 256 == 0 && tiles_m * (a.C / 256) >= sms) return launch_cfg<256, false, 1>(&a, 1, dev, st);
-  if (a.C % 256 != 0 || tiles_m * (a.C / 128) >= sms) return launch_cfg<128, false, 1>(&a, 1, dev, st);
+  if (a.C % 256 != 0 || tiles_m * (a.C / 128) >= sms || tiles_m * (a.C / 64) > sms)
+    return launch_cfg<128, false, 1>(&a, 1, dev, st);
   return launch_cfg<64, false, 1>(&a, 1, dev, st);
 }
 
