@@ -1411,10 +1411,14 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  // 128×256 tiles (two TMEM accumulators) where the output width allows, else
-  // 128×128.  Uniform-scale GEMMs with fewer 128×256 tiles than SMs (decode-sized
-  // M) take 128 columns, or 64 where 128-wide tiles leave SMs without one and the
-  // 64-wide ones still fit in one wave, so that more SMs stream the weights; the
+  // Column scales: 128×256 tiles (two TMEM accumulators) where the output width
+  // allows, else 128×128.  Uniform scales: the tile width (256, 128 or 64
+  // columns) with the fewest waves of tiles over the SMs, the narrowest of equals
+  // — each CTA runs its tiles' K loops one after another, and narrower tiles put
+  // more SMs on the weights.  At the training shapes that is always 256 (the
+  // widest tiles read the fewest operand bytes per FLOP); a decode batch of 64
+  // rows takes 64 columns on the 6144-wide QKV projection (96 tiles) but 256 on
+  // the 24576-wide gate/up (96 tiles, where 128 would need two waves).  The
   // arithmetic of every output element (its MMA blocks and promotion order) does
   // not depend on the tile width.
   const bool cols = a.b_mode == BScale::kColumn;
@@ -1424,13 +1428,13 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   // the fused quantiser needs a thread's 128 columns to be a whole 1×128 group
   if (a.out_q != nullptr)
     return a.C % 256 == 0 ? launch_cfg<256, false, 1>(&a, 1, dev, st) : cudaErrorInvalidValue;
-  // (a decode batch of 256 rows on the 6144-wide QKV projection has 96 tiles of
-  // 128 columns but 192 of 64: a second wave of the serial K loop would cost more
-  // than the narrower tiles save)
   const int64_t tiles_m = (a.R + BM - 1) / BM, sms = num_sms();
-  if (a.C % 256 == 0 && tiles_m * (a.C / 256) >= sms) return launch_cfg<256, false, 1>(&a, 1, dev, st);
-  if (a.C % 256 != 0 || tiles_m * (a.C / 128) >= sms || tiles_m * (a.C / 64) > sms)
-    return launch_cfg<128, false, 1>(&a, 1, dev, st);
+  auto waves = [&](int64_t bn) { return (tiles_m * (a.C / bn) + sms - 1) / sms; };
+  int64_t bn = 128;   // C is a multiple of 128
+  if (a.C % 64 == 0 && waves(64) <= waves(bn)) bn = 64;
+  if (a.C % 256 == 0 && waves(256) < waves(bn)) bn = 256;
+  if (bn == 256) return launch_cfg<256, false, 1>(&a, 1, dev, st);
+  if (bn == 128) return launch_cfg<128, false, 1>(&a, 1, dev, st);
   return launch_cfg<64, false, 1>(&a, 1, dev, st);
 }
 
