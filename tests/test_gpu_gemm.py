@@ -77,8 +77,9 @@ def test_fprop_decode_tiles_bit_identical_to_training_tiles(dev):
     wq, sw, _ = q_weight(w, dev, with_t=False)
     xq, sx = q_act(x, dev)
     y_all = _fprop(dev, xq, sx, wq, sw)
-    # 1, 64, 128 and 192 rows run on 64-wide tiles, 2560 rows (20 × 8 tiles) on 128-wide
-    for lo, hi in [(0, 64), (4096, 4224), (8000, 8192), (17, 18), (2048, 4608)]:
+    # 1, 64, 128 and 192 rows run on 64-wide tiles, 1920 rows (15 × 8 tiles of 128
+    # columns in one wave, 15 × 16 of 64 in two) on 128-wide, 2560 rows on 256-wide
+    for lo, hi in [(0, 64), (4096, 4224), (8000, 8192), (17, 18), (2048, 3968), (2048, 4608)]:
         xq_s, sx_s = q_act(x[lo:hi], dev)
         y_s = _fprop(dev, xq_s, sx_s, wq, sw)
         assert torch.equal(y_s, y_all[lo:hi]), (lo, hi)
